@@ -1,0 +1,33 @@
+"""The cache write, restated plainly (oracle, test-only).
+
+Each decode step appends one token's K and V into the request's current block
+("How LLM Inference Serving Works", section "Putting It Together: The Life of
+a Request in vLLM"); the keys and values are stored once and never recomputed
+("What the KV Cache Is, and How Big It Gets").  The position a token lands in
+is given by a slot number: slot = physical_block * block_size + offset, and a
+negative slot marks a padding token that is not written.  The slot encoding
+and the pool layout [num_blocks, Hkv, bs, D] are not stated on the pages; they
+are the plainest reading of "a block table maps each logical block to a
+physical block" with fixed-size blocks.
+
+This is a bit copy: arrays of raw bf16 bit patterns go in and come out.
+"""
+import numpy as np
+
+
+def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, block_size,
+                      inplace=False):
+    """Write key[t], value[t] ([T, Hkv, D]) at slot_mapping[t] of the pools.
+
+    Returns the (k_cache, v_cache) pair that results; the inputs are copied
+    first unless ``inplace`` is set.
+    """
+    kc = k_cache if inplace else np.array(k_cache, copy=True)
+    vc = v_cache if inplace else np.array(v_cache, copy=True)
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        blk, off = divmod(int(slot), block_size)
+        kc[blk, :, off, :] = key[t]
+        vc[blk, :, off, :] = value[t]
+    return kc, vc
