@@ -1,0 +1,606 @@
+"""Benchmark of the paged decode hot path: one step = the cache write of the
+batch's new tokens followed by paged decode attention over every sequence.
+
+Default workload: the Llama 3.1 8B-shaped single-layer decode (batch 64, 32
+query / 8 KV heads, head_dim 128, bf16, 16-token blocks, contexts uniform in
+[128, 2048], blocks scattered over a pool 1.25x the need) with the cache write
+of the 64 new tokens.  Inputs are synthetic (paged_kv_cache_283_gb300.inputs).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                    [--workload {2,3,4,5}] [--attn {auto,decode,splitk}]
+
+Prints one JSON line.  ``value`` is achieved HBM GB/s of the whole step
+(algorithmic bytes: K/V of every context token read once, q/out, block
+tables, the new tokens' K/V read and written) over the device time of K
+steps, replayed as CUDA graphs with inputs resident in HBM and the pool
+rotated over replicas so that no step finds its K/V in L2.  ``roofline``
+reports the dominant kernel alone; ``e2e`` the same metric through the
+public API with host buffers and the copies inside the timed region;
+``cpu_baseline`` the float64 CPU oracle on one host core.
+
+``--impl reference`` times the CPU oracle (the only reference this method
+has) on the same workload and prints the same line with "impl": "reference".
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no
+collective on the data path); rank 0 prints.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode-attention achieved HBM GB/s (frac of ~8 TB/s) and seq-layers/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context only
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes (what one step must move at least once)
+
+def decode_bytes(ctx, num_seqs, hq, hkv, d, bs):
+    """K/V of every attended token + q + out + block-table entries + lengths."""
+    import numpy as np
+    ctx = np.asarray(ctx, dtype=np.int64)
+    kv = int(ctx.sum()) * hkv * d * 2 * 2
+    qo = 2 * num_seqs * hq * d * 2
+    tables = 4 * int((-(-ctx // bs)).sum()) + 4 * num_seqs
+    return kv + qo + tables
+
+
+def cache_write_bytes(num_tokens, hkv, d):
+    """Read the new tokens' K and V, write them into the pool, read the slots."""
+    return 2 * 2 * num_tokens * hkv * d * 2 + 8 * num_tokens
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        window = [r for r in rows if t0 <= r[0] <= t1]
+        used = "timed region"
+        if not window:
+            window = rows
+            used = "whole run (timed region shorter than the sampling period)"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = sorted(float(p[1]) for _, p in window if p[1].replace(".", "").isdigit())
+        mx = max((float(p[2]) for _, p in window if p[2].replace(".", "").isdigit()), default=None)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for _, p in window for n, v in zip(names, p[5:9]) if v == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx,
+                "reasons": reasons, "samples": len(window), "window": used}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (runs in a fresh process: no CUDA, one BLAS thread)
+
+def oracle_step_sample(idx, max_seconds, out_json=True):
+    """Times the float64 oracle on a bounded sample of the workload's step.
+
+    The sample is the first n sequences of the batch (cache write of their
+    new tokens + their decode), n grown until one sample takes >= 0.2 s or
+    covers the batch; repeated until ``max_seconds`` have passed.
+    Returns GB/s over the sample's algorithmic bytes.
+    """
+    import numpy as np
+
+    from oracle import attention as OA
+    from oracle import cache as OC
+    from oracle.allocator import BlockAllocatorModel
+    from paged_kv_cache_283_gb300 import inputs as I
+
+    w = I.workload(idx)
+    m = BlockAllocatorModel(w.num_blocks, w.block_size, w.free_order)
+    for b, n in enumerate(w.context_lens.tolist()):
+        m.add_seq(b)
+        m.reserve(b, n - 1)
+    slots = np.array([x[0] for x in m.append_slots(range(w.num_seqs))], dtype=np.int64)
+    tables = [m.block_table(b) for b in range(w.num_seqs)]
+
+    def run(nseq):
+        OC.reshape_and_cache(w.key[:nseq], w.value[:nseq], w.k_cache, w.v_cache, slots[:nseq],
+                             w.block_size, inplace=True)
+        for b in range(nseq):
+            OA.decode_sequence(w.q[b], w.k_cache, w.v_cache, tables[b], int(w.context_lens[b]),
+                               w.scale, w.block_size)
+
+    nseq = 1
+    while True:
+        t = time.perf_counter()
+        run(nseq)
+        dt = time.perf_counter() - t
+        if dt >= 0.2 or nseq >= w.num_seqs:
+            break
+        nseq = min(w.num_seqs, nseq * 2)
+    reps, total = 0, 0.0
+    while total < max_seconds or reps == 0:
+        t = time.perf_counter()
+        run(nseq)
+        total += time.perf_counter() - t
+        reps += 1
+    nbytes = decode_bytes(w.context_lens[:nseq], nseq, w.num_q_heads, w.num_kv_heads,
+                          w.head_dim, w.block_size) + cache_write_bytes(nseq, w.num_kv_heads,
+                                                                        w.head_dim)
+    res = {"value": nbytes * reps / total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": f"first {nseq} of {w.num_seqs} sequences of the step (cache write + "
+                     f"float64 decode), {reps} repetitions, {total:.1f} s",
+           "seconds_per_sample": total / reps, "seqs": nseq, "bytes_per_sample": nbytes}
+    if out_json:
+        print(json.dumps(res))
+    return res
+
+
+def cpu_baseline(idx, seconds):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import bench, sys; bench.oracle_step_sample(%d, %f)" % (idx, seconds))
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
+                       text=True, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+                "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle as it stands
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # one oracle sample per step, sized so that warmup + steps stay within ~2 minutes
+    probe = oracle_step_sample(args.workload, 0.0, out_json=False)
+    per = probe["seconds_per_sample"]
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    import math
+    from paged_kv_cache_283_gb300 import inputs as I
+    w = I.workload(args.workload, with_data=False)
+    nseq = max(1, min(probe["seqs"], int(math.floor(probe["seqs"] * budget / per))))
+    res = _reference_timed(args, nseq)
+    print(json.dumps(res))
+    return 0
+
+
+def _reference_timed(args, nseq):
+    import numpy as np
+
+    from oracle import attention as OA
+    from oracle import cache as OC
+    from oracle.allocator import BlockAllocatorModel
+    from paged_kv_cache_283_gb300 import inputs as I
+
+    w = I.workload(args.workload)
+    m = BlockAllocatorModel(w.num_blocks, w.block_size, w.free_order)
+    for b, n in enumerate(w.context_lens.tolist()):
+        m.add_seq(b)
+        m.reserve(b, n - 1)
+    slots = np.array([x[0] for x in m.append_slots(range(w.num_seqs))], dtype=np.int64)
+    tables = [m.block_table(b) for b in range(w.num_seqs)]
+
+    def step():
+        OC.reshape_and_cache(w.key[:nseq], w.value[:nseq], w.k_cache, w.v_cache, slots[:nseq],
+                             w.block_size, inplace=True)
+        for b in range(nseq):
+            OA.decode_sequence(w.q[b], w.k_cache, w.v_cache, tables[b], int(w.context_lens[b]),
+                               w.scale, w.block_size)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t
+    nbytes = decode_bytes(w.context_lens[:nseq], nseq, w.num_q_heads, w.num_kv_heads,
+                          w.head_dim, w.block_size) + cache_write_bytes(nseq, w.num_kv_heads,
+                                                                        w.head_dim)
+    value = nbytes * args.steps / dt / 1e9
+    threads = os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample_seqs": nseq, "batch": w.num_seqs},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                             "cores": int(threads) if threads.isdigit() else threads,
+                             "sample": f"first {nseq} of {w.num_seqs} sequences per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+
+def _setup(idx, device, replicas_min_bytes):
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_283_gb300 import inputs as I
+    from paged_kv_cache_283_gb300 import pa
+
+    w = I.workload(idx)
+    alloc = pa.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    seqs = list(range(w.num_seqs))
+    if idx == 4:
+        alloc.add_seq(-1)
+        alloc.reserve(-1, w.prefix_len)
+        for b, s in enumerate(w.suffix_lens.tolist()):
+            alloc.fork(-1, b)
+            alloc.reserve(b, s - 1)
+        alloc.free_seq(-1)
+    else:
+        for b, n in enumerate(w.context_lens.tolist()):
+            alloc.add_seq(b)
+            alloc.reserve(b, n - 1)
+    slots, cow_src, _ = alloc.append_slots(seqs)
+    assert np.all(cow_src == -1)
+    bt, ctx = alloc.block_tables(seqs, w.max_blocks_per_seq)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(
+            torch.bfloat16)
+
+    pool_bytes = 2 * w.k_cache.nbytes
+    layers = w.layers
+    if layers > 1:
+        # one pool per layer, each a seeded block permutation of the base pool
+        base_k, base_v = bf(w.k_cache), bf(w.v_cache)
+        pools = []
+        for layer in range(layers):
+            order = torch.from_numpy(I.layer_block_order(w, layer)).to(device)
+            pools.append((base_k.index_select(0, order), base_v.index_select(0, order)))
+        del base_k, base_v
+        per_layer = [I.layer_inputs(w, layer) for layer in range(layers)]
+        qs = [bf(x[0]) for x in per_layer]
+        keys = [bf(x[1]) for x in per_layer]
+        vals = [bf(x[2]) for x in per_layer]
+        replicas = [pools]
+    else:
+        nrep = max(2, -(-replicas_min_bytes // pool_bytes))
+        k0, v0 = bf(w.k_cache), bf(w.v_cache)
+        replicas = [[(k0, v0)]] + [[(k0.clone(), v0.clone())] for _ in range(nrep - 1)]
+        qs, keys, vals = [bf(w.q)], [bf(w.key)], [bf(w.value)]
+    st = {
+        "w": w, "bt": torch.from_numpy(bt).to(device), "ctx": torch.from_numpy(ctx).to(device),
+        "slots": torch.from_numpy(slots).to(device), "replicas": replicas, "q": qs,
+        "key": keys, "value": vals, "bt_host": bt, "ctx_host": ctx, "slots_host": slots,
+        "pool_bytes": pool_bytes,
+    }
+    return st
+
+
+def _attn_fns(st, attn, partition):
+    import torch
+
+    from paged_kv_cache_283_gb300 import pa
+
+    w = st["w"]
+    outs = [torch.empty_like(q) for q in st["q"]]
+    ws = None
+    if attn == "splitk":
+        ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
+                                 int(w.context_lens.max()), partition, st["q"][0].device)
+
+    def attend(layer, kc, vc):
+        if attn == "splitk":
+            pa.pa_decode_splitk(*ws, st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale,
+                                partition_size=partition)
+            pa.pa_splitk_reduce(outs[layer], *ws, st["ctx"], partition_size=partition)
+        else:
+            pa.pa_decode(outs[layer], st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale)
+
+    def dominant(layer, kc, vc):
+        if attn == "splitk":
+            pa.pa_decode_splitk(*ws, st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale,
+                                partition_size=partition)
+        else:
+            pa.pa_decode(outs[layer], st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale)
+
+    def step(r):
+        for layer, (kc, vc) in enumerate(st["replicas"][r]):
+            pa.pa_reshape_and_cache(st["key"][layer], st["value"][layer], kc, vc, st["slots"])
+            attend(layer, kc, vc)
+
+    return step, dominant, outs
+
+
+def _capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    return g
+
+
+def _time_graphs(graphs, count, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for k in range(count):
+            graphs[k % len(graphs)].replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / 1e3
+
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from paged_kv_cache_283_gb300 import pa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        print(f"bench: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
+    base = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(args.workload, args.cpu_seconds)
+    if world > 1:
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    from paged_kv_cache_283_gb300 import build as _b
+    _b.build()
+    pa.lib()
+    pa.pa_clear_device_error()
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    props = torch.cuda.get_device_properties(device)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    st = _setup(args.workload, device, 4 * l2)
+    w = st["w"]
+    stream = torch.cuda.Stream(device)
+    attn = args.attn
+    if attn == "auto":
+        attn = "splitk" if args.workload in (2, 3) else "decode"
+    step, dominant, outs = _attn_fns(st, attn, args.partition)
+
+    # eager warmup (sets kernel attributes, checks the error word)
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            step(k % len(st["replicas"]))
+    stream.synchronize()
+    assert pa.pa_get_device_error() == 0, "device error word set during warmup"
+
+    graphs = [_capture(lambda r=r: step(r), stream) for r in range(len(st["replicas"]))]
+    launches_per_step = w.layers * (2 if attn == "decode" else 3)
+
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    # soak so that the clock sampler sees the GPU under this load
+    soak = 0.0
+    while soak < args.soak_seconds:
+        soak += _time_graphs(graphs, 200, stream)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    dt = _time_graphs(graphs, args.steps, stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+
+    # dominant kernel alone: graphs of back-to-back launches over the replicas
+    def dom_all(r):
+        for layer, (kc, vc) in enumerate(st["replicas"][r]):
+            dominant(layer, kc, vc)
+    dom_graphs = [_capture(lambda r=r: dom_all(r), stream) for r in range(len(st["replicas"]))]
+    _time_graphs(dom_graphs, 20, stream)
+    n_dom = max(args.steps, 50)
+    dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * w.layers)
+
+    # end to end through the public API with pinned host buffers
+    e2e = _e2e(st, attn, args, stream)
+    assert pa.pa_get_device_error() == 0, "device error word set during the run"
+
+    step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
+                                          w.num_kv_heads, w.head_dim, w.block_size)
+                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim))
+    dom_bytes = decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                             w.head_dim, w.block_size)
+    times = torch.tensor([dt], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    dt_max = float(times.item())
+    value = world * step_bytes * args.steps / dt_max / 1e9
+    hbm_peak = peaks.get("hbm_gbs")
+    achieved = dom_bytes / dom_dt / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak if hbm_peak else 6800.0, "unit": "GB/s",
+                "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
+                "traffic": args.traffic,
+                "kernel": "pa_decode_splitk" if attn == "splitk" else "pa_decode",
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
+                else "fallback 6.8 TB/s",
+                "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_dt * 1e6, 2)}
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {
+            "workload": w.name, "batch": w.num_seqs, "layers": w.layers,
+            "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "num_blocks": w.num_blocks,
+            "mean_context": float(np.mean(w.context_lens)), "new_tokens_per_step": w.num_seqs,
+            "attention": ("pa_decode_splitk+pa_splitk_reduce, partition %d" % args.partition)
+            if attn == "splitk" else "pa_decode",
+            "graph": "one CUDA graph per step (cache write + attention)",
+            "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
+                  % (len(st["replicas"]), st["pool_bytes"] / 1e6, l2 / 1e6)
+            if len(st["replicas"]) > 1 else "32 distinct per-layer pools per step",
+            "parallelism": "dp%d (independent sequences per GPU)" % world,
+        },
+        "seq_layers_per_s": round(world * w.num_seqs * w.layers * args.steps / dt_max, 1),
+        "tokens_per_s": round(world * w.num_seqs * args.steps / dt_max, 1),
+        "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+        "frac_of_measured_hbm": round(value / world / hbm_peak, 4) if hbm_peak else None,
+        "bytes_per_step": step_bytes,
+        "roofline": roofline,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if base is not None:
+        res["cpu_baseline"] = base
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def _e2e(st, attn, args, stream):
+    """Same metric through the public API: pinned host inputs copied in, the
+    step's output copied out, every step, inside the timed region."""
+    import torch
+
+    from paged_kv_cache_283_gb300 import pa
+
+    w = st["w"]
+    dev = st["bt"].device
+    host = {
+        "q": [x.cpu().pin_memory() for x in st["q"]],
+        "key": [x.cpu().pin_memory() for x in st["key"]],
+        "value": [x.cpu().pin_memory() for x in st["value"]],
+        "slots": st["slots"].cpu().pin_memory(), "bt": st["bt"].cpu().pin_memory(),
+        "ctx": st["ctx"].cpu().pin_memory(),
+    }
+    dq = [torch.empty_like(x) for x in st["q"]]
+    dkey = [torch.empty_like(x) for x in st["key"]]
+    dval = [torch.empty_like(x) for x in st["value"]]
+    dslots, dbt, dctx = (torch.empty_like(st["slots"]), torch.empty_like(st["bt"]),
+                         torch.empty_like(st["ctx"]))
+    out = [torch.empty_like(x) for x in st["q"]]
+    hout = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in st["q"]]
+    ws = None
+    if attn == "splitk":
+        ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
+                                 int(w.context_lens.max()), args.partition, dev)
+    h2d = (sum(x.numel() * 2 for x in host["q"] + host["key"] + host["value"])
+           + host["slots"].numel() * 8 + host["bt"].numel() * 4 + host["ctx"].numel() * 4)
+    d2h = sum(x.numel() * 2 for x in hout)
+
+    def one(r):
+        dslots.copy_(host["slots"], non_blocking=True)
+        dbt.copy_(host["bt"], non_blocking=True)
+        dctx.copy_(host["ctx"], non_blocking=True)
+        for layer, (kc, vc) in enumerate(st["replicas"][r]):
+            dq[layer].copy_(host["q"][layer], non_blocking=True)
+            dkey[layer].copy_(host["key"][layer], non_blocking=True)
+            dval[layer].copy_(host["value"][layer], non_blocking=True)
+            pa.pa_reshape_and_cache(dkey[layer], dval[layer], kc, vc, dslots)
+            if attn == "splitk":
+                pa.pa_decode_splitk(*ws, dq[layer], kc, vc, dbt, dctx, w.scale,
+                                    partition_size=args.partition)
+                pa.pa_splitk_reduce(out[layer], *ws, dctx, partition_size=args.partition)
+            else:
+                pa.pa_decode(out[layer], dq[layer], kc, vc, dbt, dctx, w.scale)
+            hout[layer].copy_(out[layer], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            one(k % len(st["replicas"]))
+        stream.synchronize()
+        n = args.steps
+        t = time.perf_counter()
+        for k in range(n):
+            one(k % len(st["replicas"]))
+        stream.synchronize()
+        dt = time.perf_counter() - t
+    step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
+                                          w.num_kv_heads, w.head_dim, w.block_size)
+                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim))
+    return {"value": round(step_bytes * n / dt / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": dt / n * 1e3,
+            "how": "eager public-API calls (ctypes), pinned host buffers, copies on the "
+                   "launch stream, wall clock around all steps"}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])
+    ap.add_argument("--partition", type=int, default=512)
+    ap.add_argument("--soak-seconds", type=float, default=0.5)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,262 @@
+/*
+ * pa.h -- C ABI of libpa.so: PagedAttention decode on GB300 (sm_103a).
+ *
+ * Two device operations make up the decode hot path, plus a host-side block
+ * allocator that produces their index inputs:
+ *
+ *   pa_reshape_and_cache   write each new token's K and V into the block pool
+ *   pa_decode              single-query grouped-query attention over each
+ *                          sequence's blocks, found through its block table
+ *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
+ *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
+ *   pa_alloc_*             fixed-size block allocator with reference counts
+ *                          and copy-on-write (host only, never on the GPU path)
+ *
+ * Passages these follow (page title, section):
+ *   [KV]   "How LLM Inference Serving Works: KV Cache, PagedAttention and
+ *          Continuous Batching", section "What the KV Cache Is, and How Big It
+ *          Gets" -- each decode step compares the new token's query with the
+ *          keys of the earlier tokens and mixes their values; K and V are
+ *          cached per token; 32 query heads share 8 KV heads (GQA).
+ *   [PA]   same page, "PagedAttention: Virtual Memory for the KV Cache" --
+ *          fixed-size blocks, a block table from logical to physical blocks,
+ *          blocks allocated on demand, the attention kernel follows the table.
+ *   [SH]   same page, "Sharing comes for free" -- blocks shared by several
+ *          tables with reference counts, copied only when a branch writes.
+ *   [LIFE] same page, "Putting It Together: The Life of a Request in vLLM" --
+ *          each decode step appends one token's K and V into the request's
+ *          current block; a new block only when that block fills; counts
+ *          drop when the request ends.
+ *   [OOM]  same page, "When memory runs out anyway" -- when blocks run out
+ *          the engine preempts a request.
+ *   [WALK] "LLM serving (vLLM, quantized inference): Visual walkthrough",
+ *          Steps 7-8 -- block_size 16, at most block_size-1 slots wasted,
+ *          shared prefixes stored once.
+ *
+ * Conventions shared by every device entry point:
+ *   - Pointers named *_cache, q, out, key, value, ws_* and the index arrays
+ *     are DEVICE pointers owned by the caller.  The library allocates no
+ *     device memory on these paths and keeps no pointer after returning.
+ *   - Element types: K/V/q/out/key/value are bf16 (2 bytes, stored as raw
+ *     bits); the split-K workspace is fp32; block tables and context lengths
+ *     are int32; slots are int64.
+ *   - Layouts (row-major, contiguous):
+ *       k_cache, v_cache : [num_blocks, num_kv_heads, block_size, head_dim]
+ *       q, out           : [num_seqs, num_q_heads, head_dim]
+ *       key, value       : [num_tokens, num_kv_heads, head_dim]
+ *       slot_mapping     : [num_tokens]; slot = block * block_size + offset;
+ *                          a negative slot means "skip this token"
+ *       block_tables     : [num_seqs, max_blocks_per_seq]; entry j of row b
+ *                          is the physical block holding tokens
+ *                          [j*block_size, (j+1)*block_size) of sequence b
+ *       context_lens     : [num_seqs]; tokens attended by sequence b, i.e.
+ *                          positions [0, context_lens[b]) (the new token,
+ *                          written first by pa_reshape_and_cache, included)
+ *     Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *   - Alignment: bf16 and fp32 arrays 16-byte aligned; int32 arrays 4-byte;
+ *     int64 arrays 8-byte.  A misaligned pointer is PA_ERR_INVALID_ARG.
+ *   - All work is enqueued asynchronously on `stream`; a return of PA_OK
+ *     means the launch was accepted, not that the kernel has finished.
+ *   - Arguments are checked on the host before any launch.  Values that
+ *     live in device memory (block ids, context lengths, slots) are checked
+ *     by the kernels: an out-of-range value sets a bit in a per-device error
+ *     word (pa_get_device_error) and is never dereferenced -- a bad block id
+ *     reads block 0 instead, a bad slot is not written, a context length
+ *     beyond max_blocks_per_seq * block_size is clamped.  Kernels never trap.
+ *   - No C++ exception crosses this ABI.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* pa_stream_t;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,       /* null / misaligned pointer, bad size, unknown sequence */
+  PA_ERR_UNSUPPORTED_SHAPE = 2, /* a (head_dim, group, block_size) with no compiled kernel */
+  PA_ERR_OUT_OF_BLOCKS = 3,     /* allocator: too few free blocks; state unchanged */
+  PA_ERR_CUDA = 4               /* a CUDA runtime call or launch failed */
+} pa_status;
+
+/* Bits of the per-device error word written by the kernels. */
+#define PA_DEVERR_BLOCK_ID 0x1u     /* block table entry outside [0, num_blocks) */
+#define PA_DEVERR_CONTEXT_LEN 0x2u  /* context length < 0 or > max_blocks_per_seq*block_size */
+#define PA_DEVERR_SLOT 0x4u         /* slot >= num_blocks * block_size */
+#define PA_DEVERR_WAIT_TIMEOUT 0x8u /* an asynchronous copy did not complete in time */
+
+/* Static description of a status code; never NULL. */
+const char* pa_status_string(pa_status status);
+
+/* Text of the last CUDA error seen by this thread inside the library
+ * ("" if none).  Valid until the next call from the same thread. */
+const char* pa_last_cuda_error(void);
+
+/* Reads the error word of the current device into *bits (0 = no error).
+ * Synchronises the device.  PA_ERR_INVALID_ARG if bits is NULL. */
+pa_status pa_get_device_error(unsigned* bits);
+
+/* Resets the current device's error word to 0 (synchronous). */
+pa_status pa_clear_device_error(void);
+
+/* PA_OK if pa_decode / pa_decode_splitk have a kernel for this shape:
+ * block_size 16, head_dim in {64, 128}, num_q_heads / num_kv_heads in
+ * {2, 4, 8}; otherwise PA_ERR_UNSUPPORTED_SHAPE (or PA_ERR_INVALID_ARG for
+ * non-positive or non-divisible values). */
+pa_status pa_decode_supported(int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size);
+
+/*
+ * Cache write [KV], [LIFE]: for every t in [0, num_tokens) with
+ * s = slot_mapping[t] >= 0,
+ *   k_cache[s / block_size, h, s % block_size, :] = key[t, h, :]
+ *   v_cache[s / block_size, h, s % block_size, :] = value[t, h, :]
+ * for every KV head h.  A bit copy.  Slots must be distinct (two tokens
+ * writing one slot race).  head_dim must be a multiple of 8; num_tokens == 0
+ * is a no-op.
+ */
+pa_status pa_reshape_and_cache(const void* key, const void* value,
+                               void* k_cache, void* v_cache,
+                               const int64_t* slot_mapping, int num_tokens,
+                               int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, pa_stream_t stream);
+
+/*
+ * Paged decode attention [KV], [PA]: for every sequence b and query head h
+ * (g = h / (num_q_heads / num_kv_heads), n = context_lens[b]),
+ *   s_j   = scale * dot(q[b, h, :], K_j),   K_j = k_cache[tbl(j), g, j % bs, :]
+ *   out[b, h, :] = sum_j softmax(s)_j * V_j over j in [0, n),
+ * with tbl(j) = block_tables[b * max_blocks_per_seq + j / bs], fp32
+ * accumulation, bf16 output rounded to nearest even.  n == 0 gives zeros.
+ * One CTA per (sequence, KV head) reads each K/V block once for all the
+ * query heads of its group.  No workspace.
+ */
+pa_status pa_decode(void* out, const void* q, const void* k_cache,
+                    const void* v_cache, const int32_t* block_tables,
+                    int max_blocks_per_seq, const int32_t* context_lens,
+                    int num_seqs, int num_q_heads, int num_kv_heads,
+                    int head_dim, int block_size, int num_blocks, float scale,
+                    pa_stream_t stream);
+
+/* Bytes of fp32 workspace pa_decode_splitk needs for contexts up to
+ * max_context_len: ws_out [B, Hq, P, D] + ws_m [B, Hq, P] + ws_l [B, Hq, P]
+ * with P = ceil(max_context_len / partition_size).  0 on invalid input. */
+size_t pa_splitk_workspace_bytes(int num_seqs, int num_q_heads, int head_dim,
+                                 int max_context_len, int partition_size);
+
+/*
+ * Split-K partition pass: the decode above restricted to partition p, i.e.
+ * tokens [p * partition_size, min(n, (p + 1) * partition_size)), for every
+ * p < ceil(n / partition_size).  Writes, at index [b, h, p] (row stride
+ * max_partitions):
+ *   ws_m  = max_j s_j                       (natural-log units)
+ *   ws_l  = sum_j exp(s_j - ws_m)
+ *   ws_out[.., :] = sum_j exp(s_j - ws_m) * V_j / ws_l
+ * Partitions at or beyond ceil(n / partition_size) are not written.
+ * partition_size must be a positive multiple of block_size, and every
+ * context length must satisfy ceil(n / partition_size) <= max_partitions
+ * (else PA_DEVERR_CONTEXT_LEN and the excess is dropped).
+ */
+pa_status pa_decode_splitk(float* ws_out, float* ws_m, float* ws_l,
+                           int max_partitions, const void* q,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* block_tables, int max_blocks_per_seq,
+                           const int32_t* context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int num_blocks, float scale,
+                           int partition_size, pa_stream_t stream);
+
+/*
+ * Log-sum-exp merge of the partitions written by pa_decode_splitk:
+ *   M = max_p ws_m[b,h,p],  w_p = ws_l[b,h,p] * exp(ws_m[b,h,p] - M),
+ *   out[b, h, :] = sum_p w_p * ws_out[b,h,p,:] / sum_p w_p   (bf16),
+ * over p < ceil(context_lens[b] / partition_size); zeros if n == 0.
+ * Arguments must match the pa_decode_splitk call that filled the workspace.
+ */
+pa_status pa_splitk_reduce(void* out, const float* ws_out, const float* ws_m,
+                           const float* ws_l, int max_partitions,
+                           const int32_t* context_lens, int num_seqs,
+                           int num_q_heads, int head_dim, int partition_size,
+                           pa_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Host block allocator [PA], [SH], [LIFE], [OOM], [WALK].  Not thread-safe;
+ * one allocator per caller thread or external locking.  Deterministic: the
+ * free list is first-in first-out, seeded with initial_free_order (NULL means
+ * 0, 1, ..., num_blocks-1); a sequence's freed blocks go to the tail in its
+ * logical order.  Every call that fails leaves the allocator unchanged.
+ * Slot of position pos of a sequence: table[pos / bs] * bs + pos % bs. */
+typedef struct pa_alloc pa_alloc;
+
+/* Creates an allocator over num_blocks blocks of block_size tokens.
+ * initial_free_order, if not NULL, must be a permutation of [0, num_blocks). */
+pa_status pa_alloc_create(int num_blocks, int block_size,
+                          const int32_t* initial_free_order, pa_alloc** out);
+void pa_alloc_destroy(pa_alloc* a);
+
+/* Registers an empty sequence.  PA_ERR_INVALID_ARG if seq_id exists. */
+pa_status pa_alloc_add_seq(pa_alloc* a, int seq_id);
+
+/* Appends one token.  *slot_out receives its slot.  A new block is taken
+ * when the token opens a block; when it lands in a partly filled block
+ * shared with another sequence (reference count > 1), the sequence moves to
+ * a fresh block first and *cow_src / *cow_dst receive the (old, new) block
+ * ids, whose first pos % bs token rows the caller must copy; otherwise both
+ * are -1.  cow_src / cow_dst may be NULL.  PA_ERR_OUT_OF_BLOCKS if a block is
+ * needed and none is free. */
+pa_status pa_alloc_append_slot(pa_alloc* a, int seq_id, int64_t* slot_out,
+                               int32_t* cow_src, int32_t* cow_dst);
+
+/* One append for each of n distinct sequences, all or nothing: slots_out[i],
+ * cow_src[i], cow_dst[i] as pa_alloc_append_slot for seq_ids[i]
+ * (cow arrays may be NULL). */
+pa_status pa_alloc_append_slots(pa_alloc* a, const int* seq_ids, int n,
+                                int64_t* slots_out, int32_t* cow_src,
+                                int32_t* cow_dst);
+
+/* Appends num_tokens tokens to one sequence, all or nothing (a prompt).
+ * Only the first append can need a copy; its pair goes to cow_src/cow_dst. */
+pa_status pa_alloc_reserve(pa_alloc* a, int seq_id, int num_tokens,
+                           int32_t* cow_src, int32_t* cow_dst);
+
+/* child_id becomes a copy of parent_id sharing all its blocks (+1 reference
+ * each).  PA_ERR_INVALID_ARG if parent is unknown or child exists. */
+pa_status pa_alloc_fork(pa_alloc* a, int parent_id, int child_id);
+
+/* Drops the sequence; blocks whose count reaches 0 return to the free tail. */
+pa_status pa_alloc_free_seq(pa_alloc* a, int seq_id);
+
+/* Copies the sequence's block table (its first min(cap, length) entries) to
+ * out and its length to *n_out.  out may be NULL when cap == 0. */
+pa_status pa_alloc_block_table(const pa_alloc* a, int seq_id, int32_t* out,
+                               int cap, int* n_out);
+
+/* Fills a padded table [n, max_blocks] (entries past a sequence's length are
+ * -1) and, if ctx_out is not NULL, its token count per sequence.
+ * PA_ERR_INVALID_ARG if a table is longer than max_blocks. */
+pa_status pa_alloc_block_tables(const pa_alloc* a, const int* seq_ids, int n,
+                                int32_t* out, int max_blocks, int32_t* ctx_out);
+
+/* Tokens held by a sequence, or -1 if unknown. */
+int64_t pa_alloc_seq_len(const pa_alloc* a, int seq_id);
+/* Reference count of a block, or -1 if out of range. */
+int pa_alloc_refcount(const pa_alloc* a, int block);
+int pa_alloc_num_free(const pa_alloc* a);
+int pa_alloc_num_blocks(const pa_alloc* a);
+/* Copies the free list, head first (at most cap entries); *n_out = its size. */
+pa_status pa_alloc_free_list(const pa_alloc* a, int32_t* out, int cap, int* n_out);
+/* Empty slots in the sequence's last block, or -1 if unknown [WALK]. */
+int pa_alloc_tail_waste(const pa_alloc* a, int seq_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

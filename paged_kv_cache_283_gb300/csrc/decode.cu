@@ -1,0 +1,545 @@
+// Paged decode attention (plain and split-K) and the split-K merge, sm_103a.
+//
+// What is computed: "How LLM Inference Serving Works" (dev.to), sections
+// "What the KV Cache Is, and How Big It Gets" (the new token's query against
+// every cached key, a softmax-weighted mix of the cached values; 32 query
+// heads share 8 KV heads) and "PagedAttention: Virtual Memory for the KV
+// Cache" (the kernel follows the block table to wherever each block lives).
+// Decode is memory-bound ("Two Phases: Prefill and Decode"), so the design
+// is about moving each K/V byte from HBM exactly once at full bandwidth:
+//
+//  * One CTA per (sequence, KV head[, partition]).  All G query heads of the
+//    group are evaluated against each K/V block while it sits in shared
+//    memory, so the block is read from HBM once, not G times.
+//  * Pool layout [num_blocks, Hkv, 16, D] makes one (block, head) tile a
+//    contiguous 16*D*2-byte run (4 KiB at D = 128).  Each warp runs its own
+//    S-stage ring of such tiles, filled by single-instruction bulk async
+//    copies (cp.async.bulk, completion counted on an mbarrier) with an
+//    evict-first L2 policy; the warps of a CTA take the sequence's blocks
+//    round-robin and never wait on one another until the final merge.
+//  * Compute is CUDA-core fp32 (packed f32x2 FMAs): lane (row group rg, sub
+//    s) owns dims [8s, 8s+8) of tokens rg, rg+ROWS, ...  QK partial dots are
+//    finished by a transposing butterfly (each level halves the values a
+//    lane holds), which leaves every lane with R complete scores of one
+//    head; the softmax is online per warp in base-2 units (q is pre-scaled
+//    by scale*log2 e); P is handed to the PV loop through a 256-byte smem
+//    buffer; warps merge (m, l, acc) through shared memory at the end.
+//  * Split-K writes per-partition (m, l, o/l) in fp32; a second small kernel
+//    merges partitions by the log-sum-exp identity.
+//  * Every device-resident index is checked: bad block ids read block 0 and
+//    set PA_DEVERR_BLOCK_ID; bad context lengths are clamped; every mbarrier
+//    wait is bounded.  Nothing traps.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <atomic>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kBlockSize = 16;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int G>
+struct Geometry {
+  static constexpr int BS = kBlockSize;
+  static constexpr int L = D / 8;         // lanes per K/V row, 16 bytes each
+  static constexpr int ROWS = 32 / L;     // rows one warp-wide 16-byte load covers
+  static constexpr int P = BS / ROWS;     // passes over a tile
+  static constexpr int NV = P * G;        // partial dot products per lane
+  static constexpr int R = NV / L;        // complete scores per lane after the butterfly
+  static constexpr int HEAD_LANES = P / R;  // sub-lanes holding one head's scores
+  static constexpr int TILE = BS * D * 2;   // bytes of one (block, KV head) tile
+  static_assert(32 % L == 0 && BS % ROWS == 0, "row geometry");
+  static_assert(NV % L == 0 && R >= 1 && P % R == 0, "score geometry");
+};
+
+// Pipeline shape per head_dim: warps per CTA and stages per warp.
+template <int D>
+struct Pipe;
+template <>
+struct Pipe<128> {
+  static constexpr int NW = 4;
+  static constexpr int S = 3;
+};
+template <>
+struct Pipe<64> {
+  static constexpr int NW = 4;
+  static constexpr int S = 4;
+};
+
+template <int D, int G, int NW, int S>
+struct SmemLayout {
+  using Geo = Geometry<D, G>;
+  static constexpr int TILES = S * 2 * Geo::TILE;  // per stage: K tile then V tile
+  static constexpr int PS = Geo::BS * G * 4;       // softmax weights of one tile
+  static constexpr int ALPHA = ((G * 4 + 15) / 16) * 16;
+  static constexpr int BARS = S * 8;
+  static constexpr int MERGE = (G * D + 2 * G) * 4;  // aliases TILES after the loop
+  static constexpr int WARP = ((TILES + PS + ALPHA + BARS + 127) / 128) * 128;
+  static constexpr int TOTAL = NW * WARP;
+  static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
+};
+
+// One K/V tile through QK, the online softmax update and PV.
+template <int D, int G, bool FULL>
+__device__ __forceinline__ void tile_step(const uint4* __restrict__ kt, const uint4* __restrict__ vt,
+                                          float* ps, float* alpha_s, const float2 (&q2)[G][4],
+                                          float2 (&acc)[G][4], float& m_run, float& l_run,
+                                          int nvalid, int lane, int sub, int rg, int my_head,
+                                          int my_i0) {
+  using Geo = Geometry<D, G>;
+  constexpr int L = Geo::L, ROWS = Geo::ROWS, P = Geo::P, NV = Geo::NV, R = Geo::R;
+
+  // QK: partial dots over this lane's 8 dims, value index g * P + i.
+  float sc[NV];
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int t = i * ROWS + rg;
+    const uint4 w = kt[t * L + sub];
+    const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+    const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 a = __fmul2_rn(q2[g][0], k0);
+      a = __ffma2_rn(q2[g][1], k1, a);
+      a = __ffma2_rn(q2[g][2], k2, a);
+      a = __ffma2_rn(q2[g][3], k3, a);
+      sc[g * P + i] = a.x + a.y;
+    }
+  }
+
+  // Transposing butterfly across the L lanes of a row: at each level a lane
+  // keeps one half of its values (upper half if its mask bit is set), adds
+  // the partner's copy of that half, and sends the other half away.  After
+  // log2(L) levels lane `sub` holds values [sub*R, sub*R + R), complete.
+#pragma unroll
+  for (int m = L / 2, n = NV; m >= 1; m >>= 1, n >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = up ? sc[k] : sc[k + n / 2];
+      const float keep = up ? sc[k + n / 2] : sc[k];
+      sc[k] = keep + __shfl_xor_sync(kFullMask, send, m);
+    }
+  }
+
+  // Online softmax for this lane's head (all lanes of a head agree on m_run).
+  float s[R];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int t = (my_i0 + r) * ROWS + rg;
+    s[r] = (FULL || t < nvalid) ? sc[r] : -INFINITY;
+    mx = fmaxf(mx, s[r]);
+  }
+#pragma unroll
+  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+#pragma unroll
+  for (int m = L; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+  const float m_new = fmaxf(m_run, mx);  // finite: every tile has a valid token
+  const float alpha = exp2f(m_run - m_new);
+  float psum = 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const float pr = exp2f(s[r] - m_new);
+    psum += pr;
+    ps[((my_i0 + r) * ROWS + rg) * G + my_head] = pr;
+  }
+  l_run = l_run * alpha + psum;
+  m_run = m_new;
+  if (sub % Geo::HEAD_LANES == 0 && rg == 0) alpha_s[my_head] = alpha;
+  const bool rescale = __any_sync(kFullMask, alpha != 1.0f);
+  __syncwarp();
+
+  if (rescale) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float a = alpha_s[g];
+      const float2 a2 = make_float2(a, a);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[g][k] = __fmul2_rn(acc[g][k], a2);
+    }
+  }
+
+  // PV: acc[g][dims] += p[t][g] * V[t][dims] for this lane's tokens.
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int t = i * ROWS + rg;
+    if (FULL || t < nvalid) {
+      const uint4 w = vt[t * L + sub];
+      const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
+      const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
+      float pw[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int g = 0; g < G; g += 4) {
+          const float4 x = *reinterpret_cast<const float4*>(ps + t * G + g);
+          pw[g] = x.x;
+          pw[g + 1] = x.y;
+          pw[g + 2] = x.z;
+          pw[g + 3] = x.w;
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < G; g += 2) {
+          const float2 x = *reinterpret_cast<const float2*>(ps + t * G + g);
+          pw[g] = x.x;
+          pw[g + 1] = x.y;
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float2 pp = make_float2(pw[g], pw[g]);
+        acc[g][0] = __ffma2_rn(pp, v0, acc[g][0]);
+        acc[g][1] = __ffma2_rn(pp, v1, acc[g][1]);
+        acc[g][2] = __ffma2_rn(pp, v2, acc[g][2]);
+        acc[g][3] = __ffma2_rn(pp, v3, acc[g][3]);
+      }
+    }
+  }
+}
+
+template <int D, int G, int NW, int S, bool SPLIT>
+__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
+  using Geo = Geometry<D, G>;
+  using Lay = SmemLayout<D, G, NW, S>;
+  constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
+  extern __shared__ __align__(128) unsigned char smem[];
+
+  const int kvh = blockIdx.x;
+  const int b = blockIdx.y;
+  const int part = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int sub = lane % L;
+  const int rg = lane / L;
+
+  // Context length lives in device memory: check it here.
+  int ctx = p.context_lens[b];
+  const int ctx_cap = p.max_blocks_per_seq * BS;
+  if (ctx < 0 || ctx > ctx_cap) {
+    if (threadIdx.x == 0 && part == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    ctx = ctx < 0 ? 0 : ctx_cap;
+  }
+  const int nblk = (ctx + BS - 1) / BS;
+  int jb = 0, je = nblk;
+  if constexpr (SPLIT) {
+    if (part == 0 && threadIdx.x == 0 &&
+        (nblk + p.partition_blocks - 1) / p.partition_blocks > p.max_partitions)
+      raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    jb = part * p.partition_blocks;
+    if (jb >= nblk) return;  // past the end of this sequence; CTA-uniform, nothing issued yet
+    je = min(nblk, jb + p.partition_blocks);
+  }
+
+  unsigned char* wbase = smem + warp * Lay::WARP;
+  unsigned char* tiles = wbase;
+  float* ps = reinterpret_cast<float*>(wbase + Lay::TILES);
+  float* alpha_s = reinterpret_cast<float*>(wbase + Lay::TILES + Lay::PS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wbase + Lay::TILES + Lay::PS + Lay::ALPHA);
+
+  // This warp's share: logical blocks jb + warp + i * NW for i < nw.
+  const int span = je - jb;
+  const int nw = span > warp ? (span - warp + NW - 1) / NW : 0;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  // Block ids, 32 tiles per window, lane l holding tile (window * 32 + l).
+  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq + jb + warp;
+  auto load_ids = [&](int win) -> int {
+    const int i = win * 32 + lane;
+    int id = 0;
+    if (i < nw) {
+      id = __ldg(tbl + static_cast<size_t>(i) * NW);
+      if (id < 0 || id >= p.num_blocks) {
+        raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        id = 0;
+      }
+    }
+    return id;
+  };
+  int ids_win = 0;
+  int ids_cur = load_ids(0);
+  int ids_next = nw > 32 ? load_ids(1) : 0;
+
+  // q of the G heads of this group, this lane's 8 dims, times scale*log2(e).
+  float2 q2[G][4];
+  {
+    const __nv_bfloat16* qb =
+        p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const uint4 w = *reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D);
+      q2[g][0] = __fmul2_rn(bf16x2_to_float2(w.x), sc2);
+      q2[g][1] = __fmul2_rn(bf16x2_to_float2(w.y), sc2);
+      q2[g][2] = __fmul2_rn(bf16x2_to_float2(w.z), sc2);
+      q2[g][3] = __fmul2_rn(bf16x2_to_float2(w.w), sc2);
+    }
+  }
+
+  const uint64_t policy = l2_policy_evict_first();
+  const size_t block_stride = static_cast<size_t>(p.num_kv_heads) * BS * D;
+  const size_t head_off = static_cast<size_t>(kvh) * BS * D;
+  int issued = 0;
+  // Called by the whole warp, in tile order.
+  auto issue = [&](int i) {
+    if ((i >> 5) != ids_win) {
+      ids_cur = ids_next;
+      ++ids_win;
+      ids_next = (ids_win + 1) * 32 < nw ? load_ids(ids_win + 1) : 0;
+    }
+    const int id = __shfl_sync(kFullMask, ids_cur, i & 31);
+    if (lane == 0) {
+      const int st = i % S;
+      uint64_t* bar = &bars[st];
+      unsigned char* dst = tiles + st * 2 * Geo::TILE;
+      const size_t off = static_cast<size_t>(id) * block_stride + head_off;
+      mbar_arrive_expect_tx(bar, 2 * Geo::TILE);
+      bulk_copy_g2s(dst, p.k_cache + off, Geo::TILE, bar, policy);
+      bulk_copy_g2s(dst + Geo::TILE, p.v_cache + off, Geo::TILE, bar, policy);
+    }
+    issued = i + 1;
+  };
+
+  float2 acc[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc[g][k] = make_float2(0.f, 0.f);
+  float m_run = -INFINITY;  // running max of this lane's head, base-2 units
+  float l_run = 0.f;        // this lane's share of that head's exp-sum
+  const int my_head = (sub * R) / P;
+  const int my_i0 = (sub * R) % P;
+
+  const int npro = nw < S ? nw : S;
+  for (int i = 0; i < npro; ++i) issue(i);
+
+  int consumed = 0;
+  for (int i = 0; i < nw; ++i) {
+    const int st = i % S;
+    const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&bars[st], (i / S) & 1, p.err));
+    if (!ready) break;
+    const int j = jb + warp + i * NW;
+    const int nvalid = min(BS, ctx - j * BS);
+    const uint4* kt = reinterpret_cast<const uint4*>(tiles + st * 2 * Geo::TILE);
+    const uint4* vt = kt + Geo::TILE / 16;
+    if (nvalid == BS)
+      tile_step<D, G, true>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub, rg,
+                            my_head, my_i0);
+    else
+      tile_step<D, G, false>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub, rg,
+                             my_head, my_i0);
+    consumed = i + 1;
+    __syncwarp();  // every lane is done with this stage and with ps / alpha_s
+    if (i + S < nw) issue(i + S);
+  }
+  // Only after a timed-out wait: let copies still in flight land (bounded)
+  // before this CTA's shared memory can be reused.
+  for (int i = consumed; i < issued; ++i) mbar_wait_bounded(&bars[i % S], (i / S) & 1, p.err);
+
+  // Per-warp totals: l over the lanes of each head, acc over row groups.
+#pragma unroll
+  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+#pragma unroll
+  for (int m = L; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+#pragma unroll
+  for (int m = L; m < 32; m <<= 1)
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        acc[g][k].x += __shfl_xor_sync(kFullMask, acc[g][k].x, m);
+        acc[g][k].y += __shfl_xor_sync(kFullMask, acc[g][k].y, m);
+      }
+
+  // Merge warps through shared memory (each warp writes into its own, now
+  // idle, tile ring): [G][D] acc, then m[G], l[G].
+  float* mrg = reinterpret_cast<float*>(wbase);
+  if (rg == 0) {
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float4* dst = reinterpret_cast<float4*>(mrg + g * D + sub * 8);
+      dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+      dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+    }
+    if (sub % Geo::HEAD_LANES == 0) {
+      mrg[G * D + my_head] = m_run;
+      mrg[G * D + G + my_head] = l_run;
+    }
+  }
+  __syncthreads();
+
+  for (int idx = threadIdx.x; idx < G * (D / 8); idx += NW * 32) {
+    const int g = idx / (D / 8);
+    const int d0 = (idx % (D / 8)) * 8;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      M = fmaxf(M, reinterpret_cast<const float*>(smem + w * Lay::WARP)[G * D + g]);
+    float o[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) o[k] = 0.f;
+    float Ls = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float* mw = reinterpret_cast<const float*>(smem + w * Lay::WARP);
+        const float c = exp2f(mw[G * D + g] - M);
+        Ls += mw[G * D + G + g] * c;
+        const float4 a = *reinterpret_cast<const float4*>(mw + g * D + d0);
+        const float4 bq = *reinterpret_cast<const float4*>(mw + g * D + d0 + 4);
+        o[0] += a.x * c;
+        o[1] += a.y * c;
+        o[2] += a.z * c;
+        o[3] += a.w * c;
+        o[4] += bq.x * c;
+        o[5] += bq.y * c;
+        o[6] += bq.z * c;
+        o[7] += bq.w * c;
+      }
+      const float inv = 1.0f / Ls;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) o[k] *= inv;
+    }
+    const int hq = kvh * G + g;
+    if constexpr (SPLIT) {
+      const size_t row =
+          (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions + part;
+      float4* dst = reinterpret_cast<float4*>(p.ws_o + row * D + d0);
+      dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+      dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+      if (d0 == 0) {
+        p.ws_m[row] = M * kLn2;  // back to natural-log units
+        p.ws_l[row] = Ls;
+      }
+    } else {
+      __nv_bfloat162 h[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) h[k] = __float22bfloat162_rn(make_float2(o[2 * k], o[2 * k + 1]));
+      *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(b) * p.num_q_heads + hq) * D + d0) =
+          *reinterpret_cast<const uint4*>(h);
+    }
+  }
+}
+
+// Log-sum-exp merge of split-K partitions: one CTA of D threads per
+// (sequence, query head); thread d owns output dim d.  Partition weights
+// are recomputed by every thread from (m, l), which are warp-uniform loads.
+template <int D>
+__global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p) {
+  const int hq = blockIdx.x;
+  const int b = blockIdx.y;
+  const int d = threadIdx.x;
+  int ctx = p.context_lens[b];
+  const int64_t cap = static_cast<int64_t>(p.max_partitions) * p.partition_size;
+  if (ctx < 0 || ctx > cap) {
+    if (d == 0 && hq == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    ctx = ctx < 0 ? 0 : static_cast<int>(cap);
+  }
+  const int np = (ctx + p.partition_size - 1) / p.partition_size;
+  const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions;
+  const float* m = p.ws_m + row0;
+  const float* l = p.ws_l + row0;
+  const float* o = p.ws_o + row0 * D + d;
+  float M = -INFINITY;
+  for (int i = 0; i < np; ++i) M = fmaxf(M, m[i]);
+  float acc = 0.f, Ls = 0.f;
+  int i = 0;
+  for (; i + 4 <= np; i += 4) {
+    const float w0 = l[i] * expf(m[i] - M), w1 = l[i + 1] * expf(m[i + 1] - M);
+    const float w2 = l[i + 2] * expf(m[i + 2] - M), w3 = l[i + 3] * expf(m[i + 3] - M);
+    const float o0 = o[static_cast<size_t>(i) * D], o1 = o[static_cast<size_t>(i + 1) * D];
+    const float o2 = o[static_cast<size_t>(i + 2) * D], o3 = o[static_cast<size_t>(i + 3) * D];
+    Ls += (w0 + w1) + (w2 + w3);
+    acc += (w0 * o0 + w1 * o1) + (w2 * o2 + w3 * o3);
+  }
+  for (; i < np; ++i) {
+    const float w = l[i] * expf(m[i] - M);
+    Ls += w;
+    acc += w * o[static_cast<size_t>(i) * D];
+  }
+  const float r = np > 0 ? acc / Ls : 0.f;
+  p.out[(static_cast<size_t>(b) * p.num_q_heads + hq) * D + d] = __float2bfloat16_rn(r);
+}
+
+// Raises the dynamic shared-memory limit of a kernel once per device.
+template <typename K>
+cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (done_mask.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done_mask.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+template <int D, int G, bool SPLIT>
+cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  constexpr int NW = Pipe<D>::NW, S = Pipe<D>::S;
+  using Lay = SmemLayout<D, G, NW, S>;
+  static std::atomic<uint64_t> smem_set{0};
+  auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT>;
+  cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
+  kernel<<<grid, NW * 32, Lay::TOTAL, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeParams& p, int group, bool split, cudaStream_t stream) {
+  switch (group) {
+    case 2:
+      return split ? launch_decode_t<D, 2, true>(p, stream) : launch_decode_t<D, 2, false>(p, stream);
+    case 4:
+      return split ? launch_decode_t<D, 4, true>(p, stream) : launch_decode_t<D, 4, false>(p, stream);
+    case 8:
+      return split ? launch_decode_t<D, 8, true>(p, stream) : launch_decode_t<D, 8, false>(p, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+bool decode_shape_supported(int head_dim, int group, int block_size) {
+  return block_size == kBlockSize && (head_dim == 64 || head_dim == 128) &&
+         (group == 2 || group == 4 || group == 8);
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool split,
+                          cudaStream_t stream) {
+  if (head_dim == 128) return launch_decode_d<128>(p, group, split, stream);
+  if (head_dim == 64) return launch_decode_d<64>(p, group, split, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream) {
+  const dim3 grid(p.num_q_heads, p.num_seqs);
+  if (head_dim == 128)
+    splitk_reduce_kernel<128><<<grid, 128, 0, stream>>>(p);
+  else if (head_dim == 64)
+    splitk_reduce_kernel<64><<<grid, 64, 0, stream>>>(p);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,74 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pa.h"
+
+namespace pa {
+
+// Arguments of the decode kernels (plain and split-K).  Pointers are device
+// pointers, already validated on the host.
+struct DecodeParams {
+  __nv_bfloat16* out;  // pa_decode: [B, Hq, D]
+  float* ws_o;         // split-K: [B, Hq, max_partitions, D]
+  float* ws_m;         // split-K: [B, Hq, max_partitions]
+  float* ws_l;         // split-K: [B, Hq, max_partitions]
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k_cache;
+  const __nv_bfloat16* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  unsigned* err;
+  int max_blocks_per_seq;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int max_partitions;    // split-K only
+  int partition_blocks;  // split-K only: blocks per partition
+  float scale_log2;      // scale * log2(e): scores are kept in base-2 units
+};
+
+struct ReduceParams {
+  __nv_bfloat16* out;
+  const float* ws_o;
+  const float* ws_m;
+  const float* ws_l;
+  const int32_t* context_lens;
+  unsigned* err;
+  int num_seqs;
+  int num_q_heads;
+  int max_partitions;
+  int partition_size;
+};
+
+struct CacheWriteParams {
+  const __nv_bfloat16* key;
+  const __nv_bfloat16* value;
+  __nv_bfloat16* k_cache;
+  __nv_bfloat16* v_cache;
+  const int64_t* slot_mapping;
+  unsigned* err;
+  int num_tokens;
+  int num_kv_heads;
+  int head_dim;
+  int block_size;
+  int64_t num_slots;  // num_blocks * block_size
+};
+
+// Shapes with a compiled decode kernel.
+bool decode_shape_supported(int head_dim, int group, int block_size);
+
+cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool split,
+                          cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream);
+
+// Address of the current device's error word (device memory), or nullptr.
+unsigned* device_error_word();
+
+}  // namespace pa

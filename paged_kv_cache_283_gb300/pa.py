@@ -1,0 +1,337 @@
+"""Thin ctypes binding of libpa.so (include/pa.h), same names as the C ABI.
+
+Argument marshalling only: every device function here checks the tensors'
+device / dtype / contiguity, reads their shapes, and passes ``data_ptr()`` and
+the current CUDA stream to the C entry point; all computation happens in the
+library's kernels.  A non-OK status raises ``PAError``.  There is no fallback:
+if ``libpa.so`` is missing this module raises on first use.
+
+Tensors: bf16 data is passed as ``torch.bfloat16`` tensors; block tables and
+context lengths as ``torch.int32``; slot mappings as ``torch.int64``.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpa.so")
+
+PA_OK = 0
+PA_ERR_INVALID_ARG = 1
+PA_ERR_UNSUPPORTED_SHAPE = 2
+PA_ERR_OUT_OF_BLOCKS = 3
+PA_ERR_CUDA = 4
+
+PA_DEVERR_BLOCK_ID = 0x1
+PA_DEVERR_CONTEXT_LEN = 0x2
+PA_DEVERR_SLOT = 0x4
+PA_DEVERR_WAIT_TIMEOUT = 0x8
+
+# Every function include/pa.h declares: name -> (restype, argtypes).
+_vp, _i, _u, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
+_i64, _pi32, _pi64, _pint = ctypes.c_int64, ctypes.POINTER(ctypes.c_int32), \
+    ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int)
+SIGNATURES = {
+    "pa_status_string": (ctypes.c_char_p, [_i]),
+    "pa_last_cuda_error": (ctypes.c_char_p, []),
+    "pa_get_device_error": (_i, [ctypes.POINTER(_u)]),
+    "pa_clear_device_error": (_i, []),
+    "pa_decode_supported": (_i, [_i, _i, _i, _i]),
+    "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
+    "pa_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
+                              _i, _i, _f, _i, _vp]),
+    "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
+    "pa_alloc_create": (_i, [_i, _i, _vp, ctypes.POINTER(_vp)]),
+    "pa_alloc_destroy": (None, [_vp]),
+    "pa_alloc_add_seq": (_i, [_vp, _i]),
+    "pa_alloc_append_slot": (_i, [_vp, _i, _pi64, _pi32, _pi32]),
+    "pa_alloc_append_slots": (_i, [_vp, _vp, _i, _vp, _vp, _vp]),
+    "pa_alloc_reserve": (_i, [_vp, _i, _i, _pi32, _pi32]),
+    "pa_alloc_fork": (_i, [_vp, _i, _i]),
+    "pa_alloc_free_seq": (_i, [_vp, _i]),
+    "pa_alloc_block_table": (_i, [_vp, _i, _vp, _i, _pint]),
+    "pa_alloc_block_tables": (_i, [_vp, _vp, _i, _vp, _i, _vp]),
+    "pa_alloc_seq_len": (_i64, [_vp, _i]),
+    "pa_alloc_refcount": (_i, [_vp, _i]),
+    "pa_alloc_num_free": (_i, [_vp]),
+    "pa_alloc_num_blocks": (_i, [_vp]),
+    "pa_alloc_free_list": (_i, [_vp, _vp, _i, _pint]),
+    "pa_alloc_tail_waste": (_i, [_vp, _i]),
+}
+
+_lib = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = lib().pa_status_string(status).decode()
+        if status == PA_ERR_CUDA:
+            msg += ": " + lib().pa_last_cuda_error().decode()
+        super().__init__(f"{where}: {msg}")
+
+
+class OutOfBlocks(PAError):
+    pass
+
+
+def lib():
+    """The loaded library (ctypes.CDLL); raises if libpa.so was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m paged_kv_cache_283_gb300.build` (needs nvcc)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status, where):
+    if status != PA_OK:
+        if status == PA_ERR_OUT_OF_BLOCKS:
+            raise OutOfBlocks(status, where)
+        raise PAError(status, where)
+
+
+# --------------------------------------------------------------------------
+# device entry points (torch tensors in, launches on the current stream)
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, dtype, name, ndim=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def pa_decode_supported(num_q_heads, num_kv_heads, head_dim, block_size):
+    return lib().pa_decode_supported(num_q_heads, num_kv_heads, head_dim, block_size) == PA_OK
+
+
+def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None):
+    """key/value [T, Hkv, D] bf16; pools [NB, Hkv, bs, D] bf16; slot_mapping [T] int64."""
+    torch = _torch()
+    T, hkv, d = key.shape
+    nb, hkv2, bs, d2 = k_cache.shape
+    if value.shape != key.shape or v_cache.shape != k_cache.shape or (hkv, d) != (hkv2, d2):
+        raise ValueError("pa_reshape_and_cache: inconsistent shapes")
+    if slot_mapping.shape != (T,):
+        raise ValueError("pa_reshape_and_cache: slot_mapping must be [num_tokens]")
+    st = lib().pa_reshape_and_cache(
+        _dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3),
+        _dev(k_cache, torch.bfloat16, "k_cache", 4), _dev(v_cache, torch.bfloat16, "v_cache", 4),
+        _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb, _stream(stream))
+    _check(st, "pa_reshape_and_cache")
+
+
+def _decode_common(q, k_cache, v_cache, block_tables, context_lens):
+    torch = _torch()
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d != d2:
+        raise ValueError("decode: inconsistent q / cache shapes")
+    if block_tables.dim() != 2 or block_tables.shape[0] != B or context_lens.shape != (B,):
+        raise ValueError("decode: block_tables must be [B, max_blocks], context_lens [B]")
+    ptrs = (_dev(q, torch.bfloat16, "q", 3), _dev(k_cache, torch.bfloat16, "k_cache", 4),
+            _dev(v_cache, torch.bfloat16, "v_cache", 4),
+            _dev(block_tables, torch.int32, "block_tables", 2),
+            _dev(context_lens, torch.int32, "context_lens", 1))
+    return ptrs, (B, hq, hkv, d, bs, nb, block_tables.shape[1])
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, stream=None):
+    """out, q [B, Hq, D] bf16; pools [NB, Hkv, 16, D]; block_tables [B, MB] int32."""
+    torch = _torch()
+    (pq, pk, pv, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_common(
+        q, k_cache, v_cache, block_tables, context_lens)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode: out must match q")
+    st = lib().pa_decode(_dev(out, torch.bfloat16, "out", 3), pq, pk, pv, pt, mb, pc, B, hq, hkv,
+                         d, bs, nb, float(scale), _stream(stream))
+    _check(st, "pa_decode")
+
+
+def pa_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, partition_size):
+    return int(lib().pa_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
+                                               partition_size))
+
+
+def pa_decode_splitk(ws_out, ws_m, ws_l, q, k_cache, v_cache, block_tables, context_lens, scale,
+                     partition_size=512, stream=None):
+    """ws_out [B, Hq, P, D] fp32, ws_m / ws_l [B, Hq, P] fp32 (P = max partitions)."""
+    torch = _torch()
+    (pq, pk, pv, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_common(
+        q, k_cache, v_cache, block_tables, context_lens)
+    maxp = ws_m.shape[2]
+    if ws_out.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape or ws_m.shape[:2] != (B, hq):
+        raise ValueError("pa_decode_splitk: workspace shapes")
+    st = lib().pa_decode_splitk(
+        _dev(ws_out, torch.float32, "ws_out", 4), _dev(ws_m, torch.float32, "ws_m", 3),
+        _dev(ws_l, torch.float32, "ws_l", 3), maxp, pq, pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb,
+        float(scale), int(partition_size), _stream(stream))
+    _check(st, "pa_decode_splitk")
+
+
+def pa_splitk_reduce(out, ws_out, ws_m, ws_l, context_lens, partition_size=512, stream=None):
+    torch = _torch()
+    B, hq, maxp, d = ws_out.shape
+    if out.shape != (B, hq, d) or ws_m.shape != (B, hq, maxp) or ws_l.shape != ws_m.shape:
+        raise ValueError("pa_splitk_reduce: shapes")
+    st = lib().pa_splitk_reduce(
+        _dev(out, torch.bfloat16, "out", 3), _dev(ws_out, torch.float32, "ws_out", 4),
+        _dev(ws_m, torch.float32, "ws_m", 3), _dev(ws_l, torch.float32, "ws_l", 3), maxp,
+        _dev(context_lens, torch.int32, "context_lens", 1), B, hq, d, int(partition_size),
+        _stream(stream))
+    _check(st, "pa_splitk_reduce")
+
+
+def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition_size=512,
+                     device="cuda"):
+    """Allocates (ws_out, ws_m, ws_l) for pa_decode_splitk with torch."""
+    torch = _torch()
+    maxp = max(1, -(-int(max_context_len) // int(partition_size)))
+    return (torch.empty((num_seqs, num_q_heads, maxp, head_dim), dtype=torch.float32, device=device),
+            torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device),
+            torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device))
+
+
+def pa_get_device_error():
+    v = ctypes.c_uint(0)
+    _check(lib().pa_get_device_error(ctypes.byref(v)), "pa_get_device_error")
+    return v.value
+
+
+def pa_clear_device_error():
+    _check(lib().pa_clear_device_error(), "pa_clear_device_error")
+
+
+# --------------------------------------------------------------------------
+# host block allocator (no GPU needed)
+
+class BlockAllocator:
+    """Wraps pa_alloc_* (include/pa.h).  numpy arrays in and out."""
+
+    def __init__(self, num_blocks, block_size, initial_free_order=None):
+        import numpy as np
+        self._np = np
+        h = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            if order.shape != (num_blocks,):
+                raise ValueError("initial_free_order must have num_blocks entries")
+        st = lib().pa_alloc_create(num_blocks, block_size,
+                                   None if order is None else order.ctypes.data_as(_vp),
+                                   ctypes.byref(h))
+        _check(st, "pa_alloc_create")
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().pa_alloc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def add_seq(self, seq):
+        _check(lib().pa_alloc_add_seq(self._h, seq), "pa_alloc_add_seq")
+
+    def append_slot(self, seq):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pa_alloc_append_slot(self._h, seq, ctypes.byref(slot), ctypes.byref(src),
+                                          ctypes.byref(dst)), "pa_alloc_append_slot")
+        return slot.value, src.value, dst.value
+
+    def append_slots(self, seqs):
+        np = self._np
+        ids = np.ascontiguousarray(seqs, dtype=np.intc)
+        n = ids.shape[0]
+        slots = np.empty(n, dtype=np.int64)
+        src = np.empty(n, dtype=np.int32)
+        dst = np.empty(n, dtype=np.int32)
+        _check(lib().pa_alloc_append_slots(self._h, ids.ctypes.data_as(_vp), n,
+                                           slots.ctypes.data_as(_vp), src.ctypes.data_as(_vp),
+                                           dst.ctypes.data_as(_vp)), "pa_alloc_append_slots")
+        return slots, src, dst
+
+    def reserve(self, seq, num_tokens):
+        src, dst = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().pa_alloc_reserve(self._h, seq, int(num_tokens), ctypes.byref(src),
+                                      ctypes.byref(dst)), "pa_alloc_reserve")
+        return src.value, dst.value
+
+    def fork(self, parent, child):
+        _check(lib().pa_alloc_fork(self._h, parent, child), "pa_alloc_fork")
+
+    def free_seq(self, seq):
+        _check(lib().pa_alloc_free_seq(self._h, seq), "pa_alloc_free_seq")
+
+    def block_table(self, seq):
+        np = self._np
+        n = ctypes.c_int()
+        _check(lib().pa_alloc_block_table(self._h, seq, None, 0, ctypes.byref(n)),
+               "pa_alloc_block_table")
+        out = np.empty(n.value, dtype=np.int32)
+        _check(lib().pa_alloc_block_table(self._h, seq, out.ctypes.data_as(_vp), n.value,
+                                          ctypes.byref(n)), "pa_alloc_block_table")
+        return out
+
+    def block_tables(self, seqs, max_blocks):
+        np = self._np
+        ids = np.ascontiguousarray(seqs, dtype=np.intc)
+        out = np.empty((ids.shape[0], max_blocks), dtype=np.int32)
+        ctx = np.empty(ids.shape[0], dtype=np.int32)
+        _check(lib().pa_alloc_block_tables(self._h, ids.ctypes.data_as(_vp), ids.shape[0],
+                                           out.ctypes.data_as(_vp), max_blocks,
+                                           ctx.ctypes.data_as(_vp)), "pa_alloc_block_tables")
+        return out, ctx
+
+    def seq_len(self, seq):
+        return int(lib().pa_alloc_seq_len(self._h, seq))
+
+    def refcount(self, blk):
+        return int(lib().pa_alloc_refcount(self._h, blk))
+
+    def num_free(self):
+        return int(lib().pa_alloc_num_free(self._h))
+
+    def free_list(self):
+        np = self._np
+        n = ctypes.c_int()
+        out = np.empty(self.num_blocks, dtype=np.int32)
+        _check(lib().pa_alloc_free_list(self._h, out.ctypes.data_as(_vp), self.num_blocks,
+                                        ctypes.byref(n)), "pa_alloc_free_list")
+        return out[:n.value]
+
+    def tail_waste(self, seq):
+        return int(lib().pa_alloc_tail_waste(self._h, seq))
