@@ -258,6 +258,25 @@ def _reference_timed(args, nseq):
 
 
 # ---------------------------------------------------------------------------
+# multi-rank aggregation (weak scaling: every rank times its own batch)
+
+def combine_ranks(local_seconds, step_bytes, steps, world, device="cpu"):
+    """Max of the ranks' timed seconds and the whole-job GB/s it implies.
+
+    Each rank processed ``steps`` steps of ``step_bytes`` algorithmic bytes;
+    the job took as long as the slowest rank.  Host-side timing exchange only:
+    the data path has no collective.
+    """
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(local_seconds)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dt = float(t.item())
+    return dt, world * step_bytes * steps / dt / 1e9
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 
 def _setup(idx, device, replicas_min_bytes):
@@ -351,6 +370,25 @@ def _attn_fns(st, attn, partition):
             attend(layer, kc, vc)
 
     return step, dominant, outs
+
+
+def recorded_traffic(kernel, workload_name, partition):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source or the launch shape changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+    try:
+        kv = dict(line.strip().split("=", 1) for line in open(path)
+                  if "=" in line and not line.startswith("#"))
+        with open(os.path.join(ROOT, "paged_kv_cache_283_gb300", "csrc", "decode.cu"), "rb") as f:
+            sha = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if (sha.startswith(kv.get("kernel_source_sha256_prefix", "-")) and kv.get("kernel") == kernel
+            and kv.get("workload") == workload_name
+            and (kernel != "pa_decode_splitk" or int(kv.get("partition", -1)) == partition)):
+        return int(kv["dram_bytes_per_launch"])
+    return None
 
 
 def _capture(fn, stream):
@@ -460,17 +498,15 @@ def run_gpu(args):
                              + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim))
     dom_bytes = decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads, w.num_kv_heads,
                              w.head_dim, w.block_size)
-    times = torch.tensor([dt], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    dt_max = float(times.item())
-    value = world * step_bytes * args.steps / dt_max / 1e9
+    dt_max, value = combine_ranks(dt, step_bytes, args.steps, world, device)
     hbm_peak = peaks.get("hbm_gbs")
     achieved = dom_bytes / dom_dt / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak if hbm_peak else 6800.0, "unit": "GB/s",
                 "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
-                "traffic": args.traffic,
+                "traffic": args.traffic if args.traffic is not None else recorded_traffic(
+                    "pa_decode_splitk" if attn == "splitk" else "pa_decode", w.name,
+                    args.partition),
                 "kernel": "pa_decode_splitk" if attn == "splitk" else "pa_decode",
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
                 else "fallback 6.8 TB/s",
