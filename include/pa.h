@@ -186,6 +186,37 @@ pa_status pa_splitk_reduce(void* out, const float* ws_out, const float* ws_m,
                            int num_q_heads, int head_dim, int partition_size,
                            pa_stream_t stream);
 
+/*
+ * Split-K decode with no allocation.  The pages have no counterpart to this
+ * entry point: it exists for callers that cannot call cudaMalloc -- serving
+ * runtimes that reserve all device memory up front for their own pools, and
+ * latency-critical threads that must not take the device synchronisation an
+ * allocation can imply.  It computes exactly pa_decode_splitk followed by
+ * pa_splitk_reduce (same kernels, same results), but their fp32 workspace is
+ * a fixed array of PA_DECODE_NOALLOC_WORKSPACE_BYTES compiled into the
+ * library, resident on every GPU that loads it until the process exits.
+ *   max_context_len: an upper bound on every context_lens[b] (host value);
+ *   the workspace holds B * Hq * P rows of (head_dim + 2) floats with
+ *   P = ceil(max_context_len / partition_size).  A call needing more than
+ *   PA_DECODE_NOALLOC_WORKSPACE_BYTES (or P > 65535) returns
+ *   PA_ERR_INVALID_ARG before any launch.  A context longer than
+ *   max_context_len sets PA_DEVERR_CONTEXT_LEN and its excess is dropped.
+ * Calls no cudaMalloc / cudaFree.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  All calls share the one
+ * array: calls whose kernels overlap on the GPU (other streams, other
+ * threads) race on it.  Nothing in it needs to start at zero; it keeps the
+ * last call's partials.
+ */
+#define PA_DECODE_NOALLOC_WORKSPACE_BYTES ((size_t)8 << 20)
+pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_tables,
+                                   int max_blocks_per_seq, const int32_t* context_lens,
+                                   int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks,
+                                   float scale, int partition_size, int max_context_len,
+                                   pa_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Host block allocator [PA], [SH], [LIFE], [OOM], [WALK].  Not thread-safe;
  * one allocator per caller thread or external locking.  Deterministic: the

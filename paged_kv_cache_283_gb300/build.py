@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 
-SOURCES = ["api.cu", "decode.cu", "reshape_and_cache.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "decode.cu", "reshape_and_cache.cu", "noalloc.cu", "allocator.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
            os.path.join(CSRC, "device.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

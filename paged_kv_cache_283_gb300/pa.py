@@ -42,6 +42,8 @@ SIGNATURES = {
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
                               _i, _i, _f, _i, _vp]),
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
+    "pa_decode_splitk_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                                      _f, _i, _i, _vp]),
     "pa_alloc_create": (_i, [_i, _i, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i, [_vp, _i]),
@@ -217,6 +219,28 @@ def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition
     return (torch.empty((num_seqs, num_q_heads, maxp, head_dim), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device))
+
+
+def pa_decode_splitk_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                             max_context_len, partition_size=512, stream=None):
+    """Split-K decode + merge with the library's built-in workspace.
+
+    For callers that must not allocate device memory: nothing is allocated,
+    by this binding or the library.  ``max_context_len`` bounds every context
+    length; calls needing more than PA_DECODE_NOALLOC_WORKSPACE_BYTES of
+    workspace raise PAError (invalid argument).  Concurrent calls on
+    different streams share the workspace and race.
+    """
+    torch = _torch()
+    (pq, pk, pv, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_common(
+        q, k_cache, v_cache, block_tables, context_lens)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode_splitk_noalloc: out must match q")
+    st = lib().pa_decode_splitk_noalloc(_dev(out, torch.bfloat16, "out", 3), pq, pk, pv, pt, mb,
+                                        pc, B, hq, hkv, d, bs, nb, float(scale),
+                                        int(partition_size), int(max_context_len),
+                                        _stream(stream))
+    _check(st, "pa_decode_splitk_noalloc")
 
 
 def pa_get_device_error():
