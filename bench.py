@@ -449,7 +449,7 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device)
     attn = args.attn
     if attn == "auto":
-        attn = "splitk" if args.workload in (2, 3) else "decode"
+        attn = "splitk" if args.workload in (2, 3, 5) else "decode"
     step, dominant, outs = _attn_fns(st, attn, args.partition)
 
     # eager warmup (sets kernel attributes, checks the error word)

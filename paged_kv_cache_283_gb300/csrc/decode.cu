@@ -61,18 +61,33 @@ struct Geometry {
   static_assert(NV % L == 0 && R >= 1 && P % R == 0, "score geometry");
 };
 
-// Pipeline shape per head_dim: warps per CTA and stages per warp.
-template <int D>
-struct Pipe;
-template <>
-struct Pipe<128> {
-  static constexpr int NW = 4;
-  static constexpr int S = 3;
-};
-template <>
-struct Pipe<64> {
+// Pipeline shape: warps per CTA and stages per warp (each stage holds one K
+// and one V tile), per head_dim and per kernel (whole sequence vs split-K
+// partition).  Chosen by measurement on the batch-64 Llama-8B decode: 4 warps
+// x 2 stages lets three split-K CTAs share an SM; whole-sequence CTAs do
+// better with 8 warps x 2 stages, one long CTA per SM.  Overridable at compile
+// time for tuning.
+#ifndef PA_SPLIT_WARPS_D128
+#define PA_SPLIT_WARPS_D128 4
+#endif
+#ifndef PA_SPLIT_STAGES_D128
+#define PA_SPLIT_STAGES_D128 2
+#endif
+#ifndef PA_WHOLE_WARPS_D128
+#define PA_WHOLE_WARPS_D128 8
+#endif
+#ifndef PA_WHOLE_STAGES_D128
+#define PA_WHOLE_STAGES_D128 2
+#endif
+template <int D, bool SPLIT>
+struct Pipe {  // head_dim 64: 2 KiB tiles, deeper rings
   static constexpr int NW = 4;
   static constexpr int S = 4;
+};
+template <bool SPLIT>
+struct Pipe<128, SPLIT> {
+  static constexpr int NW = SPLIT ? PA_SPLIT_WARPS_D128 : PA_WHOLE_WARPS_D128;
+  static constexpr int S = SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128;
 };
 
 template <int D, int G, int NW, int S>
@@ -207,13 +222,19 @@ __device__ __forceinline__ void tile_step(const uint4* __restrict__ kt, const ui
   }
 }
 
+// Small CTAs are meant to share an SM three at a time: give the register
+// allocator that budget (<= 168 per thread) instead of its default guess;
+// groups of 8 heads need more registers than that and get one CTA's worth.
 template <int D, int G, int NW, int S, bool SPLIT>
-__global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
+    paged_decode_kernel(const DecodeParams p) {
   using Geo = Geometry<D, G>;
   using Lay = SmemLayout<D, G, NW, S>;
   constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
   extern __shared__ __align__(128) unsigned char smem[];
 
+  griddep_wait();  // the previous kernel (e.g. the cache write) is complete
+  griddep_launch_dependents();
   const int kvh = blockIdx.x;
   const int b = blockIdx.y;
   const int part = blockIdx.z;
@@ -222,8 +243,40 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
   const int sub = lane % L;
   const int rg = lane / L;
 
+  // The context length, this warp's first 32 block ids and q are independent
+  // loads, so they go out together: the ids are read speculatively from the
+  // table slots this CTA may use (in bounds whatever the context length is)
+  // and only those below the context length are used, after a range check.
+  const int64_t part_first = SPLIT ? static_cast<int64_t>(part) * p.partition_blocks : 0;
+  const int tbl_end = SPLIT ? static_cast<int>(min(static_cast<int64_t>(p.max_blocks_per_seq),
+                                                   part_first + p.partition_blocks))
+                            : p.max_blocks_per_seq;
+  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+  auto load_ids = [&](int win) -> int {
+    const int64_t j = part_first + warp + static_cast<int64_t>(win * 32 + lane) * NW;
+    return j < tbl_end ? __ldg(tbl + j) : 0;
+  };
+  int ctx = __ldg(p.context_lens + b);
+  int ids_cur = load_ids(0);
+  float2 q2[G][4];
+  {
+    const __nv_bfloat16* qb =
+        p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
+    uint4 qw[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      qw[g] = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D));
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
+      q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
+      q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
+      q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
+    }
+  }
+
   // Context length lives in device memory: check it here.
-  int ctx = p.context_lens[b];
   const int ctx_cap = p.max_blocks_per_seq * BS;
   if (ctx < 0 || ctx > ctx_cap) {
     if (threadIdx.x == 0 && part == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
@@ -235,8 +288,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
     if (part == 0 && threadIdx.x == 0 &&
         (nblk + p.partition_blocks - 1) / p.partition_blocks > p.max_partitions)
       raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    jb = part * p.partition_blocks;
-    if (jb >= nblk) return;  // past the end of this sequence; CTA-uniform, nothing issued yet
+    if (part_first >= nblk) return;  // past the end of this sequence; CTA-uniform, nothing issued
+    jb = static_cast<int>(part_first);
     je = min(nblk, jb + p.partition_blocks);
   }
 
@@ -257,39 +310,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
   }
   __syncwarp();
 
-  // Block ids, 32 tiles per window, lane l holding tile (window * 32 + l).
-  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq + jb + warp;
-  auto load_ids = [&](int win) -> int {
-    const int i = win * 32 + lane;
-    int id = 0;
-    if (i < nw) {
-      id = __ldg(tbl + static_cast<size_t>(i) * NW);
-      if (id < 0 || id >= p.num_blocks) {
-        raise_error(p.err, PA_DEVERR_BLOCK_ID);
-        id = 0;
-      }
-    }
-    return id;
-  };
+  // Block ids: 32 tiles per window, lane l holding tile (window * 32 + l);
+  // the next window is prefetched while the current one is in use.
   int ids_win = 0;
-  int ids_cur = load_ids(0);
   int ids_next = nw > 32 ? load_ids(1) : 0;
-
-  // q of the G heads of this group, this lane's 8 dims, times scale*log2(e).
-  float2 q2[G][4];
-  {
-    const __nv_bfloat16* qb =
-        p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const uint4 w = *reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D);
-      q2[g][0] = __fmul2_rn(bf16x2_to_float2(w.x), sc2);
-      q2[g][1] = __fmul2_rn(bf16x2_to_float2(w.y), sc2);
-      q2[g][2] = __fmul2_rn(bf16x2_to_float2(w.z), sc2);
-      q2[g][3] = __fmul2_rn(bf16x2_to_float2(w.w), sc2);
-    }
-  }
 
   const uint64_t policy = l2_policy_evict_first();
   const size_t block_stride = static_cast<size_t>(p.num_kv_heads) * BS * D;
@@ -302,8 +326,12 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
       ++ids_win;
       ids_next = (ids_win + 1) * 32 < nw ? load_ids(ids_win + 1) : 0;
     }
-    const int id = __shfl_sync(kFullMask, ids_cur, i & 31);
+    int id = __shfl_sync(kFullMask, ids_cur, i & 31);
     if (lane == 0) {
+      if (id < 0 || id >= p.num_blocks) {  // never dereferenced: read block 0 instead
+        raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        id = 0;
+      }
       const int st = i % S;
       uint64_t* bar = &bars[st];
       unsigned char* dst = tiles + st * 2 * Geo::TILE;
@@ -441,6 +469,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_kernel(const DecodeParam
 // are recomputed by every thread from (m, l), which are warp-uniform loads.
 template <int D>
 __global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p) {
+  griddep_wait();  // the partition pass is complete
+  griddep_launch_dependents();
   const int hq = blockIdx.x;
   const int b = blockIdx.y;
   const int d = threadIdx.x;
@@ -492,15 +522,14 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
 
 template <int D, int G, bool SPLIT>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int NW = Pipe<D>::NW, S = Pipe<D>::S;
+  constexpr int NW = Pipe<D, SPLIT>::NW, S = Pipe<D, SPLIT>::S;
   using Lay = SmemLayout<D, G, NW, S>;
   static std::atomic<uint64_t> smem_set{0};
   auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT>;
   cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
-  kernel<<<grid, NW * 32, Lay::TOTAL, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kernel, grid, dim3(NW * 32), Lay::TOTAL, stream, p);
 }
 
 template <int D>
@@ -533,13 +562,9 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool s
 
 cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream) {
   const dim3 grid(p.num_q_heads, p.num_seqs);
-  if (head_dim == 128)
-    splitk_reduce_kernel<128><<<grid, 128, 0, stream>>>(p);
-  else if (head_dim == 64)
-    splitk_reduce_kernel<64><<<grid, 64, 0, stream>>>(p);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (head_dim == 128) return launch_pdl(splitk_reduce_kernel<128>, grid, dim3(128), 0, stream, p);
+  if (head_dim == 64) return launch_pdl(splitk_reduce_kernel<64>, grid, dim3(64), 0, stream, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

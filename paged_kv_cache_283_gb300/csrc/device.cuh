@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/pa.h"
 
 namespace pa {
@@ -93,6 +95,38 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
       "[%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+
+// Programmatic dependent launch.  Every kernel of this library is launched
+// with programmatic stream serialisation, so it may be scheduled while the
+// previous kernel in the stream is still running; it executes griddep_wait()
+// before its first global-memory access (which returns once that kernel has
+// finished and its writes are visible), so the result is the same as with
+// plain stream order whatever the previous kernel is.  griddep_launch_dependents()
+// lets the next kernel be scheduled as soon as this grid has started.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel<<<grid, block, smem, stream>>>(args...)` with
+// programmatic stream serialisation allowed (see above).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 }  // namespace pa

@@ -23,6 +23,8 @@ namespace pa {
 namespace {
 
 __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheWriteParams p) {
+  griddep_wait();  // the producer of key / value / slots is complete
+  griddep_launch_dependents();
   const int chunks = p.head_dim / 8;  // 16-byte chunks per row
   const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * chunks;
   const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -55,8 +57,8 @@ cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t str
   const int threads = 256;
   const int64_t blocks = (total + threads - 1) / threads;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-  reshape_and_cache_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(reshape_and_cache_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0,
+                    stream, p);
 }
 
 }  // namespace pa
