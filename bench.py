@@ -198,6 +198,16 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    if os.environ.get("OMP_NUM_THREADS") != "1":
+        # time the oracle on exactly one host thread, in a fresh process
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+                   MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+        env.pop("RANK", None)
+        env.pop("WORLD_SIZE", None)
+        r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                            "--steps", str(args.steps), "--warmup", str(args.warmup),
+                            "--workload", str(args.workload)], env=env, cwd=ROOT)
+        return r.returncode
     # one oracle sample per step, sized so that warmup + steps stay within ~2 minutes
     probe = oracle_step_sample(args.workload, 0.0, out_json=False)
     per = probe["seconds_per_sample"]
@@ -380,8 +390,11 @@ def recorded_traffic(kernel, workload_name, partition):
     try:
         kv = dict(line.strip().split("=", 1) for line in open(path)
                   if "=" in line and not line.startswith("#"))
-        with open(os.path.join(ROOT, "paged_kv_cache_283_gb300", "csrc", "decode.cu"), "rb") as f:
-            sha = hashlib.sha256(f.read()).hexdigest()
+        h = hashlib.sha256()
+        for name in ("decode.cu", "decode_tile.cuh"):
+            with open(os.path.join(ROOT, "paged_kv_cache_283_gb300", "csrc", name), "rb") as f:
+                h.update(f.read())
+        sha = h.hexdigest()
     except OSError:
         return None
     if (sha.startswith(kv.get("kernel_source_sha256_prefix", "-")) and kv.get("kernel") == kernel

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libpa.so")
 
 SOURCES = ["api.cu", "decode.cu", "reshape_and_cache.cu", "noalloc.cu", "allocator.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
-           os.path.join(CSRC, "device.cuh")]
+           os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                    "-Xptxas", "-v", "--expt-relaxed-constexpr"]

@@ -327,3 +327,37 @@ def test_binding_rejects_cpu_tensors():
         pa.pa_decode(q, q, torch.zeros(1, 2, 16, 64, dtype=torch.bfloat16),
                      torch.zeros(1, 2, 16, 64, dtype=torch.bfloat16),
                      torch.zeros(1, 1, dtype=torch.int32), torch.ones(1, dtype=torch.int32), 1.0)
+
+
+@pytest.mark.parametrize("case", ["many_seqs", "long_partition"])
+def test_splitk_large_batch_and_long_partitions(case):
+    # A batch of 1100 short sequences, and partitions of 512 blocks.
+    if case == "many_seqs":
+        rng = np.random.default_rng(3030)
+        ctx = rng.integers(1, 80, size=1100)
+        w = I.random_case(3031, 1100, ctx, 8, 2, 64)
+        split = 32
+    else:
+        w = I.random_case(3032, 3, [9000, 4100, 17], 16, 8, 128)
+        split = 8192
+    bt_m, sl_m, bt_p, sl_p = both_tables(w)
+    got = _gpu_step(w, bt_p, sl_p, w.k_cache, w.v_cache, w.q, w.key, w.value, split)
+    ref = _oracle_step(w, bt_m, sl_m, w.k_cache.copy(), w.v_cache.copy(), w.q, w.key, w.value)
+    _compare(got, ref, None, f"split-K ({case})")
+    _assert_no_device_error()
+
+
+@pytest.mark.parametrize("split", [16, 48, 256])
+def test_splitk_schedule_mixes(split):
+    # Many small and a few long sequences: partial partitions of every size,
+    # sequences with no full partition, and an empty one.
+    rng = np.random.default_rng(split)
+    ctx = np.concatenate([rng.integers(1, 40, size=60), rng.integers(1000, 3000, size=6), [0]])
+    w = I.random_case(5000 + split, len(ctx), ctx, 32, 8, 128)
+    bt, _ = model_tables(w, step_append=False)
+    bt[bt < 0] = 0
+    out = _run_decode(dev_bf16(w.q), dev_bf16(w.k_cache), dev_bf16(w.v_cache), _dev_i32(bt),
+                      _dev_i32(w.context_lens), w.scale, split)
+    ref = OA.decode(w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.scale, 16)
+    assert_close(bf16_to_f64(out), ref, f"schedule mix, partition {split}")
+    _assert_no_device_error()
