@@ -629,6 +629,56 @@ def _e2e(st, attn, args, stream):
                    "launch stream, wall clock around all steps"}
 
 
+def run_copy_blocks(args):
+    """Copy-on-write block copies of a parallel-sampling step: 64 prompts
+    forked into 4 samples each, whose shared, partly filled last blocks are
+    copied in all 32 layers (256 pairs x 32 layers x K and V)."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_283_gb300 import build as _b
+    from paged_kv_cache_283_gb300 import pa
+
+    _b.build()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    layers, hkv, bs, d, pairs_n = 32, 8, 16, 128, 256
+    nb = 2 * pairs_n + 64
+    rng = np.random.default_rng(283 + 6)
+    perm = rng.permutation(nb)
+    pairs = torch.from_numpy(perm[:2 * pairs_n].reshape(pairs_n, 2).astype(np.int64)).to(dev)
+    reps = 2
+    pools = [([torch.randn(nb, hkv, bs, d, device=dev).to(torch.bfloat16) for _ in range(layers)],
+              [torch.randn(nb, hkv, bs, d, device=dev).to(torch.bfloat16) for _ in range(layers)])
+             for _ in range(reps)]
+    stream = torch.cuda.Stream(dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            pa.pa_copy_blocks(pools[r][0], pools[r][1], pairs)
+    stream.synchronize()
+    for r in range(reps):
+        graphs.append(_capture(lambda r=r: pa.pa_copy_blocks(pools[r][0], pools[r][1], pairs),
+                               stream))
+    _time_graphs(graphs, args.warmup, stream)
+    dt = _time_graphs(graphs, args.steps, stream) / args.steps
+    nbytes = 2 * pairs_n * layers * 2 * hkv * bs * d * 2   # read + write, K and V
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    gbs = nbytes / dt / 1e9
+    print(json.dumps({"metric": "copy-on-write block copy GB/s", "value": round(gbs, 1),
+                      "unit": "GB/s", "us_per_call": round(dt * 1e6, 2), "bytes": nbytes,
+                      "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4)
+                      if peaks.get("hbm_gbs") else None,
+                      "config": {"pairs": pairs_n, "layers": layers, "block_bytes": hkv * bs * d * 2,
+                                 "l2": "2 pool replicas of %.0f MB" % (2 * layers * nb * hkv * bs * d * 2 / 1e6)}}))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -636,6 +686,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
+                    help="copy_blocks: time pa_copy_blocks on a parallel-sampling step")
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--soak-seconds", type=float, default=0.5)
@@ -648,6 +700,8 @@ def main(argv=None):
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "copy_blocks":
+        return run_copy_blocks(args)
     return run_gpu(args)
 
 

@@ -9,6 +9,7 @@
  *                          sequence's blocks, found through its block table
  *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
+ *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
  *   pa_alloc_*             fixed-size block allocator with reference counts
  *                          and copy-on-write (host only, never on the GPU path)
  *
@@ -127,6 +128,24 @@ pa_status pa_reshape_and_cache(const void* key, const void* value,
                                const int64_t* slot_mapping, int num_tokens,
                                int num_kv_heads, int head_dim, int block_size,
                                int num_blocks, pa_stream_t stream);
+
+/*
+ * Copy-on-write block copy [SH]: for every pair i, with src = block_mapping[2i]
+ * and dst = block_mapping[2i + 1] (device int64 [num_pairs, 2]), copies the
+ * whole block in the K pool and the V pool of every layer:
+ *   k_caches[l][dst, :, :, :] = k_caches[l][src, :, :, :]  (and V), l < num_layers.
+ * k_caches / v_caches are HOST arrays of num_layers device pointers, each a
+ * pool [num_blocks, num_kv_heads, block_size, head_dim] bf16.  These are the
+ * (cow_src, cow_dst) pairs pa_alloc_append_slot(s) report; copying the whole
+ * block is a superset of the rows the new owner needs.  No destination may
+ * appear twice or also as a source (such copies race).  Ids outside
+ * [0, num_blocks) set PA_DEVERR_BLOCK_ID and the pair is skipped; src == dst
+ * is a no-op.  num_pairs == 0 or num_layers == 0 is a no-op.
+ */
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                         const int64_t* block_mapping, int num_pairs,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int num_blocks, pa_stream_t stream);
 
 /*
  * Paged decode attention [KV], [PA]: for every sequence b and query head h

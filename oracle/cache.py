@@ -11,6 +11,11 @@ are the plainest reading of "a block table maps each logical block to a
 physical block" with fixed-size blocks.
 
 This is a bit copy: arrays of raw bf16 bit patterns go in and come out.
+
+``copy_blocks`` is the copy half of copy-on-write ("Sharing comes for free": a
+shared block is copied only when one branch needs to write into it): for each
+(source, destination) pair the whole destination block takes the source
+block's contents, in every layer's K and V pool.
 """
 import numpy as np
 
@@ -31,3 +36,15 @@ def reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, block_size,
         kc[blk, :, off, :] = key[t]
         vc[blk, :, off, :] = value[t]
     return kc, vc
+
+
+def copy_blocks(k_caches, v_caches, pairs, inplace=False):
+    """Copy block src to block dst for every (src, dst) in ``pairs``, in every
+    layer's pools; returns the lists of resulting pools."""
+    ks = [k if inplace else np.array(k, copy=True) for k in k_caches]
+    vs = [v if inplace else np.array(v, copy=True) for v in v_caches]
+    for src, dst in np.asarray(pairs).reshape(-1, 2).tolist():
+        for k, v in zip(ks, vs):
+            k[dst] = k[src]
+            v[dst] = v[src]
+    return ks, vs

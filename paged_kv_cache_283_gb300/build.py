@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 
-SOURCES = ["api.cu", "decode.cu", "reshape_and_cache.cu", "noalloc.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "decode.cu", "splitk_reduce.cu", "reshape_and_cache.cu", "copy_blocks.cu",
+           "noalloc.cu", "allocator.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
            os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -121,6 +121,35 @@ pa_status pa_reshape_and_cache(const void* key, const void* value, void* k_cache
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
+pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_layers,
+                         const int64_t* block_mapping, int num_pairs, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_stream_t stream) {
+  if (num_layers < 0 || num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 8 != 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_layers == 0 || num_pairs == 0) return PA_OK;
+  if (num_pairs > 0x7fffffff / 2 || !k_caches || !v_caches || !ok_ptr(block_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l)
+    if (!ok_ptr(k_caches[l], 16) || !ok_ptr(v_caches[l], 16)) return PA_ERR_INVALID_ARG;
+  CopyBlocksParams p{};
+  p.block_mapping = block_mapping;
+  p.block_bytes = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * 2;
+  p.num_blocks = num_blocks;
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  for (int l0 = 0; l0 < num_layers; l0 += kCopyMaxLayers) {
+    const int n = num_layers - l0 < kCopyMaxLayers ? num_layers - l0 : kCopyMaxLayers;
+    for (int l = 0; l < n; ++l) {
+      p.k_caches[l] = k_caches[l0 + l];
+      p.v_caches[l] = v_caches[l0 + l];
+    }
+    cudaError_t e = launch_copy_blocks(p, num_pairs, n, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  return PA_OK;
+}
+
 namespace {
 
 // Checks shared by pa_decode and pa_decode_splitk.

@@ -25,7 +25,7 @@
 //    by scale*log2 e); P is handed to the PV loop through a 256-byte smem
 //    buffer; warps merge (m, l, acc) through shared memory at the end.
 //  * Split-K writes per-partition (m, l, o/l) in fp32; a second small kernel
-//    merges partitions by the log-sum-exp identity.
+//    (splitk_reduce.cu) merges partitions by the log-sum-exp identity.
 //  * Every device-resident index is checked: bad block ids read block 0 and
 //    set PA_DEVERR_BLOCK_ID; bad context lengths are clamped; every mbarrier
 //    wait is bounded.  Nothing traps.
@@ -332,48 +332,6 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
   }
 }
 
-// Log-sum-exp merge of split-K partitions: one CTA of D threads per
-// (sequence, query head); thread d owns output dim d.  Partition weights
-// are recomputed by every thread from (m, l), which are warp-uniform loads.
-template <int D>
-__global__ void __launch_bounds__(D) splitk_reduce_kernel(const ReduceParams p) {
-  griddep_wait();  // the partition pass is complete
-  griddep_launch_dependents();
-  const int hq = blockIdx.x;
-  const int b = blockIdx.y;
-  const int d = threadIdx.x;
-  int ctx = p.context_lens[b];
-  const int64_t cap = static_cast<int64_t>(p.max_partitions) * p.partition_size;
-  if (ctx < 0 || ctx > cap) {
-    if (d == 0 && hq == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    ctx = ctx < 0 ? 0 : static_cast<int>(cap);
-  }
-  const int np = (ctx + p.partition_size - 1) / p.partition_size;
-  const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions;
-  const float* m = p.ws_m + row0;
-  const float* l = p.ws_l + row0;
-  const float* o = p.ws_o + row0 * D + d;
-  float M = -INFINITY;
-  for (int i = 0; i < np; ++i) M = fmaxf(M, m[i]);
-  float acc = 0.f, Ls = 0.f;
-  int i = 0;
-  for (; i + 4 <= np; i += 4) {
-    const float w0 = l[i] * expf(m[i] - M), w1 = l[i + 1] * expf(m[i + 1] - M);
-    const float w2 = l[i + 2] * expf(m[i + 2] - M), w3 = l[i + 3] * expf(m[i + 3] - M);
-    const float o0 = o[static_cast<size_t>(i) * D], o1 = o[static_cast<size_t>(i + 1) * D];
-    const float o2 = o[static_cast<size_t>(i + 2) * D], o3 = o[static_cast<size_t>(i + 3) * D];
-    Ls += (w0 + w1) + (w2 + w3);
-    acc += (w0 * o0 + w1 * o1) + (w2 * o2 + w3 * o3);
-  }
-  for (; i < np; ++i) {
-    const float w = l[i] * expf(m[i] - M);
-    Ls += w;
-    acc += w * o[static_cast<size_t>(i) * D];
-  }
-  const float r = np > 0 ? acc / Ls : 0.f;
-  p.out[(static_cast<size_t>(b) * p.num_q_heads + hq) * D + d] = __float2bfloat16_rn(r);
-}
-
 // Raises the dynamic shared-memory limit of a kernel once per device.
 template <typename K>
 cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
@@ -428,11 +386,5 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool s
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream) {
-  const dim3 grid(p.num_q_heads, p.num_seqs);
-  if (head_dim == 128) return launch_pdl(splitk_reduce_kernel<128>, grid, dim3(128), 0, stream, p);
-  if (head_dim == 64) return launch_pdl(splitk_reduce_kernel<64>, grid, dim3(64), 0, stream, p);
-  return cudaErrorInvalidValue;
-}
 
 }  // namespace pa

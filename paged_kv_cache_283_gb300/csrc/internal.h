@@ -60,6 +60,18 @@ struct CacheWriteParams {
   int64_t num_slots;  // num_blocks * block_size
 };
 
+// Pools of up to kCopyMaxLayers layers go to one copy_blocks launch.
+constexpr int kCopyMaxLayers = 64;
+
+struct CopyBlocksParams {
+  void* k_caches[kCopyMaxLayers];
+  void* v_caches[kCopyMaxLayers];
+  const int64_t* block_mapping;  // [num_pairs, 2]: (src, dst)
+  unsigned* err;
+  int64_t block_bytes;  // Hkv * bs * D * 2
+  int64_t num_blocks;
+};
+
 // Shapes with a compiled decode kernel.
 bool decode_shape_supported(int head_dim, int group, int block_size);
 
@@ -67,6 +79,8 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool s
                           cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const CopyBlocksParams& p, int num_pairs, int num_layers,
+                               cudaStream_t stream);
 
 // Address of the current device's error word (device memory), or nullptr.
 unsigned* device_error_word();

@@ -33,6 +33,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheWrite
   const int64_t row = idx / chunks;  // token * Hkv + head
   const int h = static_cast<int>(row % p.num_kv_heads);
   const int64_t t = row / p.num_kv_heads;
+  // the new K/V chunk and its slot are independent loads: issue them together
+  const int64_t src = row * p.head_dim + c * 8;
+  const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.key + src));
+  const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.value + src));
   const int64_t slot = __ldg(p.slot_mapping + t);
   if (slot < 0) return;
   if (slot >= p.num_slots) {
@@ -41,10 +45,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheWrite
   }
   const int64_t blk = slot / p.block_size;
   const int64_t off = slot % p.block_size;
-  const int64_t src = row * p.head_dim + c * 8;
   const int64_t dst = ((blk * p.num_kv_heads + h) * p.block_size + off) * p.head_dim + c * 8;
-  const uint4 kv = __ldg(reinterpret_cast<const uint4*>(p.key + src));
-  const uint4 vv = __ldg(reinterpret_cast<const uint4*>(p.value + src));
   *reinterpret_cast<uint4*>(p.k_cache + dst) = kv;
   *reinterpret_cast<uint4*>(p.v_cache + dst) = vv;
 }

@@ -37,6 +37,7 @@ SIGNATURES = {
     "pa_clear_device_error": (_i, []),
     "pa_decode_supported": (_i, [_i, _i, _i, _i]),
     "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_copy_blocks": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp]),
     "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "pa_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
@@ -148,6 +149,26 @@ def pa_reshape_and_cache(key, value, k_cache, v_cache, slot_mapping, stream=None
         _dev(k_cache, torch.bfloat16, "k_cache", 4), _dev(v_cache, torch.bfloat16, "v_cache", 4),
         _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb, _stream(stream))
     _check(st, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_caches, v_caches, block_mapping, stream=None):
+    """Copy-on-write copies: block_mapping [n, 2] int64 (src, dst) on the device;
+    k_caches / v_caches: lists of per-layer pools [NB, Hkv, bs, D] bf16."""
+    torch = _torch()
+    if len(k_caches) != len(v_caches) or not k_caches:
+        raise ValueError("pa_copy_blocks: one K and one V pool per layer")
+    nb, hkv, bs, d = k_caches[0].shape
+    for kc, vc in zip(k_caches, v_caches):
+        if kc.shape != k_caches[0].shape or vc.shape != kc.shape:
+            raise ValueError("pa_copy_blocks: all pools must have one shape")
+    if block_mapping.dim() != 2 or block_mapping.shape[1] != 2:
+        raise ValueError("pa_copy_blocks: block_mapping must be [num_pairs, 2]")
+    n = len(k_caches)
+    kp = (ctypes.c_void_p * n)(*[_dev(t, torch.bfloat16, "k_cache", 4).value for t in k_caches])
+    vp = (ctypes.c_void_p * n)(*[_dev(t, torch.bfloat16, "v_cache", 4).value for t in v_caches])
+    st = lib().pa_copy_blocks(kp, vp, n, _dev(block_mapping, torch.int64, "block_mapping", 2),
+                              block_mapping.shape[0], hkv, d, bs, nb, _stream(stream))
+    _check(st, "pa_copy_blocks")
 
 
 def _decode_common(q, k_cache, v_cache, block_tables, context_lens):

@@ -178,3 +178,38 @@ def test_random_script_invariants():
         assert len(set(free)) == len(free)
         assert all(refs[b] == 0 for b in free)
         assert len(free) + sum(1 for r in refs if r > 0) == nb
+
+
+def test_copy_blocks_copies_whole_blocks_in_every_layer():
+    from oracle.cache import copy_blocks
+    rng = np.random.default_rng(5)
+    ks = [rng.integers(0, 65535, size=(6, 2, 16, 8), dtype=np.uint16) for _ in range(3)]
+    vs = [rng.integers(0, 65535, size=(6, 2, 16, 8), dtype=np.uint16) for _ in range(3)]
+    k2, v2 = copy_blocks(ks, vs, [[1, 4], [5, 0]])
+    for l in range(3):
+        assert np.array_equal(k2[l][4], ks[l][1]) and np.array_equal(v2[l][4], vs[l][1])
+        assert np.array_equal(k2[l][0], ks[l][5]) and np.array_equal(v2[l][0], vs[l][5])
+        for blk in (1, 2, 3, 5):
+            assert np.array_equal(k2[l][blk], ks[l][blk])
+            assert np.array_equal(v2[l][blk], vs[l][blk])
+
+
+def test_copy_on_write_keeps_branches_apart():
+    # a forked sequence that writes into the shared partial block gets its own
+    # copy; the parent's view of the block is unchanged
+    from oracle.cache import copy_blocks, reshape_and_cache
+    rng = np.random.default_rng(6)
+    m = BlockAllocatorModel(6, 16, [3, 1, 4, 0, 2, 5])
+    m.add_seq(0)
+    m.reserve(0, 20)                       # blocks [3, 1], 4 tokens in block 1
+    m.fork(0, 1)
+    slot, src, dst = m.append_slot(1)
+    assert (src, dst) == (1, 4) and slot == 4 * 16 + 4
+    kc = rng.integers(0, 65535, size=(6, 1, 16, 4), dtype=np.uint16)
+    vc = rng.integers(0, 65535, size=(6, 1, 16, 4), dtype=np.uint16)
+    (kc2,), (vc2,) = copy_blocks([kc], [vc], [[src, dst]])
+    key = rng.integers(0, 65535, size=(1, 1, 4), dtype=np.uint16)
+    kc3, vc3 = reshape_and_cache(key, key, kc2, vc2, [slot], 16)
+    assert np.array_equal(kc3[4, :, :4], kc[1, :, :4])      # prefix rows copied
+    assert np.array_equal(kc3[4, 0, 4], key[0, 0])           # child's new token
+    assert np.array_equal(kc3[1], kc[1])                     # parent's block untouched
