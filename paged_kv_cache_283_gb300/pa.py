@@ -264,6 +264,78 @@ def pa_decode_splitk_noalloc(out, q, k_cache, v_cache, block_tables, context_len
     _check(st, "pa_decode_splitk_noalloc")
 
 
+class DecodeStep:
+    """One decode step of one layer on fixed device buffers: the cache write
+    of the batch's new tokens, then paged attention (split-K pass + merge, or
+    the whole-sequence kernel).
+
+    Every argument is checked and marshalled once, here; each call then makes
+    two or three bare C calls, which keeps the host ahead of the GPU when a
+    step lasts only tens of microseconds.  The buffers' contents may change
+    between calls (that is the point); their shapes and addresses may not.
+    The split-K workspace is allocated with torch unless one is passed.
+    """
+
+    def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
+                 context_lens, out, scale, split=True, partition_size=512,
+                 max_context_len=None, workspace=None, stream=None):
+        torch = _torch()
+        T, hkv, d = key.shape
+        nb, hkv2, bs, d2 = k_cache.shape
+        if value.shape != key.shape or v_cache.shape != k_cache.shape or (hkv, d) != (hkv2, d2):
+            raise ValueError("DecodeStep: inconsistent key / cache shapes")
+        if slot_mapping.shape != (T,):
+            raise ValueError("DecodeStep: slot_mapping must be [num_tokens]")
+        (pq, pk, pv, pt, pc), (B, hq, _, _, _, _, mb) = _decode_common(
+            q, k_cache, v_cache, block_tables, context_lens)
+        if out.shape != q.shape:
+            raise ValueError("DecodeStep: out must match q")
+        po = _dev(out, torch.bfloat16, "out", 3)
+        self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables, context_lens,
+                      out]
+        self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+        self._rc = (_dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3),
+                    pk, pv, _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb)
+        self.split = bool(split)
+        if self.split:
+            if workspace is None:
+                mc = int(max_context_len) if max_context_len is not None else mb * bs
+                workspace = splitk_workspace(B, hq, d, mc, partition_size, q.device)
+            ws_o, ws_m, ws_l = workspace
+            maxp = ws_m.shape[2]
+            if ws_o.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape:
+                raise ValueError("DecodeStep: workspace shapes")
+            self._keep += list(workspace)
+            self.workspace = workspace
+            wo = _dev(ws_o, torch.float32, "ws_out", 4)
+            wm = _dev(ws_m, torch.float32, "ws_m", 3)
+            wl = _dev(ws_l, torch.float32, "ws_l", 3)
+            self._dk = (wo, wm, wl, maxp, pq, pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb,
+                        float(scale), int(partition_size))
+            self._rd = (po, wo, wm, wl, maxp, pc, B, hq, d, int(partition_size))
+        else:
+            self._dc = (po, pq, pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale))
+        lib()
+
+    def __call__(self, stream=None):
+        L = _lib
+        s = self._stream if stream is None and self._stream is not None else _stream(stream)
+        st = L.pa_reshape_and_cache(*self._rc, s)
+        if st != PA_OK:
+            _check(st, "DecodeStep: pa_reshape_and_cache")
+        if self.split:
+            st = L.pa_decode_splitk(*self._dk, s)
+            if st != PA_OK:
+                _check(st, "DecodeStep: pa_decode_splitk")
+            st = L.pa_splitk_reduce(*self._rd, s)
+            if st != PA_OK:
+                _check(st, "DecodeStep: pa_splitk_reduce")
+        else:
+            st = L.pa_decode(*self._dc, s)
+            if st != PA_OK:
+                _check(st, "DecodeStep: pa_decode")
+
+
 def pa_get_device_error():
     v = ctypes.c_uint(0)
     _check(lib().pa_get_device_error(ctypes.byref(v)), "pa_get_device_error")

@@ -361,3 +361,34 @@ def test_splitk_schedule_mixes(split):
     ref = OA.decode(w.q, w.k_cache, w.v_cache, bt, w.context_lens, w.scale, 16)
     assert_close(bf16_to_f64(out), ref, f"schedule mix, partition {split}")
     _assert_no_device_error()
+
+
+@pytest.mark.parametrize("split", [False, True])
+def test_decode_step_object_matches_oracle(split):
+    # pa.DecodeStep: the same cache write + attention with pre-marshalled
+    # calls; called twice with new inputs written into the same buffers
+    w = I.random_case(777, 6, [300, 17, 1, 2049, 512, 96], 32, 8, 128)
+    bt_m, sl_m, bt_p, sl_p = both_tables(w)
+    kc, vc = dev_bf16(w.k_cache), dev_bf16(w.v_cache)
+    key, val, q = dev_bf16(w.key), dev_bf16(w.value), dev_bf16(w.q)
+    slots, bt, ctx = _dev_i64(sl_p), _dev_i32(bt_p), _dev_i32(w.context_lens)
+    out = torch.empty_like(q)
+    step = pa.DecodeStep(key, val, kc, vc, slots, q, bt, ctx, out, w.scale, split=split,
+                         partition_size=256, max_context_len=int(w.context_lens.max()))
+    kc_o, vc_o = w.k_cache.copy(), w.v_cache.copy()
+    rng = np.random.default_rng(778)
+    for it in range(2):
+        if it == 1:
+            nk, nv, nq = (I.normal_bf16(rng, w.key.shape), I.normal_bf16(rng, w.value.shape),
+                          I.normal_bf16(rng, w.q.shape))
+            key.copy_(dev_bf16(nk))
+            val.copy_(dev_bf16(nv))
+            q.copy_(dev_bf16(nq))
+        else:
+            nk, nv, nq = w.key, w.value, w.q
+        step()
+        torch.cuda.synchronize()
+        kc_o, vc_o = OC.reshape_and_cache(nk, nv, kc_o, vc_o, sl_m, 16, inplace=True)
+        ref = OA.decode(nq, kc_o, vc_o, bt_m, w.context_lens, w.scale, 16)
+        assert_close(bf16_to_f64(out), ref, f"DecodeStep split={split} call {it}")
+    _assert_no_device_error()
