@@ -10,8 +10,9 @@
  *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
  *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
- *   pa_alloc_*             fixed-size block allocator with reference counts
- *                          and copy-on-write (host only, never on the GPU path)
+ *   pa_alloc_*             fixed-size block allocator with reference counts,
+ *                          copy-on-write and automatic prefix caching (host
+ *                          only, never on the GPU path)
  *
  * Passages these follow (page title, section):
  *   [KV]   "How LLM Inference Serving Works: KV Cache, PagedAttention and
@@ -30,6 +31,9 @@
  *          drop when the request ends.
  *   [OOM]  same page, "When memory runs out anyway" -- when blocks run out
  *          the engine preempts a request.
+ *   [PFX]  same page, "Prefix Caching and Chunked Prefill" -- blocks named
+ *          by a hash of their tokens and the prefix before them are reused
+ *          by later prompts; unused cached blocks are evicted in LRU order.
  *   [WALK] "LLM serving (vLLM, quantized inference): Visual walkthrough",
  *          Steps 7-8 -- block_size 16, at most block_size-1 slots wasted,
  *          shared prefixes stored once.
@@ -304,6 +308,52 @@ int pa_alloc_num_blocks(const pa_alloc* a);
 pa_status pa_alloc_free_list(const pa_alloc* a, int32_t* out, int cap, int* n_out);
 /* Empty slots in the sequence's last block, or -1 if unknown [WALK]. */
 int pa_alloc_tail_waste(const pa_alloc* a, int seq_id);
+
+/* ------------------------------------------------------------------------ */
+/* Automatic prefix caching [PFX] ("How LLM Inference Serving Works",
+ * section "Prefix Caching and Chunked Prefill", and "Putting It Together":
+ * blocks become cached-but-evictable when their counts drop).  Every full
+ * block of a prompt is named by a chained hash of the tokens in it and of
+ * all tokens before it; a table maps names to physical blocks, so a prompt
+ * reuses the blocks of the longest cached prefix, and a block matches only
+ * if the whole prefix up to it is identical.  The pages fix no hash; here a
+ * block's name is SHA-256(parent name || its tokens as little-endian int32),
+ * the first block's parent being 32 zero bytes, or SHA-256(cache_salt) when
+ * the request carries a salt (so tenants with different salts never share).
+ * A named block whose count reaches 0 is kept, cached-but-evictable, in
+ * least-recently-used order; fresh blocks come from the free list first and
+ * then by evicting the least recently used cached block (its name is
+ * dropped).  Only prompt blocks are named; blocks filled by later appends
+ * are not. */
+
+/* Turns prefix caching on; only while the allocator holds no sequence. */
+pa_status pa_alloc_enable_prefix_cache(pa_alloc* a);
+
+/* Registers seq_id with a prompt of num_tokens tokens: the longest cached
+ * prefix of whole blocks is shared (+1 reference each), the rest of the
+ * prompt gets fresh blocks, and the prompt's new full blocks are named.
+ * *cached_tokens (may be NULL) receives how many leading tokens already
+ * have their K/V in the cache (a multiple of block_size); the caller
+ * computes the rest.  salt / salt_len: optional per-request cache salt
+ * (salt_len 0: none).  PA_ERR_OUT_OF_BLOCKS (state unchanged) if the free
+ * and evictable blocks cannot hold the uncached part; PA_ERR_INVALID_ARG if
+ * prefix caching is off or seq_id exists. */
+pa_status pa_alloc_add_seq_prompt(pa_alloc* a, int seq_id, const int32_t* tokens,
+                                  int num_tokens, const void* salt, int salt_len,
+                                  int* cached_tokens);
+
+/* Number of cached-but-evictable blocks (-1 if a is NULL). */
+int pa_alloc_num_evictable(const pa_alloc* a);
+
+/* Copies the cached-but-evictable blocks, least recently used first. */
+pa_status pa_alloc_evictable_list(const pa_alloc* a, int32_t* out, int cap, int* n_out);
+
+/* The names used above, exposed for callers that keep their own index:
+ * out[32] = the first block's parent name for this salt (salt_len 0: none). */
+pa_status pa_prefix_root_hash(const void* salt, int salt_len, uint8_t* out);
+/* out[32] = SHA-256(parent[32] || tokens as little-endian int32). */
+pa_status pa_prefix_block_hash(const uint8_t* parent, const int32_t* tokens, int num_tokens,
+                               uint8_t* out);
 
 #ifdef __cplusplus
 }

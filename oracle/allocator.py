@@ -29,7 +29,8 @@ seeded with the caller's order (default 0..num_blocks-1); blocks freed by a
 sequence are appended at its tail in the sequence's logical block order; the
 slot of position ``pos`` is table[pos // bs] * bs + pos % bs.
 """
-from collections import deque
+import hashlib
+from collections import OrderedDict, deque
 
 
 class InvalidArg(ValueError):
@@ -73,10 +74,18 @@ class BlockAllocatorModel:
             return 1
         return 1 if self.ref[self.tables[seq][-1]] > 1 else 0
 
+    def _available(self):
+        return len(self.free)
+
     def _take(self):
         blk = self.free.popleft()
         self.ref[blk] = 1
         return blk
+
+    def _release(self, blk):
+        self.ref[blk] -= 1
+        if self.ref[blk] == 0:
+            self.free.append(blk)
 
     def _append(self, seq):
         table = self.tables[seq]
@@ -97,7 +106,7 @@ class BlockAllocatorModel:
     def append_slot(self, seq):
         """Append one token; returns (slot, cow_src, cow_dst) with -1 for no copy."""
         self._check(seq)
-        if self._needs_block(seq) > len(self.free):
+        if self._needs_block(seq) > self._available():
             raise OutOfBlocks("no free block")
         return self._append(seq)
 
@@ -112,7 +121,7 @@ class BlockAllocatorModel:
         for s in seqs:
             self._check(s)
         need = sum(self._needs_block(s) for s in seqs)
-        if need > len(self.free):
+        if need > self._available():
             raise OutOfBlocks("not enough free blocks for the batch")
         return [self._append(s) for s in seqs]
 
@@ -131,7 +140,7 @@ class BlockAllocatorModel:
         bs = self.block_size
         fresh = -(-(pos + num_tokens) // bs) - (-(-pos // bs))
         cow = 1 if (pos % bs != 0 and self.ref[self.tables[seq][-1]] > 1) else 0
-        if fresh + cow > len(self.free):
+        if fresh + cow > self._available():
             raise OutOfBlocks("not enough free blocks")
         first = self._append(seq)
         for _ in range(num_tokens - 1):
@@ -152,9 +161,7 @@ class BlockAllocatorModel:
         """Drop the sequence; blocks whose count reaches zero go to the free tail."""
         self._check(seq)
         for blk in self.tables[seq]:
-            self.ref[blk] -= 1
-            if self.ref[blk] == 0:
-                self.free.append(blk)
+            self._release(blk)
         del self.tables[seq]
         del self.lens[seq]
 
@@ -180,3 +187,98 @@ class BlockAllocatorModel:
         """Empty slots in the sequence's last block (Visual walkthrough, Step 7)."""
         self._check(seq)
         return len(self.tables[seq]) * self.block_size - self.lens[seq]
+
+
+class PrefixCachingAllocatorModel(BlockAllocatorModel):
+    """The allocator with automatic prefix caching ("How LLM Inference Serving
+    Works", section "Prefix Caching and Chunked Prefill"; "Putting It
+    Together": counts drop at the end of a request and the blocks become
+    cached-but-evictable).
+
+    * Each full block of a prompt is named by a hash of the tokens in the
+      block and of all tokens before it: name_i = H(name_{i-1}, tokens_i).
+      The pages do not fix H; the reading used is SHA-256 over the parent's
+      32-byte name followed by the block's tokens as little-endian int32, the
+      first block's parent being 32 zero bytes or, with a per-request
+      cache_salt, SHA-256(salt) ("mixed into the first block's hash").
+    * A new prompt reuses the blocks of its longest cached prefix; a block
+      matches only if the whole prefix up to it is identical.
+    * A named block nobody references is kept, cached-but-evictable, in LRU
+      order; fresh blocks come from the free list first, then by evicting the
+      least recently used cached block (its name is dropped).
+    * Only prompt blocks are named.  A name already held by another block
+      keeps that block.
+    """
+
+    def __init__(self, num_blocks, block_size, initial_free_order=None):
+        super().__init__(num_blocks, block_size, initial_free_order)
+        self.by_name = {}
+        self.name_of = {}
+        self.evictable = OrderedDict()   # least recently used first
+
+    @staticmethod
+    def root_name(salt=b""):
+        return hashlib.sha256(bytes(salt)).digest() if salt else bytes(32)
+
+    @staticmethod
+    def block_name(parent, tokens):
+        body = b"".join(int(t).to_bytes(4, "little", signed=True) for t in tokens)
+        return hashlib.sha256(bytes(parent) + body).digest()
+
+    def _available(self):
+        return len(self.free) + len(self.evictable)
+
+    def _take(self):
+        if self.free:
+            blk = self.free.popleft()
+        else:
+            blk, _ = self.evictable.popitem(last=False)
+            del self.by_name[self.name_of.pop(blk)]
+        self.ref[blk] = 1
+        return blk
+
+    def _release(self, blk):
+        self.ref[blk] -= 1
+        if self.ref[blk] == 0:
+            if blk in self.name_of:
+                self.evictable[blk] = True
+            else:
+                self.free.append(blk)
+
+    def add_seq_prompt(self, seq, tokens, salt=b""):
+        """Registers ``seq`` with its prompt; returns the number of cached tokens."""
+        if seq in self.tables:
+            raise InvalidArg(f"sequence {seq} exists")
+        tokens = [int(t) for t in tokens]
+        bs = self.block_size
+        names, parent = [], self.root_name(salt)
+        for i in range(len(tokens) // bs):
+            parent = self.block_name(parent, tokens[i * bs:(i + 1) * bs])
+            names.append(parent)
+        hits = 0
+        while hits < len(names) and names[hits] in self.by_name:
+            hits += 1
+        hit_blocks = [self.by_name[n] for n in names[:hits]]
+        unreferenced = sum(1 for b in hit_blocks if self.ref[b] == 0)
+        need = -(-len(tokens) // bs) - hits
+        if need > self._available() - unreferenced:
+            raise OutOfBlocks("not enough free or evictable blocks for the prompt")
+        self.tables[seq] = []
+        for b in hit_blocks:
+            if self.ref[b] == 0:
+                del self.evictable[b]
+            self.ref[b] += 1
+            self.tables[seq].append(b)
+        self.lens[seq] = hits * bs
+        for _ in range(len(tokens) - hits * bs):
+            self._append(seq)
+        for i in range(hits, len(names)):
+            if names[i] in self.by_name:
+                continue
+            blk = self.tables[seq][i]
+            self.by_name[names[i]] = blk
+            self.name_of[blk] = names[i]
+        return hits * bs
+
+    def evictable_list(self):
+        return list(self.evictable)

@@ -20,9 +20,10 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libpa.so")
 
 SOURCES = ["api.cu", "decode.cu", "splitk_reduce.cu", "reshape_and_cache.cu", "copy_blocks.cu",
-           "noalloc.cu", "allocator.cpp"]
+           "noalloc.cu", "allocator.cpp", "sha256.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
-           os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh")]
+           os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh"),
+           os.path.join(CSRC, "sha256.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                    "-Xptxas", "-v", "--expt-relaxed-constexpr"]

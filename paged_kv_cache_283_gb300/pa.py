@@ -61,6 +61,12 @@ SIGNATURES = {
     "pa_alloc_num_blocks": (_i, [_vp]),
     "pa_alloc_free_list": (_i, [_vp, _vp, _i, _pint]),
     "pa_alloc_tail_waste": (_i, [_vp, _i]),
+    "pa_alloc_enable_prefix_cache": (_i, [_vp]),
+    "pa_alloc_add_seq_prompt": (_i, [_vp, _i, _vp, _i, _vp, _i, _pint]),
+    "pa_alloc_num_evictable": (_i, [_vp]),
+    "pa_alloc_evictable_list": (_i, [_vp, _vp, _i, _pint]),
+    "pa_prefix_root_hash": (_i, [_vp, _i, _vp]),
+    "pa_prefix_block_hash": (_i, [_vp, _vp, _i, _vp]),
 }
 
 _lib = None
@@ -452,3 +458,46 @@ class BlockAllocator:
 
     def tail_waste(self, seq):
         return int(lib().pa_alloc_tail_waste(self._h, seq))
+
+    # automatic prefix caching
+    def enable_prefix_cache(self):
+        _check(lib().pa_alloc_enable_prefix_cache(self._h), "pa_alloc_enable_prefix_cache")
+
+    def add_seq_prompt(self, seq, tokens, salt=b""):
+        """Registers a sequence with its prompt; returns the number of cached tokens."""
+        np = self._np
+        tok = np.ascontiguousarray(tokens, dtype=np.int32)
+        salt = bytes(salt)
+        n = ctypes.c_int()
+        _check(lib().pa_alloc_add_seq_prompt(self._h, seq, tok.ctypes.data_as(_vp), tok.shape[0],
+                                              salt if salt else None, len(salt), ctypes.byref(n)),
+               "pa_alloc_add_seq_prompt")
+        return n.value
+
+    def num_evictable(self):
+        return int(lib().pa_alloc_num_evictable(self._h))
+
+    def evictable_list(self):
+        np = self._np
+        n = ctypes.c_int()
+        out = np.empty(self.num_blocks, dtype=np.int32)
+        _check(lib().pa_alloc_evictable_list(self._h, out.ctypes.data_as(_vp), self.num_blocks,
+                                             ctypes.byref(n)), "pa_alloc_evictable_list")
+        return out[:n.value]
+
+
+def pa_prefix_root_hash(salt=b""):
+    out = (ctypes.c_uint8 * 32)()
+    salt = bytes(salt)
+    _check(lib().pa_prefix_root_hash(salt if salt else None, len(salt), out), "pa_prefix_root_hash")
+    return bytes(out)
+
+
+def pa_prefix_block_hash(parent, tokens):
+    import numpy as np
+    tok = np.ascontiguousarray(tokens, dtype=np.int32)
+    par = (ctypes.c_uint8 * 32)(*bytes(parent))
+    out = (ctypes.c_uint8 * 32)()
+    _check(lib().pa_prefix_block_hash(par, tok.ctypes.data_as(_vp), tok.shape[0], out),
+           "pa_prefix_block_hash")
+    return bytes(out)
