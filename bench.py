@@ -43,19 +43,22 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context only
 # ---------------------------------------------------------------------------
 # algorithmic bytes (what one step must move at least once)
 
-def decode_bytes(ctx, num_seqs, hq, hkv, d, bs):
-    """K/V of every attended token + q + out + block-table entries + lengths."""
+def decode_bytes(ctx, num_seqs, hq, hkv, d, bs, kv_dtype="bf16"):
+    """K/V of every attended token + q + out + block-table entries + lengths
+    (an INT8 cache stores d codes and one fp32 scale per token and KV head)."""
     import numpy as np
     ctx = np.asarray(ctx, dtype=np.int64)
-    kv = int(ctx.sum()) * hkv * d * 2 * 2
+    per = (d + 4) if kv_dtype == "int8" else 2 * d
+    kv = int(ctx.sum()) * hkv * per * 2
     qo = 2 * num_seqs * hq * d * 2
     tables = 4 * int((-(-ctx // bs)).sum()) + 4 * num_seqs
     return kv + qo + tables
 
 
-def cache_write_bytes(num_tokens, hkv, d):
+def cache_write_bytes(num_tokens, hkv, d, kv_dtype="bf16"):
     """Read the new tokens' K and V, write them into the pool, read the slots."""
-    return 2 * 2 * num_tokens * hkv * d * 2 + 8 * num_tokens
+    written = (d + 4) if kv_dtype == "int8" else 2 * d
+    return 2 * num_tokens * hkv * (2 * d + written) + 8 * num_tokens
 
 
 # ---------------------------------------------------------------------------
@@ -123,12 +126,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (runs in a fresh process: no CUDA, one BLAS thread)
 
-def oracle_step_sample(idx, max_seconds, out_json=True):
+def oracle_step_sample(idx, max_seconds, out_json=True, kv="bf16"):
     """Times the float64 oracle on a bounded sample of the workload's step.
 
     The sample is the first n sequences of the batch (cache write of their
     new tokens + their decode), n grown until one sample takes >= 0.2 s or
-    covers the batch; repeated until ``max_seconds`` have passed.
+    covers the batch; repeated until ``max_seconds`` have passed.  With
+    ``kv="int8"`` the oracle's INT8 cache write and decode run over the pool
+    quantised once beforehand (untimed).
     Returns GB/s over the sample's algorithmic bytes.
     """
     import numpy as np
@@ -153,6 +158,17 @@ def oracle_step_sample(idx, max_seconds, out_json=True):
             OA.decode_sequence(w.q[b], w.k_cache, w.v_cache, tables[b], int(w.context_lens[b]),
                                w.scale, w.block_size)
 
+    if kv == "int8":
+        from oracle import quant as OQ
+        kc8, ks8 = OQ.quantize_int8(w.k_cache)
+        vc8, vs8 = OQ.quantize_int8(w.v_cache)
+
+        def run(nseq):  # noqa: F811
+            OQ.reshape_and_cache_int8(w.key[:nseq], w.value[:nseq], kc8, vc8, ks8, vs8,
+                                      slots[:nseq], w.block_size, inplace=True)
+            OQ.decode_int8(w.q[:nseq], kc8, vc8, ks8, vs8, tables[:nseq],
+                           w.context_lens[:nseq], w.scale, w.block_size)
+
     nseq = 1
     while True:
         t = time.perf_counter()
@@ -168,21 +184,21 @@ def oracle_step_sample(idx, max_seconds, out_json=True):
         total += time.perf_counter() - t
         reps += 1
     nbytes = decode_bytes(w.context_lens[:nseq], nseq, w.num_q_heads, w.num_kv_heads,
-                          w.head_dim, w.block_size) + cache_write_bytes(nseq, w.num_kv_heads,
-                                                                        w.head_dim)
+                          w.head_dim, w.block_size, kv) + cache_write_bytes(
+                              nseq, w.num_kv_heads, w.head_dim, kv)
     res = {"value": nbytes * reps / total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
            "sample": f"first {nseq} of {w.num_seqs} sequences of the step (cache write + "
-                     f"float64 decode), {reps} repetitions, {total:.1f} s",
+                     f"float64 decode, {kv} KV), {reps} repetitions, {total:.1f} s",
            "seconds_per_sample": total / reps, "seqs": nseq, "bytes_per_sample": nbytes}
     if out_json:
         print(json.dumps(res))
     return res
 
 
-def cpu_baseline(idx, seconds):
+def cpu_baseline(idx, seconds, kv="bf16"):
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    code = ("import bench, sys; bench.oracle_step_sample(%d, %f)" % (idx, seconds))
+    code = ("import bench, sys; bench.oracle_step_sample(%d, %f, kv=%r)" % (idx, seconds, kv))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     if r.returncode != 0:
@@ -289,7 +305,7 @@ def combine_ranks(local_seconds, step_bytes, steps, world, device="cpu"):
 # ---------------------------------------------------------------------------
 # GPU arm
 
-def _setup(idx, device, replicas_min_bytes):
+def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
     import numpy as np
     import torch
 
@@ -338,11 +354,32 @@ def _setup(idx, device, replicas_min_bytes):
         k0, v0 = bf(w.k_cache), bf(w.v_cache)
         replicas = [[(k0, v0)]] + [[(k0.clone(), v0.clone())] for _ in range(nrep - 1)]
         qs, keys, vals = [bf(w.q)], [bf(w.key)], [bf(w.value)]
+    if kv_dtype == "int8":
+        # synthetic INT8 pools of the same shape: codes uniform in [-127, 127],
+        # scales as N(0, 1) rows give (about 3.5 / 127)
+        gen = torch.Generator(device=device)
+        gen.manual_seed(283 + idx)
+
+        def int8_pool():
+            nb = w.num_blocks
+            shape = (nb, w.num_kv_heads, w.block_size, w.head_dim)
+            return (torch.randint(-127, 128, shape, generator=gen, device=device,
+                                  dtype=torch.int8),
+                    torch.randint(-127, 128, shape, generator=gen, device=device,
+                                  dtype=torch.int8),
+                    torch.rand(shape[:3], generator=gen, device=device) * 0.01 + 0.02,
+                    torch.rand(shape[:3], generator=gen, device=device) * 0.01 + 0.02)
+        pool_bytes = 2 * w.num_blocks * w.num_kv_heads * w.block_size * (w.head_dim + 4)
+        if layers > 1:
+            replicas = [[int8_pool() for _ in range(layers)]]
+        else:
+            nrep = max(2, -(-replicas_min_bytes // pool_bytes))
+            replicas = [[int8_pool()] for _ in range(nrep)]
     st = {
         "w": w, "bt": torch.from_numpy(bt).to(device), "ctx": torch.from_numpy(ctx).to(device),
         "slots": torch.from_numpy(slots).to(device), "replicas": replicas, "q": qs,
         "key": keys, "value": vals, "bt_host": bt, "ctx_host": ctx, "slots_host": slots,
-        "pool_bytes": pool_bytes,
+        "pool_bytes": pool_bytes, "kv": kv_dtype,
     }
     return st
 
@@ -359,25 +396,35 @@ def _attn_fns(st, attn, partition):
         ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
                                  int(w.context_lens.max()), partition, st["q"][0].device)
 
-    def attend(layer, kc, vc):
-        if attn == "splitk":
-            pa.pa_decode_splitk(*ws, st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale,
-                                partition_size=partition)
-            pa.pa_splitk_reduce(outs[layer], *ws, st["ctx"], partition_size=partition)
-        else:
-            pa.pa_decode(outs[layer], st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale)
+    i8 = st.get("kv") == "int8"
 
-    def dominant(layer, kc, vc):
+    def dominant(layer, *pool):
+        q = st["q"][layer]
         if attn == "splitk":
-            pa.pa_decode_splitk(*ws, st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale,
-                                partition_size=partition)
+            if i8:
+                pa.pa_decode_splitk_int8(*ws, q, *pool, st["bt"], st["ctx"], w.scale,
+                                         partition_size=partition)
+            else:
+                pa.pa_decode_splitk(*ws, q, *pool, st["bt"], st["ctx"], w.scale,
+                                    partition_size=partition)
+        elif i8:
+            pa.pa_decode_int8(outs[layer], q, *pool, st["bt"], st["ctx"], w.scale)
         else:
-            pa.pa_decode(outs[layer], st["q"][layer], kc, vc, st["bt"], st["ctx"], w.scale)
+            pa.pa_decode(outs[layer], q, *pool, st["bt"], st["ctx"], w.scale)
+
+    def attend(layer, *pool):
+        dominant(layer, *pool)
+        if attn == "splitk":
+            pa.pa_splitk_reduce(outs[layer], *ws, st["ctx"], partition_size=partition)
 
     def step(r):
-        for layer, (kc, vc) in enumerate(st["replicas"][r]):
-            pa.pa_reshape_and_cache(st["key"][layer], st["value"][layer], kc, vc, st["slots"])
-            attend(layer, kc, vc)
+        for layer, pool in enumerate(st["replicas"][r]):
+            if i8:
+                pa.pa_reshape_and_cache_int8(st["key"][layer], st["value"][layer], *pool,
+                                             st["slots"])
+            else:
+                pa.pa_reshape_and_cache(st["key"][layer], st["value"][layer], *pool, st["slots"])
+            attend(layer, *pool)
 
     return step, dominant, outs
 
@@ -440,7 +487,7 @@ def run_gpu(args):
         print(f"bench: --gpus {args.gpus} but WORLD_SIZE={world}", file=sys.stderr)
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(args.workload, args.cpu_seconds)
+        base = cpu_baseline(args.workload, args.cpu_seconds, args.kv)
     if world > 1:
         dist.init_process_group("nccl")
     device = torch.device("cuda", local)
@@ -457,7 +504,7 @@ def run_gpu(args):
         pass
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
-    st = _setup(args.workload, device, 4 * l2)
+    st = _setup(args.workload, device, 4 * l2, args.kv)
     w = st["w"]
     stream = torch.cuda.Stream(device)
     attn = args.attn
@@ -495,8 +542,8 @@ def run_gpu(args):
 
     # dominant kernel alone: graphs of back-to-back launches over the replicas
     def dom_all(r):
-        for layer, (kc, vc) in enumerate(st["replicas"][r]):
-            dominant(layer, kc, vc)
+        for layer, pool in enumerate(st["replicas"][r]):
+            dominant(layer, *pool)
     dom_graphs = [_capture(lambda r=r: dom_all(r), stream) for r in range(len(st["replicas"]))]
     _time_graphs(dom_graphs, 20, stream)
     n_dom = max(args.steps, 50)
@@ -507,10 +554,11 @@ def run_gpu(args):
     assert pa.pa_get_device_error() == 0, "device error word set during the run"
 
     step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
-                                          w.num_kv_heads, w.head_dim, w.block_size)
-                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim))
+                                          w.num_kv_heads, w.head_dim, w.block_size, args.kv)
+                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
+                                                 args.kv))
     dom_bytes = decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads, w.num_kv_heads,
-                             w.head_dim, w.block_size)
+                             w.head_dim, w.block_size, args.kv)
     dt_max, value = combine_ranks(dt, step_bytes, args.steps, world, device)
     hbm_peak = peaks.get("hbm_gbs")
     achieved = dom_bytes / dom_dt / 1e9
@@ -518,9 +566,10 @@ def run_gpu(args):
                 "peak": hbm_peak if hbm_peak else 6800.0, "unit": "GB/s",
                 "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(
-                    "pa_decode_splitk" if attn == "splitk" else "pa_decode", w.name,
-                    args.partition),
-                "kernel": "pa_decode_splitk" if attn == "splitk" else "pa_decode",
+                    ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
+                    + ("_int8" if args.kv == "int8" else ""), w.name, args.partition),
+                "kernel": ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
+                + ("_int8" if args.kv == "int8" else ""),
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
                 else "fallback 6.8 TB/s",
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_dt * 1e6, 2)}
@@ -528,14 +577,16 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": args.kv, "data": "synthetic",
         "config": {
             "workload": w.name, "batch": w.num_seqs, "layers": w.layers,
             "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(np.mean(w.context_lens)), "new_tokens_per_step": w.num_seqs,
-            "attention": ("pa_decode_splitk+pa_splitk_reduce, partition %d" % args.partition)
-            if attn == "splitk" else "pa_decode",
+            "attention": ("pa_decode_splitk%s+pa_splitk_reduce, partition %d"
+                          % ("_int8" if args.kv == "int8" else "", args.partition))
+            if attn == "splitk" else ("pa_decode_int8" if args.kv == "int8" else "pa_decode"),
+            "kv_cache": args.kv,
             "graph": "one CUDA graph per step (cache write + attention)",
             "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
                   % (len(st["replicas"]), st["pool_bytes"] / 1e6, l2 / 1e6)
@@ -601,11 +652,13 @@ def _e2e(st, attn, args, stream):
             views[(name, layer)] = staged[off:off + n].view(t.dtype).view(t.shape)
         out = torch.empty((layers,) + tuple(st["q"][0].shape), dtype=torch.bfloat16, device=dev)
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        steps = [[pa.DecodeStep(views[("key", l)], views[("value", l)], kc, vc,
+        steps = [[pa.DecodeStep(views[("key", l)], views[("value", l)], pool[0], pool[1],
                                 views[("slots", 0)], views[("q", l)], views[("bt", 0)],
                                 views[("ctx", 0)], out[l], w.scale, split=attn == "splitk",
-                                partition_size=args.partition, workspace=ws, stream=stream)
-                  for l, (kc, vc) in enumerate(st["replicas"][r])] for r in range(nrep)]
+                                partition_size=args.partition, workspace=ws, stream=stream,
+                                k_scales=pool[2] if len(pool) == 4 else None,
+                                v_scales=pool[3] if len(pool) == 4 else None)
+                  for l, pool in enumerate(st["replicas"][r])] for r in range(nrep)]
         sets.append({"host": host, "staged": staged, "out": out, "hout": hout, "steps": steps,
                      "in_done": torch.cuda.Event(), "computed": torch.cuda.Event(),
                      "out_done": torch.cuda.Event()})
@@ -638,8 +691,9 @@ def _e2e(st, attn, args, stream):
     torch.cuda.synchronize()
     dt = time.perf_counter() - t
     step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
-                                          w.num_kv_heads, w.head_dim, w.block_size)
-                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim))
+                                          w.num_kv_heads, w.head_dim, w.block_size, st["kv"])
+                             + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
+                                                 st["kv"]))
     h2d = sum(t.numel() * t.element_size() for _, _, t in pieces)
     return {"value": round(step_bytes * n / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(sets[0]["hout"].numel() * 2),
@@ -706,6 +760,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
+                    help="KV cache element type (int8: one fp32 scale per token and head)")
     ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
                     help="copy_blocks: time pa_copy_blocks on a parallel-sampling step")
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])

@@ -10,6 +10,7 @@
  *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
  *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
+ *   *_int8                 the cache write and decode over an INT8 KV cache
  *   pa_alloc_*             fixed-size block allocator with reference counts,
  *                          copy-on-write and automatic prefix caching (host
  *                          only, never on the GPU path)
@@ -167,6 +168,45 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache,
                     int num_seqs, int num_q_heads, int num_kv_heads,
                     int head_dim, int block_size, int num_blocks, float scale,
                     pa_stream_t stream);
+
+/*
+ * INT8 KV cache (quantised KV; "Visual walkthrough", Step 1: one stored number
+ * costs p = 2 bytes in FP16/BF16, 1 byte in INT8).  The pages give no scaling
+ * scheme; here every (token, KV head) row is quantised symmetrically with its
+ * own fp32 scale, so a token is written once and never re-quantised:
+ *   scale = max|x| / 127,  code = clamp(round_half_even(x / scale), -127, 127)
+ * (fp32 arithmetic; scale 0 and codes 0 for an all-zero row).  Pools:
+ *   k_cache, v_cache   : [num_blocks, num_kv_heads, block_size, head_dim] int8
+ *   k_scales, v_scales : [num_blocks, num_kv_heads, block_size] fp32
+ * 2 * (head_dim + 4) bytes per token and KV head instead of 4 * head_dim.
+ * Decode quantises each query head the same way and takes QK as an integer
+ * dot product, s_j = scale * scale_q * k_scale_j * sum_d q_code_d * k_code_jd
+ * (exact in int32); PV runs in fp32 on the dequantised V (v_scale_j folded
+ * into softmax weight j).  head_dim 64 or 128; otherwise as the bf16 calls.
+ */
+pa_status pa_reshape_and_cache_int8(const void* key, const void* value,
+                                    int8_t* k_cache, int8_t* v_cache,
+                                    float* k_scales, float* v_scales,
+                                    const int64_t* slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_stream_t stream);
+pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache,
+                         const int8_t* v_cache, const float* k_scales,
+                         const float* v_scales, const int32_t* block_tables,
+                         int max_blocks_per_seq, const int32_t* context_lens,
+                         int num_seqs, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, float scale,
+                         pa_stream_t stream);
+/* Split-K partition pass over an INT8 cache; merge with pa_splitk_reduce. */
+pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l,
+                                int max_partitions, const void* q,
+                                const int8_t* k_cache, const int8_t* v_cache,
+                                const float* k_scales, const float* v_scales,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs,
+                                int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, float scale,
+                                int partition_size, pa_stream_t stream);
 
 /* Bytes of fp32 workspace pa_decode_splitk needs for contexts up to
  * max_context_len: ws_out [B, Hq, P, D] + ws_m [B, Hq, P] + ws_l [B, Hq, P]

@@ -150,6 +150,37 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_l
   return PA_OK;
 }
 
+pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* k_cache,
+                                    int8_t* v_cache, float* k_scales, float* v_scales,
+                                    const int64_t* slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (num_tokens == 0) return PA_OK;
+  if (!ok_ptr(key, 16) || !ok_ptr(value, 16) || !ok_ptr(k_cache, 16) || !ok_ptr(v_cache, 16) ||
+      !ok_ptr(k_scales, 16) || !ok_ptr(v_scales, 16) || !ok_ptr(slot_mapping, 8))
+    return PA_ERR_INVALID_ARG;
+  CacheWriteParams p{};
+  p.key = static_cast<const __nv_bfloat16*>(key);
+  p.value = static_cast<const __nv_bfloat16*>(value);
+  p.k8 = k_cache;
+  p.v8 = v_cache;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.slot_mapping = slot_mapping;
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  p.num_tokens = num_tokens;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  cudaError_t e = launch_reshape_and_cache_int8(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 namespace {
 
 // Checks shared by pa_decode and pa_decode_splitk.
@@ -281,6 +312,76 @@ pa_status pa_splitk_reduce(void* out, const float* ws_out, const float* ws_m, co
   p.err = device_error_word();
   if (!p.err) return cuda_fail(cudaGetLastError());
   cudaError_t e = launch_splitk_reduce(p, head_dim, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                         const float* k_scales, const float* v_scales,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, pa_stream_t stream) {
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale);
+  if (s != PA_OK || num_seqs == 0) return s;
+  if (!ok_ptr(out, 16) || !ok_ptr(k_scales, 16) || !ok_ptr(v_scales, 16))
+    return PA_ERR_INVALID_ARG;
+  DecodeParams p = make_decode_params(q, nullptr, nullptr, block_tables, max_blocks_per_seq,
+                                      context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      num_blocks, scale);
+  p.k8 = k_cache;
+  p.v8 = v_cache;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.max_partitions = 1;
+  p.partition_blocks = max_blocks_per_seq;
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, false,
+                                reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l, int max_partitions,
+                                const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                const float* k_scales, const float* v_scales,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, int partition_size, pa_stream_t stream) {
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale);
+  if (s != PA_OK) return s;
+  if (max_partitions <= 0 || max_partitions > 65535 || partition_size <= 0 ||
+      partition_size % block_size != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!ok_ptr(ws_out, 16) || !ok_ptr(ws_m, 4) || !ok_ptr(ws_l, 4) || !ok_ptr(k_scales, 16) ||
+      !ok_ptr(v_scales, 16))
+    return PA_ERR_INVALID_ARG;
+  DecodeParams p = make_decode_params(q, nullptr, nullptr, block_tables, max_blocks_per_seq,
+                                      context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      num_blocks, scale);
+  p.k8 = k_cache;
+  p.v8 = v_cache;
+  p.k_scales = k_scales;
+  p.v_scales = v_scales;
+  p.ws_o = ws_out;
+  p.ws_m = ws_m;
+  p.ws_l = ws_l;
+  p.max_partitions = max_partitions;
+  p.partition_blocks = partition_size / block_size;
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true,
+                                reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 

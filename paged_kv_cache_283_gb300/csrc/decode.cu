@@ -65,21 +65,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 #ifndef PA_WHOLE_STAGES_D128
 #define PA_WHOLE_STAGES_D128 2
 #endif
-template <int D, bool SPLIT>
+template <int D, bool SPLIT, bool I8>
 struct Pipe {  // head_dim 64: 2 KiB tiles, deeper rings
   static constexpr int NW = 4;
-  static constexpr int S = 4;
+  static constexpr int S = I8 ? 8 : 4;
 };
-template <bool SPLIT>
-struct Pipe<128, SPLIT> {
+// An INT8 stage holds half the bytes of a bf16 one: twice the stages keep the
+// same bytes in flight in about the same shared memory.
+template <bool SPLIT, bool I8>
+struct Pipe<128, SPLIT, I8> {
   static constexpr int NW = SPLIT ? PA_SPLIT_WARPS_D128 : PA_WHOLE_WARPS_D128;
-  static constexpr int S = SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128;
+  static constexpr int S = (SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128) * (I8 ? 2 : 1);
 };
 
-template <int D, int G, int NW, int S>
+template <int D, int G, int NW, int S, bool I8>
 struct SmemLayout {
   using Geo = Geometry<D, G>;
-  static constexpr int TILES = S * 2 * Geo::TILE;  // per stage: K tile then V tile
+  // one stage: K tile, V tile (bf16, or int8 codes followed by 16 K and 16 V scales)
+  static constexpr int KT = I8 ? Geo::BS * D : Geo::TILE;      // bytes of one K (or V) tile
+  static constexpr int STAGE = I8 ? 2 * KT + 2 * Geo::BS * 4 : 2 * KT;
+  static constexpr int TILES = S * STAGE;
   static constexpr int PS = Geo::BS * G * 4;       // softmax weights of one tile
   static constexpr int ALPHA = ((G * 4 + 15) / 16) * 16;
   static constexpr int BARS = S * 8;
@@ -87,16 +92,16 @@ struct SmemLayout {
   static constexpr int WARP = ((TILES + PS + ALPHA + BARS + 127) / 128) * 128;
   static constexpr int TOTAL = NW * WARP;
   static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
+  static_assert(STAGE % 16 == 0 && KT % 16 == 0, "bulk copy sizes");
 };
-
 // Small CTAs are meant to share an SM three at a time: give the register
 // allocator that budget (<= 168 per thread) instead of its default guess;
 // groups of 8 heads need more registers than that and get one CTA's worth.
-template <int D, int G, int NW, int S, bool SPLIT>
+template <int D, int G, int NW, int S, bool SPLIT, bool I8>
 __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
     paged_decode_kernel(const DecodeParams p) {
   using Geo = Geometry<D, G>;
-  using Lay = SmemLayout<D, G, NW, S>;
+  using Lay = SmemLayout<D, G, NW, S, I8>;
   constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
   extern __shared__ __align__(128) unsigned char smem[];
 
@@ -126,6 +131,8 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
   int ctx = __ldg(p.context_lens + b);
   int ids_cur = load_ids(0);
   float2 q2[G][4];
+  int qc[G][2];    // int8 cache: q codes, 4 per word
+  float qsc[G];    // int8 cache: q scale times scale * log2(e)
   {
     const __nv_bfloat16* qb =
         p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
@@ -133,13 +140,44 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
 #pragma unroll
     for (int g = 0; g < G; ++g)
       qw[g] = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D));
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    if constexpr (!I8) {
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
-      q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
-      q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
-      q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
+      for (int g = 0; g < G; ++g) {
+        q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
+        q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
+        q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
+        q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
+      }
+    } else {
+      // q of each head to int8 codes with one fp32 scale (the cache's rule:
+      // scale = amax / 127, code = round-half-even(q / scale)); the scores
+      // then carry scale_q * scale * log2(e).
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float f[8];
+        const float2 a = bf16x2_to_float2(qw[g].x), b2 = bf16x2_to_float2(qw[g].y);
+        const float2 c = bf16x2_to_float2(qw[g].z), e = bf16x2_to_float2(qw[g].w);
+        f[0] = a.x; f[1] = a.y; f[2] = b2.x; f[3] = b2.y;
+        f[4] = c.x; f[5] = c.y; f[6] = e.x; f[7] = e.y;
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+#pragma unroll
+        for (int m = L / 2; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
+        const float qscale = __fdiv_rn(amax, 127.0f);
+        int packed[2] = {0, 0};
+        if (qscale > 0.f) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float c8 = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[k], qscale))));
+            packed[k / 4] |= (static_cast<int>(c8) & 0xff) << (8 * (k % 4));
+          }
+        }
+        qc[g][0] = packed[0];
+        qc[g][1] = packed[1];
+        qsc[g] = qscale * p.scale_log2;
+      }
     }
   }
 
@@ -202,11 +240,19 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
       }
       const int st = i % S;
       uint64_t* bar = &bars[st];
-      unsigned char* dst = tiles + st * 2 * Geo::TILE;
-      const size_t off = static_cast<size_t>(id) * block_stride + head_off;
-      mbar_arrive_expect_tx(bar, 2 * Geo::TILE);
-      bulk_copy_g2s(dst, p.k_cache + off, Geo::TILE, bar, policy);
-      bulk_copy_g2s(dst + Geo::TILE, p.v_cache + off, Geo::TILE, bar, policy);
+      unsigned char* dst = tiles + st * Lay::STAGE;
+      const size_t off = static_cast<size_t>(id) * block_stride + head_off;  // elements
+      mbar_arrive_expect_tx(bar, Lay::STAGE);
+      if constexpr (!I8) {
+        bulk_copy_g2s(dst, p.k_cache + off, Lay::KT, bar, policy);
+        bulk_copy_g2s(dst + Lay::KT, p.v_cache + off, Lay::KT, bar, policy);
+      } else {
+        const size_t soff = off / D;  // scales: one per token
+        bulk_copy_g2s(dst, p.k8 + off, Lay::KT, bar, policy);
+        bulk_copy_g2s(dst + Lay::KT, p.v8 + off, Lay::KT, bar, policy);
+        bulk_copy_g2s(dst + 2 * Lay::KT, p.k_scales + soff, BS * 4, bar, policy);
+        bulk_copy_g2s(dst + 2 * Lay::KT + BS * 4, p.v_scales + soff, BS * 4, bar, policy);
+      }
     }
     issued = i + 1;
   };
@@ -231,14 +277,28 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
     if (!ready) break;
     const int j = jb + warp + i * NW;
     const int nvalid = min(BS, ctx - j * BS);
-    const uint4* kt = reinterpret_cast<const uint4*>(tiles + st * 2 * Geo::TILE);
-    const uint4* vt = kt + Geo::TILE / 16;
-    if (nvalid == BS)
-      tile_step<D, G, true>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub, rg,
-                            my_head, my_i0);
-    else
-      tile_step<D, G, false>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub, rg,
-                             my_head, my_i0);
+    const unsigned char* stage = tiles + st * Lay::STAGE;
+    if constexpr (!I8) {
+      const uint4* kt = reinterpret_cast<const uint4*>(stage);
+      const uint4* vt = reinterpret_cast<const uint4*>(stage + Lay::KT);
+      if (nvalid == BS)
+        tile_step<D, G, true>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub, rg,
+                              my_head, my_i0);
+      else
+        tile_step<D, G, false>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub,
+                               rg, my_head, my_i0);
+    } else {
+      const uint2* kt = reinterpret_cast<const uint2*>(stage);
+      const uint2* vt = reinterpret_cast<const uint2*>(stage + Lay::KT);
+      const float* ksc = reinterpret_cast<const float*>(stage + 2 * Lay::KT);
+      const float* vsc = ksc + BS;
+      if (nvalid == BS)
+        tile_step_i8<D, G, true>(kt, vt, ksc, vsc, ps, alpha_s, qc, qsc, acc, m_run, l_run,
+                                 nvalid, lane, sub, rg, my_head, my_i0);
+      else
+        tile_step_i8<D, G, false>(kt, vt, ksc, vsc, ps, alpha_s, qc, qsc, acc, m_run, l_run,
+                                  nvalid, lane, sub, rg, my_head, my_i0);
+    }
     consumed = i + 1;
     __syncwarp();  // every lane is done with this stage and with ps / alpha_s
     if (i + S < nw) issue(i + S);
@@ -346,27 +406,33 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
   return e;
 }
 
-template <int D, int G, bool SPLIT>
+template <int D, int G, bool SPLIT, bool I8>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
-  constexpr int NW = Pipe<D, SPLIT>::NW, S = Pipe<D, SPLIT>::S;
-  using Lay = SmemLayout<D, G, NW, S>;
+  constexpr int NW = Pipe<D, SPLIT, I8>::NW, S = Pipe<D, SPLIT, I8>::S;
+  using Lay = SmemLayout<D, G, NW, S, I8>;
   static std::atomic<uint64_t> smem_set{0};
-  auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT>;
+  auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, I8>;
   cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
   return launch_pdl(kernel, grid, dim3(NW * 32), Lay::TOTAL, stream, p);
 }
 
-template <int D>
+template <int D, int G, bool I8>
+cudaError_t launch_decode_g(const DecodeParams& p, bool split, cudaStream_t stream) {
+  return split ? launch_decode_t<D, G, true, I8>(p, stream)
+               : launch_decode_t<D, G, false, I8>(p, stream);
+}
+
+template <int D, bool I8>
 cudaError_t launch_decode_d(const DecodeParams& p, int group, bool split, cudaStream_t stream) {
   switch (group) {
     case 2:
-      return split ? launch_decode_t<D, 2, true>(p, stream) : launch_decode_t<D, 2, false>(p, stream);
+      return launch_decode_g<D, 2, I8>(p, split, stream);
     case 4:
-      return split ? launch_decode_t<D, 4, true>(p, stream) : launch_decode_t<D, 4, false>(p, stream);
+      return launch_decode_g<D, 4, I8>(p, split, stream);
     case 8:
-      return split ? launch_decode_t<D, 8, true>(p, stream) : launch_decode_t<D, 8, false>(p, stream);
+      return launch_decode_g<D, 8, I8>(p, split, stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -381,8 +447,13 @@ bool decode_shape_supported(int head_dim, int group, int block_size) {
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool split,
                           cudaStream_t stream) {
-  if (head_dim == 128) return launch_decode_d<128>(p, group, split, stream);
-  if (head_dim == 64) return launch_decode_d<64>(p, group, split, stream);
+  const bool i8 = p.k8 != nullptr;
+  if (head_dim == 128)
+    return i8 ? launch_decode_d<128, true>(p, group, split, stream)
+              : launch_decode_d<128, false>(p, group, split, stream);
+  if (head_dim == 64)
+    return i8 ? launch_decode_d<64, true>(p, group, split, stream)
+              : launch_decode_d<64, false>(p, group, split, stream);
   return cudaErrorInvalidValue;
 }
 

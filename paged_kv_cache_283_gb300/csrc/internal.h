@@ -20,6 +20,10 @@ struct DecodeParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k_cache;
   const __nv_bfloat16* v_cache;
+  const int8_t* k8;        // int8 cache: codes [NB, Hkv, bs, D] (null for a bf16 cache)
+  const int8_t* v8;
+  const float* k_scales;   // int8 cache: one scale per (block, head, token)
+  const float* v_scales;
   const int32_t* block_tables;
   const int32_t* context_lens;
   unsigned* err;
@@ -58,6 +62,10 @@ struct CacheWriteParams {
   int head_dim;
   int block_size;
   int64_t num_slots;  // num_blocks * block_size
+  int8_t* k8;         // int8 cache (null for bf16): codes [NB, Hkv, bs, D]
+  int8_t* v8;
+  float* k_scales;    // [NB, Hkv, bs]
+  float* v_scales;
 };
 
 // Pools of up to kCopyMaxLayers layers go to one copy_blocks launch.
@@ -79,6 +87,7 @@ cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool s
                           cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream);
+cudaError_t launch_reshape_and_cache_int8(const CacheWriteParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, int num_pairs, int num_layers,
                                cudaStream_t stream);
 

@@ -50,7 +50,82 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheWrite
   *reinterpret_cast<uint4*>(p.v_cache + dst) = vv;
 }
 
+// INT8 cache write: one warp per (token, KV head) row quantises it with one
+// scale (scale = amax / 127, code = round-half-even(x / scale), fp32, as in
+// pa.h) and writes D codes and the scale.  Each lane owns D / 32 values.
+template <int D>
+__global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(const CacheWriteParams p) {
+  griddep_wait();
+  griddep_launch_dependents();
+  constexpr int PER = D / 32;  // values per lane: 4 at D = 128, 2 at D = 64
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<int64_t>(p.num_tokens) * p.num_kv_heads) return;  // warp-uniform
+  const int h = static_cast<int>(row % p.num_kv_heads);
+  const int64_t t = row / p.num_kv_heads;
+  const __nv_bfloat16* kp = p.key + row * D + lane * PER;
+  const __nv_bfloat16* vp = p.value + row * D + lane * PER;
+  uint32_t kw[PER / 2], vw[PER / 2];
+#pragma unroll
+  for (int i = 0; i < PER / 2; ++i) {
+    kw[i] = __ldg(reinterpret_cast<const unsigned int*>(kp) + i);
+    vw[i] = __ldg(reinterpret_cast<const unsigned int*>(vp) + i);
+  }
+  const int64_t slot = __ldg(p.slot_mapping + t);
+  if (slot < 0) return;
+  if (slot >= p.num_slots) {
+    if (lane == 0) raise_error(p.err, PA_DEVERR_SLOT);
+    return;
+  }
+  const int64_t blk = slot / p.block_size;
+  const int64_t off = slot % p.block_size;
+  const int64_t srow = (blk * p.num_kv_heads + h) * p.block_size + off;  // scale index
+  for (int which = 0; which < 2; ++which) {
+    float f[PER];
+#pragma unroll
+    for (int i = 0; i < PER / 2; ++i) {
+      const float2 x = bf16x2_to_float2(which ? vw[i] : kw[i]);
+      f[2 * i] = x.x;
+      f[2 * i + 1] = x.y;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(f[i]));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
+    const float scale = __fdiv_rn(amax, 127.0f);
+    uint32_t packed = 0;
+    if (scale > 0.f) {
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        const float c = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[i], scale))));
+        packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * i);
+      }
+    }
+    int8_t* dst = (which ? p.v8 : p.k8) + srow * D + lane * PER;
+    if constexpr (PER == 4)
+      *reinterpret_cast<uint32_t*>(dst) = packed;
+    else
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(packed);
+    if (lane == 0) (which ? p.v_scales : p.k_scales)[srow] = scale;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_reshape_and_cache_int8(const CacheWriteParams& p, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  if (p.head_dim == 128)
+    return launch_pdl(reshape_and_cache_int8_kernel<128>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(256), 0, stream, p);
+  if (p.head_dim == 64)
+    return launch_pdl(reshape_and_cache_int8_kernel<64>, dim3(static_cast<unsigned>(blocks)),
+                      dim3(256), 0, stream, p);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_kv_heads * (p.head_dim / 8);

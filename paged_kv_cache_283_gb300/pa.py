@@ -38,6 +38,12 @@ SIGNATURES = {
     "pa_decode_supported": (_i, [_i, _i, _i, _i]),
     "pa_reshape_and_cache": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "pa_copy_blocks": (_i, [_vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _vp]),
+    "pa_reshape_and_cache_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                       _vp]),
+    "pa_decode_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                            _f, _vp]),
+    "pa_decode_splitk_int8": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                   _i, _i, _i, _i, _i, _f, _i, _vp]),
     "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "pa_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
@@ -204,6 +210,72 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, strea
     _check(st, "pa_decode")
 
 
+def _int8_pools(k_cache, v_cache, k_scales, v_scales):
+    torch = _torch()
+    nb, hkv, bs, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_scales.shape != (nb, hkv, bs) or \
+            v_scales.shape != k_scales.shape:
+        raise ValueError("int8 cache: pools [NB, Hkv, bs, D] int8, scales [NB, Hkv, bs] fp32")
+    return (_dev(k_cache, torch.int8, "k_cache", 4), _dev(v_cache, torch.int8, "v_cache", 4),
+            _dev(k_scales, torch.float32, "k_scales", 3),
+            _dev(v_scales, torch.float32, "v_scales", 3)), (nb, hkv, bs, d)
+
+
+def pa_reshape_and_cache_int8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                              stream=None):
+    """key/value [T, Hkv, D] bf16 quantised into int8 pools + fp32 scales."""
+    torch = _torch()
+    T, hkv, d = key.shape
+    (pk, pv, pks, pvs), (nb, hkv2, bs, d2) = _int8_pools(k_cache, v_cache, k_scales, v_scales)
+    if value.shape != key.shape or (hkv, d) != (hkv2, d2) or slot_mapping.shape != (T,):
+        raise ValueError("pa_reshape_and_cache_int8: inconsistent shapes")
+    st = lib().pa_reshape_and_cache_int8(
+        _dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3), pk, pv,
+        pks, pvs, _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb,
+        _stream(stream))
+    _check(st, "pa_reshape_and_cache_int8")
+
+
+def _decode_int8_common(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens):
+    torch = _torch()
+    B, hq, d = q.shape
+    pools, (nb, hkv, bs, d2) = _int8_pools(k_cache, v_cache, k_scales, v_scales)
+    if d != d2 or block_tables.dim() != 2 or block_tables.shape[0] != B or \
+            context_lens.shape != (B,):
+        raise ValueError("int8 decode: inconsistent shapes")
+    return (_dev(q, torch.bfloat16, "q", 3),) + pools + (
+        _dev(block_tables, torch.int32, "block_tables", 2),
+        _dev(context_lens, torch.int32, "context_lens", 1)), (B, hq, hkv, d, bs, nb,
+                                                              block_tables.shape[1])
+
+
+def pa_decode_int8(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens,
+                   scale, stream=None):
+    torch = _torch()
+    (pq, pk, pv, pks, pvs, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_int8_common(
+        q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode_int8: out must match q")
+    st = lib().pa_decode_int8(_dev(out, torch.bfloat16, "out", 3), pq, pk, pv, pks, pvs, pt, mb,
+                              pc, B, hq, hkv, d, bs, nb, float(scale), _stream(stream))
+    _check(st, "pa_decode_int8")
+
+
+def pa_decode_splitk_int8(ws_out, ws_m, ws_l, q, k_cache, v_cache, k_scales, v_scales,
+                          block_tables, context_lens, scale, partition_size=512, stream=None):
+    torch = _torch()
+    (pq, pk, pv, pks, pvs, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_int8_common(
+        q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens)
+    maxp = ws_m.shape[2]
+    if ws_out.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape or ws_m.shape[:2] != (B, hq):
+        raise ValueError("pa_decode_splitk_int8: workspace shapes")
+    st = lib().pa_decode_splitk_int8(
+        _dev(ws_out, torch.float32, "ws_out", 4), _dev(ws_m, torch.float32, "ws_m", 3),
+        _dev(ws_l, torch.float32, "ws_l", 3), maxp, pq, pk, pv, pks, pvs, pt, mb, pc, B, hq, hkv,
+        d, bs, nb, float(scale), int(partition_size), _stream(stream))
+    _check(st, "pa_decode_splitk_int8")
+
+
 def pa_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len, partition_size):
     return int(lib().pa_splitk_workspace_bytes(num_seqs, num_q_heads, head_dim, max_context_len,
                                                partition_size))
@@ -284,7 +356,8 @@ class DecodeStep:
 
     def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                  context_lens, out, scale, split=True, partition_size=512,
-                 max_context_len=None, workspace=None, stream=None):
+                 max_context_len=None, workspace=None, stream=None, k_scales=None,
+                 v_scales=None):
         torch = _torch()
         T, hkv, d = key.shape
         nb, hkv2, bs, d2 = k_cache.shape
@@ -292,16 +365,27 @@ class DecodeStep:
             raise ValueError("DecodeStep: inconsistent key / cache shapes")
         if slot_mapping.shape != (T,):
             raise ValueError("DecodeStep: slot_mapping must be [num_tokens]")
-        (pq, pk, pv, pt, pc), (B, hq, _, _, _, _, mb) = _decode_common(
-            q, k_cache, v_cache, block_tables, context_lens)
+        self.int8 = k_cache.dtype == torch.int8
+        if self.int8:
+            (pq, pk, pv, pks, pvs, pt, pc), (B, hq, _, _, _, _, mb) = _decode_int8_common(
+                q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens)
+        else:
+            (pq, pk, pv, pt, pc), (B, hq, _, _, _, _, mb) = _decode_common(
+                q, k_cache, v_cache, block_tables, context_lens)
         if out.shape != q.shape:
             raise ValueError("DecodeStep: out must match q")
         po = _dev(out, torch.bfloat16, "out", 3)
         self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables, context_lens,
                       out]
         self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
-        self._rc = (_dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3),
-                    pk, pv, _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb)
+        kv = (_dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3))
+        sm = _dev(slot_mapping, torch.int64, "slot_mapping", 1)
+        if self.int8:
+            self._keep += [k_scales, v_scales]
+            self._rc = kv + (pk, pv, pks, pvs, sm, T, hkv, d, bs, nb)
+        else:
+            self._rc = kv + (pk, pv, sm, T, hkv, d, bs, nb)
+        kvp = (pk, pv, pks, pvs) if self.int8 else (pk, pv)
         self.split = bool(split)
         if self.split:
             if workspace is None:
@@ -316,30 +400,35 @@ class DecodeStep:
             wo = _dev(ws_o, torch.float32, "ws_out", 4)
             wm = _dev(ws_m, torch.float32, "ws_m", 3)
             wl = _dev(ws_l, torch.float32, "ws_l", 3)
-            self._dk = (wo, wm, wl, maxp, pq, pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb,
-                        float(scale), int(partition_size))
+            self._dk = (wo, wm, wl, maxp, pq) + kvp + (pt, mb, pc, B, hq, hkv, d, bs, nb,
+                                                      float(scale), int(partition_size))
             self._rd = (po, wo, wm, wl, maxp, pc, B, hq, d, int(partition_size))
         else:
-            self._dc = (po, pq, pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale))
-        lib()
+            self._dc = (po, pq) + kvp + (pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale))
+        L = lib()
+        if self.int8:
+            self._f_write, self._f_split, self._f_whole = (
+                L.pa_reshape_and_cache_int8, L.pa_decode_splitk_int8, L.pa_decode_int8)
+        else:
+            self._f_write, self._f_split, self._f_whole = (
+                L.pa_reshape_and_cache, L.pa_decode_splitk, L.pa_decode)
 
     def __call__(self, stream=None):
-        L = _lib
         s = self._stream if stream is None and self._stream is not None else _stream(stream)
-        st = L.pa_reshape_and_cache(*self._rc, s)
+        st = self._f_write(*self._rc, s)
         if st != PA_OK:
-            _check(st, "DecodeStep: pa_reshape_and_cache")
+            _check(st, "DecodeStep: cache write")
         if self.split:
-            st = L.pa_decode_splitk(*self._dk, s)
+            st = self._f_split(*self._dk, s)
             if st != PA_OK:
-                _check(st, "DecodeStep: pa_decode_splitk")
-            st = L.pa_splitk_reduce(*self._rd, s)
+                _check(st, "DecodeStep: split-K partition pass")
+            st = _lib.pa_splitk_reduce(*self._rd, s)
             if st != PA_OK:
                 _check(st, "DecodeStep: pa_splitk_reduce")
         else:
-            st = L.pa_decode(*self._dc, s)
+            st = self._f_whole(*self._dc, s)
             if st != PA_OK:
-                _check(st, "DecodeStep: pa_decode")
+                _check(st, "DecodeStep: decode")
 
 
 def pa_get_device_error():
