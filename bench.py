@@ -430,13 +430,15 @@ def _attn_fns(st, attn, partition):
 
 
 def recorded_traffic(kernel, workload_name, partition):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source or the launch shape changed since the counters were taken."""
+    """DRAM bytes per launch from the committed ncu summaries, or None when the
+    kernel source or the launch shape changed since the counters were taken.
+    ``profiles/decode_traffic.txt`` holds one ``key=value`` record per kernel,
+    records separated by blank lines."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
-        kv = dict(line.strip().split("=", 1) for line in open(path)
-                  if "=" in line and not line.startswith("#"))
+        with open(path) as f:
+            blocks = f.read().split("\n\n")
         h = hashlib.sha256()
         for name in ("decode.cu", "decode_tile.cuh"):
             with open(os.path.join(ROOT, "paged_kv_cache_283_gb300", "csrc", name), "rb") as f:
@@ -444,10 +446,13 @@ def recorded_traffic(kernel, workload_name, partition):
         sha = h.hexdigest()
     except OSError:
         return None
-    if (sha.startswith(kv.get("kernel_source_sha256_prefix", "-")) and kv.get("kernel") == kernel
-            and kv.get("workload") == workload_name
-            and (kernel != "pa_decode_splitk" or int(kv.get("partition", -1)) == partition)):
-        return int(kv["dram_bytes_per_launch"])
+    for block in blocks:
+        kv = dict(line.strip().split("=", 1) for line in block.splitlines()
+                  if "=" in line and not line.startswith("#"))
+        if (kv and sha.startswith(kv.get("kernel_source_sha256_prefix", "-"))
+                and kv.get("kernel") == kernel and kv.get("workload") == workload_name
+                and ("splitk" not in kernel or int(kv.get("partition", -1)) == partition)):
+            return int(kv["dram_bytes_per_launch"])
     return None
 
 

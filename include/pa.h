@@ -179,10 +179,18 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache,
  *   k_cache, v_cache   : [num_blocks, num_kv_heads, block_size, head_dim] int8
  *   k_scales, v_scales : [num_blocks, num_kv_heads, block_size] fp32
  * 2 * (head_dim + 4) bytes per token and KV head instead of 4 * head_dim.
+ * v_cache only: inside each (block, head) tile of block_size * head_dim bytes,
+ * seen as 128-byte lines of eight 16-byte units, logical unit u of line L is
+ * stored at unit u ^ ((2 * L) & 7) (for head_dim 128 a line is one token, so
+ * token t's dims [16u, 16u + 16) sit at byte 16 * (u ^ (2t & 7)) of its row).
+ * The permutation lets the decode read V for its tensor-core MMAs without
+ * shared-memory bank conflicts; whole-block copies (pa_copy_blocks) are
+ * unaffected.  k_cache is plain row-major.
  * Decode quantises each query head the same way and takes QK as an integer
  * dot product, s_j = scale * scale_q * k_scale_j * sum_d q_code_d * k_code_jd
- * (exact in int32); PV runs in fp32 on the dequantised V (v_scale_j folded
- * into softmax weight j).  head_dim 64 or 128; otherwise as the bf16 calls.
+ * (exact in int32); PV weights w_j = softmax weight j * v_scale_j mix the V
+ * codes with fp32 accumulation (each weight carried as a sum of two tf32
+ * parts, ~2^-21 relative).  head_dim 64 or 128; otherwise as the bf16 calls.
  */
 pa_status pa_reshape_and_cache_int8(const void* key, const void* value,
                                     int8_t* k_cache, int8_t* v_cache,

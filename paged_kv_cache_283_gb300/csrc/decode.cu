@@ -65,18 +65,28 @@ constexpr float kLn2 = 0.6931471805599453f;
 #ifndef PA_WHOLE_STAGES_D128
 #define PA_WHOLE_STAGES_D128 2
 #endif
+// MINB is the number of CTAs meant to share an SM, handed to the register
+// allocator through __launch_bounds__.
 template <int D, bool SPLIT, bool I8>
 struct Pipe {  // head_dim 64: 2 KiB tiles, deeper rings
   static constexpr int NW = 4;
-  static constexpr int S = I8 ? 8 : 4;
+  static constexpr int S = I8 ? 6 : 4;
 };
-// An INT8 stage holds half the bytes of a bf16 one: twice the stages keep the
-// same bytes in flight in about the same shared memory.
 template <bool SPLIT, bool I8>
 struct Pipe<128, SPLIT, I8> {
   static constexpr int NW = SPLIT ? PA_SPLIT_WARPS_D128 : PA_WHOLE_WARPS_D128;
-  static constexpr int S = (SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128) * (I8 ? 2 : 1);
+  static constexpr int S = I8 ? 3 : (SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128);
 };
+// Small bf16 CTAs share an SM three at a time (<= 168 registers); groups of 8
+// heads need more registers than that and get one CTA's worth.  The INT8
+// kernel needs fewer registers and more warps to hide its latencies: four
+// 4-warp CTAs (two 8-warp ones) per SM, <= 128 registers, each warp with 3
+// stages of 4.2 KiB in flight (head_dim 128).
+template <int NW, int G, bool I8>
+constexpr int min_blocks() {
+  if constexpr (I8) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
+  else return (NW <= 4 && G <= 4) ? 3 : 1;
+}
 
 template <int D, int G, int NW, int S, bool I8>
 struct SmemLayout {
@@ -90,15 +100,15 @@ struct SmemLayout {
   static constexpr int BARS = S * 8;
   static constexpr int MERGE = (G * D + 2 * G) * 4;  // aliases TILES after the loop
   static constexpr int WARP = ((TILES + PS + ALPHA + BARS + 127) / 128) * 128;
-  static constexpr int TOTAL = NW * WARP;
+  // int8 cache: the CTA's quantised q, codes [G][D] then scales [G]
+  static constexpr int QOFF = NW * WARP;
+  static constexpr int QREG = I8 ? ((G * D + G * 4 + 127) / 128) * 128 : 0;
+  static constexpr int TOTAL = NW * WARP + QREG;
   static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
   static_assert(STAGE % 16 == 0 && KT % 16 == 0, "bulk copy sizes");
 };
-// Small CTAs are meant to share an SM three at a time: give the register
-// allocator that budget (<= 168 per thread) instead of its default guess;
-// groups of 8 heads need more registers than that and get one CTA's worth.
 template <int D, int G, int NW, int S, bool SPLIT, bool I8>
-__global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
+__global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, I8>()))
     paged_decode_kernel(const DecodeParams p) {
   using Geo = Geometry<D, G>;
   using Lay = SmemLayout<D, G, NW, S, I8>;
@@ -130,54 +140,73 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
   };
   int ctx = __ldg(p.context_lens + b);
   int ids_cur = load_ids(0);
+  using IG = I8Geometry<D, G>;
+  const int qsub = lane % IG::QL;  // int8 cache: this lane in the QK geometry
+  const int qrg = lane / IG::QL;
   float2 q2[G][4];
-  int qc[G][2];    // int8 cache: q codes, 4 per word
-  float qsc[G];    // int8 cache: q scale times scale * log2(e)
-  {
+  int qc[G][IG::QW];  // int8 cache: this lane's q codes, 4 per word
+  float qsc[G];       // int8 cache: q scale times scale * log2(e)
+  if constexpr (!I8) {
     const __nv_bfloat16* qb =
         p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
     uint4 qw[G];
 #pragma unroll
     for (int g = 0; g < G; ++g)
       qw[g] = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D));
-    if constexpr (!I8) {
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
-        q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
-        q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
-        q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
+    for (int g = 0; g < G; ++g) {
+      q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
+      q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
+      q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
+      q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
+    }
+  } else {
+    // q of each head to int8 codes with one fp32 scale, by the cache's rule
+    // (scale = amax / 127, code = round-half-even(q / scale)), once per CTA:
+    // warp w quantises heads w, w + NW, ... into shared memory, then every
+    // lane loads the codes it needs.  The scores carry scale_q * scale * log2 e.
+    constexpr int E = D / 32;  // values per lane
+    unsigned char* q8 = smem + Lay::QOFF;
+    float* qs = reinterpret_cast<float*>(smem + Lay::QOFF + G * D);
+    for (int g = warp; g < G; g += NW) {
+      const __nv_bfloat16* qh =
+          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + g) * D +
+          lane * E;
+      float f[E];
+      if constexpr (E == 4) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh));
+        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+        f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
+      } else {
+        const float2 a = bf16x2_to_float2(__ldg(reinterpret_cast<const unsigned int*>(qh)));
+        f[0] = a.x; f[1] = a.y;
       }
-    } else {
-      // q of each head to int8 codes with one fp32 scale (the cache's rule:
-      // scale = amax / 127, code = round-half-even(q / scale)); the scores
-      // then carry scale_q * scale * log2(e).
+      float amax = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float f[8];
-        const float2 a = bf16x2_to_float2(qw[g].x), b2 = bf16x2_to_float2(qw[g].y);
-        const float2 c = bf16x2_to_float2(qw[g].z), e = bf16x2_to_float2(qw[g].w);
-        f[0] = a.x; f[1] = a.y; f[2] = b2.x; f[3] = b2.y;
-        f[4] = c.x; f[5] = c.y; f[6] = e.x; f[7] = e.y;
-        float amax = 0.f;
+      for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
 #pragma unroll
-        for (int k = 0; k < 8; ++k) amax = fmaxf(amax, fabsf(f[k]));
+      for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
+      const float qscale = __fdiv_rn(amax, 127.0f);
+      uint32_t packed = 0;
+      if (qscale > 0.f) {
 #pragma unroll
-        for (int m = L / 2; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
-        const float qscale = __fdiv_rn(amax, 127.0f);
-        int packed[2] = {0, 0};
-        if (qscale > 0.f) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float c8 = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[k], qscale))));
-            packed[k / 4] |= (static_cast<int>(c8) & 0xff) << (8 * (k % 4));
-          }
+        for (int k = 0; k < E; ++k) {
+          const float c8 = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[k], qscale))));
+          packed |= (static_cast<uint32_t>(static_cast<int>(c8)) & 0xffu) << (8 * k);
         }
-        qc[g][0] = packed[0];
-        qc[g][1] = packed[1];
-        qsc[g] = qscale * p.scale_log2;
       }
+      if constexpr (E == 4)
+        *reinterpret_cast<uint32_t*>(q8 + g * D + lane * E) = packed;
+      else
+        *reinterpret_cast<uint16_t*>(q8 + g * D + lane * E) = static_cast<uint16_t>(packed);
+      if (lane == 0) qs[g] = qscale;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      i8_load_row<IG::QB>(q8 + g * D, qsub, qrg, qc[g]);
+      qsc[g] = qs[g] * p.scale_log2;
     }
   }
 
@@ -257,15 +286,26 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
     issued = i + 1;
   };
 
-  float2 acc[G][4];
+  float2 acc[G][4];  // bf16 cache: this lane's dims of each head
 #pragma unroll
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[g][k] = make_float2(0.f, 0.f);
+  float acc8[D / 16][4];  // int8 cache: MMA accumulators (pv_i8_mma's layout)
+#pragma unroll
+  for (int c = 0; c < D / 16; ++c)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) acc8[c][k] = 0.f;
   float m_run = -INFINITY;  // running max of this lane's head, base-2 units
   float l_run = 0.f;        // this lane's share of that head's exp-sum
-  const int my_head = (sub * R) / P;
-  const int my_i0 = (sub * R) % P;
+  // The lane geometry of the scores and softmax state: the bf16 step's, or
+  // the int8 QK geometry.
+  constexpr int SL = I8 ? IG::QL : L;
+  constexpr int SHL = I8 ? IG::HEAD_LANES : Geo::HEAD_LANES;
+  const int ssub = I8 ? qsub : sub;
+  const int srg = I8 ? qrg : rg;
+  const int my_head = I8 ? (qsub * IG::R) / IG::P : (sub * R) / P;
+  const int my_i0 = I8 ? (qsub * IG::R) % IG::P : (sub * R) % P;
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i);
@@ -288,16 +328,14 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
         tile_step<D, G, false>(kt, vt, ps, alpha_s, q2, acc, m_run, l_run, nvalid, lane, sub,
                                rg, my_head, my_i0);
     } else {
-      const uint2* kt = reinterpret_cast<const uint2*>(stage);
-      const uint2* vt = reinterpret_cast<const uint2*>(stage + Lay::KT);
       const float* ksc = reinterpret_cast<const float*>(stage + 2 * Lay::KT);
       const float* vsc = ksc + BS;
       if (nvalid == BS)
-        tile_step_i8<D, G, true>(kt, vt, ksc, vsc, ps, alpha_s, qc, qsc, acc, m_run, l_run,
-                                 nvalid, lane, sub, rg, my_head, my_i0);
+        tile_step_i8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
+                                 m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
       else
-        tile_step_i8<D, G, false>(kt, vt, ksc, vsc, ps, alpha_s, qc, qsc, acc, m_run, l_run,
-                                  nvalid, lane, sub, rg, my_head, my_i0);
+        tile_step_i8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
+                                  m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
     }
     consumed = i + 1;
     __syncwarp();  // every lane is done with this stage and with ps / alpha_s
@@ -309,33 +347,48 @@ __global__ void __launch_bounds__(NW * 32, (NW <= 4 && G <= 4) ? 3 : 1)
 
   // Per-warp totals: l over the lanes of each head, acc over row groups.
 #pragma unroll
-  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+  for (int m = 1; m < SHL; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
 #pragma unroll
-  for (int m = L; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
-#pragma unroll
-  for (int m = L; m < 32; m <<= 1)
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        acc[g][k].x += __shfl_xor_sync(kFullMask, acc[g][k].x, m);
-        acc[g][k].y += __shfl_xor_sync(kFullMask, acc[g][k].y, m);
-      }
-
+  for (int m = SL; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
   // Merge warps through shared memory (each warp writes into its own, now
   // idle, tile ring): [G][D] acc, then m[G], l[G].
   float* mrg = reinterpret_cast<float*>(wbase);
-  if (rg == 0) {
+  if constexpr (!I8) {
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float4* dst = reinterpret_cast<float4*>(mrg + g * D + sub * 8);
-      dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-      dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+    for (int m = L; m < 32; m <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[g][k].x += __shfl_xor_sync(kFullMask, acc[g][k].x, m);
+          acc[g][k].y += __shfl_xor_sync(kFullMask, acc[g][k].y, m);
+        }
+    if (rg == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float4* dst = reinterpret_cast<float4*>(mrg + g * D + sub * 8);
+        dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+        dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+      }
     }
-    if (sub % Geo::HEAD_LANES == 0) {
-      mrg[G * D + my_head] = m_run;
-      mrg[G * D + G + my_head] = l_run;
+  } else {
+    // the MMAs already summed over tokens: lane (gid, tig) holds heads 2 tig,
+    // 2 tig + 1 at dims [(D/8) gid, +D/8) (see pv_i8_mma)
+    const int gid = lane >> 2, h0 = 2 * (lane & 3);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      if (h0 + hh < G) {
+        float4* dst = reinterpret_cast<float4*>(mrg + (h0 + hh) * D + (D / 8) * gid);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          dst[k] = make_float4(acc8[2 * k][hh], acc8[2 * k][2 + hh], acc8[2 * k + 1][hh],
+                               acc8[2 * k + 1][2 + hh]);
+      }
     }
+  }
+  if (srg == 0 && ssub % SHL == 0) {
+    mrg[G * D + my_head] = m_run;
+    mrg[G * D + G + my_head] = l_run;
   }
   __syncthreads();
 

@@ -154,53 +154,184 @@ namespace pa {
 // ---------------------------------------------------------------------------
 // INT8 KV cache (one fp32 scale per token and KV head; see pa.h).  A tile is
 // K codes [16][D] int8, V codes [16][D] int8, then the 16 K and 16 V scales.
-// QK is an integer dot product (q quantised per head to int8 in the CTA
-// prologue), exact in int32 through the cross-lane reduction; the K and q
-// scales are applied once per score.  PV stays in fp32: V codes become floats
-// and the V scale is folded into each softmax weight.
+//
+// QK is an exact integer dot product of the codes (q is quantised per head
+// by the CTA before the loop) and has its own lane geometry: QL lanes share a
+// K row, each holding QB = D/QL code bytes of every head of the group in
+// registers, so a pass covers 32/QL rows and the butterfly that completes the
+// partial dots has only log2(QL) levels (QL = 4: 2 levels; the bf16 step
+// needs 4).  The K and q scales are applied once per score.  PV runs on the
+// tensor cores (pv_i8_mma) with the V scale folded into each softmax weight.
+template <int D, int G>
+struct I8Geometry {
+  static constexpr int BS = kBlockSize;
+  static constexpr int QL = G >= 8 ? 8 : 4;  // lanes per K row
+  static constexpr int QB = D / QL;          // code bytes per lane and row
+  static constexpr int QW = QB / 4;          // 32-bit words of codes per lane and head
+  static constexpr int ROWS = 32 / QL;       // rows per pass
+  static constexpr int P = BS / ROWS;        // passes over a tile
+  static constexpr int NV = P * G;           // partial dots per lane
+  static constexpr int R = NV / QL;          // complete scores per lane after the butterfly
+  static constexpr int HEAD_LANES = P / R;   // lanes holding one head's scores of a row group
+  static_assert(QB == 8 || QB == 16 || QB == 32, "code bytes per lane");
+  static_assert(NV % QL == 0 && R >= 1 && P % R == 0, "int8 score geometry");
+};
 
-// 8 int8 codes (two words) to floats: byte b becomes the float 2^23 + b + 128
-// (bits 0x4B0000xx), from which 2^23 + 128 is subtracted exactly.
-__device__ __forceinline__ void int8x8_to_float(const uint2 w, float2 (&f)[4]) {
-  const uint32_t a = w.x ^ 0x80808080u, b = w.y ^ 0x80808080u;
-  const float2 off = make_float2(-8388736.0f, -8388736.0f);
-  f[0] = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540)),
-                     __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7541)));
-  f[1] = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7542)),
-                     __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7543)));
-  f[2] = make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7540)),
-                     __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7541)));
-  f[3] = make_float2(__uint_as_float(__byte_perm(b, 0x4B000000u, 0x7542)),
-                     __uint_as_float(__byte_perm(b, 0x4B000000u, 0x7543)));
-#pragma unroll
-  for (int k = 0; k < 4; ++k) f[k] = __fadd2_rn(f[k], off);
+// The 16-byte chunks lane (qrg, qsub) reads from each K row, in order.  With
+// 32 bytes per lane, odd row groups take their two chunks in the opposite
+// order so that the 8 lanes of a shared-memory phase hit 8 different chunks.
+template <int QB>
+__device__ __forceinline__ int i8_chunk(int qsub, int qrg, int k) {
+  if constexpr (QB == 32) return 2 * qsub + (k ^ (qrg & 1));
+  else return qsub;  // QB <= 16: one chunk (or half of one)
 }
 
+// Loads this lane's QB code bytes of one row (a K row, or q of one head) in
+// i8_chunk order, as QW words.
+template <int QB>
+__device__ __forceinline__ void i8_load_row(const unsigned char* row, int qsub, int qrg,
+                                            int (&w)[QB / 4]) {
+  if constexpr (QB == 32) {
+    const int4 a = *reinterpret_cast<const int4*>(row + 16 * i8_chunk<32>(qsub, qrg, 0));
+    const int4 c = *reinterpret_cast<const int4*>(row + 16 * i8_chunk<32>(qsub, qrg, 1));
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = c.x; w[5] = c.y; w[6] = c.z; w[7] = c.w;
+  } else if constexpr (QB == 16) {
+    const int4 a = *reinterpret_cast<const int4*>(row + 16 * qsub);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+  } else {
+    const int2 a = *reinterpret_cast<const int2*>(row + 8 * qsub);
+    w[0] = a.x; w[1] = a.y;
+  }
+}
+
+// One m16n8k8 tf32 tensor-core step, fp32 accumulate: c += a · b.
+__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+// 4 int8 codes (one word) to exact floats, bit patterns for the tf32 MMA.
+__device__ __forceinline__ void int8x4_to_tf32(uint32_t w, uint32_t (&f)[4]) {
+  const uint32_t a = w ^ 0x80808080u;
+  const float2 off = make_float2(-8388736.0f, -8388736.0f);
+  float2 lo = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540)),
+                          __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7541)));
+  float2 hi = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7542)),
+                          __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7543)));
+  lo = __fadd2_rn(lo, off);
+  hi = __fadd2_rn(hi, off);
+  f[0] = __float_as_uint(lo.x);
+  f[1] = __float_as_uint(lo.y);
+  f[2] = __float_as_uint(hi.x);
+  f[3] = __float_as_uint(hi.y);
+}
+
+// PV of one INT8 tile on the tensor cores: out^T[dim][head] += V^T[dim][token]
+// · W[token][head] with m16n8k8 tf32 MMAs (M = 16 dims, N = 8 heads, the
+// group padded with zeros, K = 8 tokens), two K steps per tile.  V codes are
+// small integers, exact in tf32; each weight W (softmax weight times the
+// token's V scale) is split into two tf32 parts, hi + lo, one MMA each, so
+// the products keep ~21 bits.  Lane (gid = lane / 4, tig = lane % 4) owns, in
+// MMA c, dims d0 = (D/8)·gid + 2c (row gid) and d0 + 1 (row gid + 8), and
+// heads 2·tig, 2·tig + 1: acc[c] = {(d0, 2tig), (d0, 2tig+1), (d0+1, 2tig),
+// (d0+1, 2tig+1)}.  It reads the D/8 code bytes at dims [(D/8)·gid, +D/8) of
+// tokens tig, tig + 4, tig + 8, tig + 12; the V tile's 16-byte units are
+// permuted within each 128-byte line (unit u of line L at u ^ (2L & 7)), which
+// puts the 8 lanes of every shared-memory phase on 8 different units.
+template <int D>
+__device__ __forceinline__ const unsigned char* v_i8_row_run(const unsigned char* vt, int t,
+                                                              int gid) {
+  constexpr int RUN = D / 8;                 // bytes per lane and token: 16 or 8
+  const int unit = (t * D + RUN * gid) >> 4;  // logical 16-byte unit in the tile
+  const int line = unit >> 3;
+  return vt + ((line << 3) + ((unit & 7) ^ ((2 * line) & 7))) * 16 + ((RUN * gid) & 15);
+}
+
+template <int D, int G>
+__device__ __forceinline__ void pv_i8_mma(const unsigned char* __restrict__ vt,
+                                          const float* __restrict__ ps, float (&acc)[D / 16][4],
+                                          int lane) {
+  constexpr int NWORD = D / 32;  // code words per lane and token
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t whi[4], wlo[4];  // W[token tig + 4j][head gid] = hi + lo
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float w = gid < G ? ps[(tig + 4 * j) * G + gid] : 0.f;
+    whi[j] = to_tf32(w);
+    wlo[j] = to_tf32(w - __uint_as_float(whi[j]));
+  }
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    const unsigned char* r0 = v_i8_row_run<D>(vt, 8 * ks + tig, gid);
+    const unsigned char* r1 = v_i8_row_run<D>(vt, 8 * ks + tig + 4, gid);
+    uint32_t w0[NWORD], w1[NWORD];
+    if constexpr (NWORD == 4) {
+      const uint4 x = *reinterpret_cast<const uint4*>(r0);
+      const uint4 y = *reinterpret_cast<const uint4*>(r1);
+      w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
+      w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(r0);
+      const uint2 y = *reinterpret_cast<const uint2*>(r1);
+      w0[0] = x.x; w0[1] = x.y;
+      w1[0] = y.x; w1[1] = y.y;
+    }
+#pragma unroll
+    for (int j = 0; j < NWORD; ++j) {
+      uint32_t f0[4], f1[4];
+      int8x4_to_tf32(w0[j], f0);
+      int8x4_to_tf32(w1[j], f1);
+      // word j holds dims 4j .. 4j+3 of the lane's run: MMAs 2j and 2j + 1
+      mma_tf32(acc[2 * j], f0[0], f0[1], f1[0], f1[1], whi[2 * ks], whi[2 * ks + 1]);
+      mma_tf32(acc[2 * j + 1], f0[2], f0[3], f1[2], f1[3], whi[2 * ks], whi[2 * ks + 1]);
+      mma_tf32(acc[2 * j], f0[0], f0[1], f1[0], f1[1], wlo[2 * ks], wlo[2 * ks + 1]);
+      mma_tf32(acc[2 * j + 1], f0[2], f0[3], f1[2], f1[3], wlo[2 * ks], wlo[2 * ks + 1]);
+    }
+  }
+}
+
+// One INT8 tile.  (qsub, qrg): this lane in the QK geometry; my_head / my_i0:
+// the head and first pass of this lane's scores.
 template <int D, int G, bool FULL>
-__device__ __forceinline__ void tile_step_i8(const uint2* __restrict__ kt,
-                                             const uint2* __restrict__ vt,
+__device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ kt,
+                                             const unsigned char* __restrict__ vt,
                                              const float* __restrict__ ksc,
                                              const float* __restrict__ vsc, float* ps,
-                                             float* alpha_s, const int (&qc)[G][2],
-                                             const float (&qsc)[G], float2 (&acc)[G][4],
+                                             float* alpha_s,
+                                             const int (&qc)[G][I8Geometry<D, G>::QW],
+                                             const float (&qsc)[G], float (&acc)[D / 16][4],
                                              float& m_run, float& l_run, int nvalid, int lane,
-                                             int sub, int rg, int my_head, int my_i0) {
-  using Geo = Geometry<D, G>;
-  constexpr int L = Geo::L, ROWS = Geo::ROWS, P = Geo::P, NV = Geo::NV, R = Geo::R;
+                                             int qsub, int qrg, int my_head, int my_i0) {
+  using IG = I8Geometry<D, G>;
+  constexpr int QL = IG::QL, QR = IG::ROWS, QP = IG::P, NV = IG::NV, R = IG::R;
 
-  // QK: integer partial dots over this lane's 8 dims, value index g * P + i.
+  // QK: integer partial dots over this lane's QB bytes, value index g * QP + i.
   int sc[NV];
 #pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const uint2 w = kt[(i * ROWS + rg) * L + sub];
+  for (int i = 0; i < QP; ++i) {
+    int w[IG::QW];
+    i8_load_row<IG::QB>(kt + (i * QR + qrg) * D, qsub, qrg, w);
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      sc[g * P + i] = __dp4a(qc[g][1], static_cast<int>(w.y),
-                             __dp4a(qc[g][0], static_cast<int>(w.x), 0));
+    for (int g = 0; g < G; ++g) {
+      int a = 0;
+#pragma unroll
+      for (int k = 0; k < IG::QW; ++k) a = __dp4a(qc[g][k], w[k], a);
+      sc[g * QP + i] = a;
+    }
   }
-  // the transposing butterfly of tile_step, on exact int32 sums
+  // the transposing butterfly of tile_step, over QL lanes, on exact int32 sums
 #pragma unroll
-  for (int m = L / 2, n = NV; m >= 1; m >>= 1, n >>= 1) {
+  for (int m = QL / 2, n = NV; m >= 1; m >>= 1, n >>= 1) {
     const bool up = (lane & m) != 0;
 #pragma unroll
     for (int k = 0; k < n / 2; ++k) {
@@ -218,74 +349,45 @@ __device__ __forceinline__ void tile_step_i8(const uint2* __restrict__ kt,
     if (my_head == g) my_qsc = qsc[g];
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int t = (my_i0 + r) * ROWS + rg;
+    const int t = (my_i0 + r) * QR + qrg;
     s[r] = (FULL || t < nvalid) ? static_cast<float>(sc[r]) * my_qsc * ksc[t] : -INFINITY;
     mx = fmaxf(mx, s[r]);
   }
 #pragma unroll
-  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+  for (int m = 1; m < IG::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
 #pragma unroll
-  for (int m = L; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+  for (int m = QL; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
   const float m_new = fmaxf(m_run, mx);
   const float alpha = exp2f(m_run - m_new);
   float psum = 0.f;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
-    const int t = (my_i0 + r) * ROWS + rg;
+    const int t = (my_i0 + r) * QR + qrg;
     const float pr = exp2f(s[r] - m_new);
     psum += pr;
-    ps[t * G + my_head] = pr * ((FULL || t < nvalid) ? vsc[t] : 0.f);  // V scale folded in
+    // V scale folded in; a token past the context gets weight 0 (its codes
+    // are finite whatever the pool holds, its scale may not be)
+    ps[t * G + my_head] = pr * ((FULL || t < nvalid) ? vsc[t] : 0.f);
   }
   l_run = l_run * alpha + psum;
   m_run = m_new;
-  if (sub % Geo::HEAD_LANES == 0 && rg == 0) alpha_s[my_head] = alpha;
+  if (qsub % IG::HEAD_LANES == 0 && qrg == 0) alpha_s[my_head] = alpha;
   const bool rescale = __any_sync(kFullMask, alpha != 1.0f);
   __syncwarp();
 
   if (rescale) {
+    const int h0 = 2 * (lane & 3);
+    const float a0 = h0 < G ? alpha_s[h0] : 1.f;
+    const float a1 = h0 + 1 < G ? alpha_s[h0 + 1] : 1.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float a = alpha_s[g];
-      const float2 a2 = make_float2(a, a);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) acc[g][k] = __fmul2_rn(acc[g][k], a2);
+    for (int c = 0; c < D / 16; ++c) {
+      acc[c][0] *= a0;
+      acc[c][1] *= a1;
+      acc[c][2] *= a0;
+      acc[c][3] *= a1;
     }
   }
-
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const int t = i * ROWS + rg;
-    if (FULL || t < nvalid) {
-      float2 v[4];
-      int8x8_to_float(vt[t * L + sub], v);
-      float pw[G];
-      if constexpr (G % 4 == 0) {
-#pragma unroll
-        for (int g = 0; g < G; g += 4) {
-          const float4 x = *reinterpret_cast<const float4*>(ps + t * G + g);
-          pw[g] = x.x;
-          pw[g + 1] = x.y;
-          pw[g + 2] = x.z;
-          pw[g + 3] = x.w;
-        }
-      } else {
-#pragma unroll
-        for (int g = 0; g < G; g += 2) {
-          const float2 x = *reinterpret_cast<const float2*>(ps + t * G + g);
-          pw[g] = x.x;
-          pw[g + 1] = x.y;
-        }
-      }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float2 pp = make_float2(pw[g], pw[g]);
-        acc[g][0] = __ffma2_rn(pp, v[0], acc[g][0]);
-        acc[g][1] = __ffma2_rn(pp, v[1], acc[g][1]);
-        acc[g][2] = __ffma2_rn(pp, v[2], acc[g][2]);
-        acc[g][3] = __ffma2_rn(pp, v[3], acc[g][3]);
-      }
-    }
-  }
+  pv_i8_mma<D, G>(vt, ps, acc, lane);
 }
 
 }  // namespace pa

@@ -57,6 +57,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, but a thread whose phase is not complete yet may sleep up
+// to `hint_ns` nanoseconds inside the instruction (woken early when the phase
+// completes) instead of returning at once, so waiting warps do not spin
+// through issue slots that computing warps could use.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, unsigned parity,
+                                                    unsigned hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -71,7 +88,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, unsigned parity
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if (global_timer_ns() - t0 > 2000000000ull) {
       raise_error(err, PA_DEVERR_WAIT_TIMEOUT);
       return false;

@@ -102,7 +102,15 @@ __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(const Cache
         packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * i);
       }
     }
-    int8_t* dst = (which ? p.v8 : p.k8) + srow * D + lane * PER;
+    // K rows are plain; V tiles have their 16-byte units permuted within each
+    // 128-byte line (unit u of line L at u ^ ((2L) & 7)), see pa.h
+    int64_t col = lane * PER;
+    if (which) {
+      const int unit = static_cast<int>((off * D + col) >> 4);  // within the tile
+      const int line = unit >> 3;
+      col = ((((unit & 7) ^ ((2 * line) & 7)) + 8 * line) << 4) - off * D + (col & 15);
+    }
+    int8_t* dst = (which ? p.v8 : p.k8) + srow * D + col;
     if constexpr (PER == 4)
       *reinterpret_cast<uint32_t*>(dst) = packed;
     else

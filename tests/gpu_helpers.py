@@ -89,3 +89,17 @@ def assert_close(got, ref, what=""):
         assert nmax <= NORM_RTOL, f"{what}: normwise rel err {nmax:.3e} > {NORM_RTOL}"
     assert np.all(num[~nz] == 0), f"{what}: nonzero output where the reference is zero"
     return amax
+
+
+def swizzle_v_int8(v):
+    """The INT8 V pool's storage order from the logical [NB, Hkv, bs, D] codes
+    (and back: the permutation is its own inverse).  Each (block, head) tile is
+    128-byte lines of eight 16-byte units; unit u of line L is stored at unit
+    u ^ ((2L) & 7), as the library's header states."""
+    v = np.ascontiguousarray(v)
+    nb, hkv, bs, d = v.shape
+    units = v.reshape(nb, hkv, bs * d // 128, 8, 16)
+    line = np.arange(units.shape[2])[:, None]
+    src = np.arange(8)[None, :] ^ ((2 * line) & 7)
+    out = np.take_along_axis(units, src[None, None, :, :, None], axis=3)
+    return out.reshape(v.shape)

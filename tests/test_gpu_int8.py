@@ -10,7 +10,8 @@ from oracle import quant as OQ
 from paged_kv_cache_283_gb300 import inputs as I
 from paged_kv_cache_283_gb300 import pa
 
-from gpu_helpers import assert_close, bf16_to_f64, both_tables, dev_bf16, model_tables
+from gpu_helpers import (assert_close, bf16_to_f64, both_tables, dev_bf16, model_tables,
+                         swizzle_v_int8)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +32,8 @@ def _pools(w, rng):
 
 
 def _dev_pools(kq, vq, ks, vs):
-    return (torch.from_numpy(kq).cuda(), torch.from_numpy(vq).cuda(),
+    """Device pools from logical codes (V goes to its storage order)."""
+    return (torch.from_numpy(kq).cuda(), torch.from_numpy(swizzle_v_int8(vq)).cuda(),
             torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
 
 
@@ -53,8 +55,10 @@ def test_int8_cache_write_bit_exact(d):
     pa.pa_clear_device_error()
     pa.pa_reshape_and_cache_int8(dev_bf16(key), dev_bf16(val), dk, dv, dks, dvs, _i64(slots))
     torch.cuda.synchronize()
-    for got, exp in zip((dk, dv, dks, dvs), want):
-        assert np.array_equal(got.cpu().numpy(), exp)
+    got = (dk.cpu().numpy(), swizzle_v_int8(dv.cpu().numpy()), dks.cpu().numpy(),
+           dvs.cpu().numpy())
+    for g, exp in zip(got, want):
+        assert np.array_equal(g, exp)
     assert pa.pa_get_device_error() == 0
 
 
