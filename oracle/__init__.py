@@ -14,8 +14,9 @@ Sources (by page title and section):
 
 * "How LLM Inference Serving Works: KV Cache, PagedAttention and Continuous
   Batching" (dev.to) -- sections "What the KV Cache Is, and How Big It Gets",
-  "PagedAttention: Virtual Memory for the KV Cache", "Sharing comes for free"
-  and "Putting It Together: The Life of a Request in vLLM".
+  "PagedAttention: Virtual Memory for the KV Cache", "Sharing comes for free",
+  "Two Phases: Prefill and Decode", "Chunked prefill" and "Putting It
+  Together: The Life of a Request in vLLM".
 * "LLM serving (vLLM, quantized inference): Visual walkthrough" -- Steps 1-8
   and the quick self-check.
 
@@ -25,6 +26,10 @@ Modules:
 * ``kv_size``    the KV-cache byte formulas and the paged / naive waste counts.
 * ``attention``  block-table gather + dense softmax attention, per-partition
                  statistics and the log-sum-exp merge.
+* ``prefill``    causal attention of a chunk of new tokens over the paged
+                 cache (chunked prefill; one token = one decode step).
+* ``quant``      the INT8 KV scheme: per-row quantisation, the INT8 cache
+                 write and the INT8 decode.
 * ``cache``      the cache write (scatter of new K/V through a slot mapping).
 * ``allocator``  a pure-Python block allocator model (FIFO free list,
                  refcounts, fork / copy-on-write, free).
