@@ -11,6 +11,7 @@
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
  *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
  *   *_int8                 the cache write and decode over an INT8 KV cache
+ *   pa_prefill             causal attention of chunks of new tokens (prefill)
  *   pa_alloc_*             fixed-size block allocator with reference counts,
  *                          copy-on-write and automatic prefix caching (host
  *                          only, never on the GPU path)
@@ -287,6 +288,36 @@ pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache
                                    int head_dim, int block_size, int num_blocks,
                                    float scale, int partition_size, int max_context_len,
                                    pa_stream_t stream);
+
+/*
+ * Paged (chunked) prefill attention ("How LLM Inference Serving Works",
+ * sections "Two Phases: Prefill and Decode" and "Chunked prefill"; paging as
+ * in [PA]).  Each sequence b contributes a chunk of n_b new tokens, whose
+ * K/V the caller has already written into the cache (pa_reshape_and_cache);
+ * with ctx_b = context_lens[b] (chunk included) the chunk holds positions
+ * ctx_b - n_b .. ctx_b - 1, and the query at position p attends to keys
+ * 0 .. p (causal; n_b = 1 is one decode step).
+ *   q, out            : [T, Hq, head_dim] bf16, the chunks back to back;
+ *                       T = total_query_tokens.
+ *   query_start_loc   : [num_seqs + 1] int32 (device), sequence b's rows are
+ *                       query_start_loc[b] .. query_start_loc[b+1] - 1.
+ *   max_query_len     : host bound on every n_b (sizes the grid; longer
+ *                       chunks are cut at it).
+ *   k_cache, v_cache, block_tables, context_lens: as pa_decode.
+ * Runs on the tensor cores (tcgen05, bf16 in, fp32 accumulate; P is rounded to
+ * bf16 before the PV product).  head_dim 128, block_size 16, Hq / Hkv in
+ * {1, 2, 4, 8} (else PA_ERR_UNSUPPORTED_SHAPE); num_seqs <= 65535.  Device-side
+ * checks: 0 <= n_b <= ctx_b <= max_blocks_per_seq * 16 and rows within T (else
+ * PA_DEVERR_CONTEXT_LEN and the sequence is skipped); bad block ids as
+ * pa_decode.  Pointers 16-byte aligned.  Async on `stream`.
+ */
+int pa_prefill_supported(int head_dim, int group, int block_size);
+pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                     const int32_t* block_tables, int max_blocks_per_seq,
+                     const int32_t* context_lens, const int32_t* query_start_loc,
+                     int max_query_len, int num_seqs, int total_query_tokens,
+                     int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                     int num_blocks, float scale, pa_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* Host block allocator [PA], [SH], [LIFE], [OOM], [WALK].  Not thread-safe;

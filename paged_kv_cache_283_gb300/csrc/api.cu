@@ -22,10 +22,14 @@ thread_local std::string t_last_cuda_error;
 constexpr int kMaxDevices = 64;
 std::atomic<unsigned*> g_error_word_ptr[kMaxDevices];
 
+}  // namespace
+
 pa_status cuda_fail(cudaError_t e) {
   t_last_cuda_error = cudaGetErrorString(e);
   return PA_ERR_CUDA;
 }
+
+namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

@@ -94,4 +94,8 @@ cudaError_t launch_copy_blocks(const CopyBlocksParams& p, int num_pairs, int num
 // Address of the current device's error word (device memory), or nullptr.
 unsigned* device_error_word();
 
+// Records e as the calling thread's last CUDA error (pa_last_cuda_error) and
+// returns PA_ERR_CUDA.
+pa_status cuda_fail(cudaError_t e);
+
 }  // namespace pa

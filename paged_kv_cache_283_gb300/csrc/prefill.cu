@@ -1,0 +1,597 @@
+// Paged (chunked) prefill attention on the 5th-generation tensor cores, sm_103a.
+//
+// What is computed: "How LLM Inference Serving Works" (dev.to), sections "Two
+// Phases: Prefill and Decode" (prefill runs the prompt's tokens together and
+// is compute-bound) and "Chunked prefill" (a long prompt is split into chunks
+// that share steps with decodes).  A chunk of n new tokens of a sequence with
+// context length ctx (chunk included, its K/V already in the cache) holds
+// positions ctx - n .. ctx - 1; the query at position p attends to the cached
+// keys 0 .. p through the block table ("PagedAttention: Virtual Memory for
+// the KV Cache").  n = 1 is a decode step.
+//
+// Design (one CTA of 4 warps per 128 query rows):
+//  * Rows are (token, head) pairs of one GQA group: 128 / G tokens x G heads,
+//    so each K/V tile loaded serves the whole group.  Q arrives by one 3-D TMA
+//    per 64-column half; K and V arrive per 16-token block by 2-D TMA (the
+//    block table is a gather of 16-row boxes), 8 blocks = 128 keys per chunk,
+//    two chunk stages.  TMA writes the 128-byte-swizzled layout the tensor
+//    cores read.
+//  * S = Q K^T (M = 128 rows, N = 128 keys, K = 128 dims) and O += P V
+//    (M = 128, N = 128 dims, K = 128 keys) are tcgen05.mma kind::f16 (bf16 in,
+//    fp32 accumulate) issued by one thread, with S and O in tensor memory
+//    (256 columns).  V is the MN-major operand.  Shared memory: Q 32 KiB,
+//    K and V 2 x 32 KiB each, P 2 x 32 KiB (224 KiB, one CTA per SM).
+//  * The online softmax reads its row of S from tensor memory (thread = row =
+//    TMEM lane), masks causally, keeps a running maximum that is only raised
+//    when it grows by more than 2^8 (then O's row is rescaled in tensor
+//    memory), and writes P into shared memory in the swizzled K-major layout
+//    for the second MMA as two bf16 parts, hi = bf16(p) and lo = bf16(p - hi),
+//    each multiplied with V by its own MMA: the weights keep ~17 bits instead
+//    of bf16's 8 (a single bf16 P puts elementwise errors of several per cent
+//    on outputs that are small by cancellation).
+//  * Every wait is bounded; on a timeout the CTA records PA_DEVERR_WAIT_TIMEOUT,
+//    lets its own copies and MMAs in flight land (bounded), frees tensor
+//    memory and returns.  Block ids and lengths in device memory are checked.
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "device.cuh"
+#include "internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kD = 128;                 // head_dim
+constexpr int kRows = 128;              // query rows per CTA = MMA M
+constexpr int kKeys = 128;              // keys per chunk = MMA N of S = Q K^T
+constexpr int kBS = 16;                 // tokens per cache block
+constexpr int kChunkBlocks = kKeys / kBS;
+constexpr int kHalf = 128 * 128;        // one 64-column half of a 128-row bf16 tile
+constexpr int kBox = kBS * 128;         // one TMA box of K or V: 16 rows x 128 bytes
+constexpr uint32_t kTmemCols = 256;     // S: columns [0, 128), O: [128, 256)
+
+// Shared memory, from a 1024-byte aligned base (the swizzle atom).
+constexpr int kQ = 0;                   // Q: 2 halves
+constexpr int kK = kQ + 2 * kHalf;      // K: 2 stages x 2 halves
+constexpr int kV = kK + 4 * kHalf;      // V: 2 stages x 2 halves
+constexpr int kP = kV + 4 * kHalf;      // P, high bf16 part: 2 halves
+constexpr int kPlo = kP + 2 * kHalf;    // P, low bf16 part: 2 halves
+constexpr int kBar = kPlo + 2 * kHalf;  // mbarriers and the TMEM address slot
+constexpr int kSmemBytes = kBar + 128 + 1024;
+
+struct PrefillParams {
+  __nv_bfloat16* out;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;
+  unsigned* err;
+  int max_blocks_per_seq;
+  int num_q_heads;
+  int num_kv_heads;
+  int num_blocks;
+  int total_q;
+  float scale_log2;
+};
+
+// ---- tcgen05 / TMA wrappers -------------------------------------------------
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// and stride byte offsets (16-byte units), descriptor version 1 (bit 46),
+// swizzle mode 2 (bits 61-63).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>(lbo >> 4) << 16) | (static_cast<uint64_t>(sbo >> 4) << 32) |
+         (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A
+// and B (bits 7-9, 10-12 = 1), A / B major (bit 15 / 16: 0 = K-major, 1 =
+// MN-major), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t idesc_bf16(int m, int n, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
+         (static_cast<uint32_t>(m >> 4) << 24);
+}
+constexpr uint32_t kIdescQK = idesc_bf16(kRows, kKeys, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(kRows, kD, 0, 1);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+// Generic-proxy shared-memory writes become visible to the async proxy (MMA).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]),
+        "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]),
+        "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+      "%29, %30, %31, %32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+      "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+      "r"(v[29]), "r"(v[30]), "r"(v[31]));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                       uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                       uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---- the kernel ------------------------------------------------------------
+
+// grid (query tiles, KV heads, sequences), 128 threads.
+template <int G>
+__global__ void __launch_bounds__(128, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tq,
+                         const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+  constexpr int TQ = kRows / G;  // query tokens per CTA
+  griddep_wait();
+  griddep_launch_dependents();
+  const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  // Lengths live in device memory: check them (CTA-uniform).
+  const int q0 = __ldg(p.query_start + b), q1 = __ldg(p.query_start + b + 1);
+  const int ctx = __ldg(p.context_lens + b);
+  const int n = q1 - q0;
+  if (q0 < 0 || q1 > p.total_q || n < 0 || n > ctx || ctx > p.max_blocks_per_seq * kBS) {
+    if (tid == 0 && tile == 0 && kvh == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
+    return;
+  }
+  const int i0 = tile * TQ;
+  if (i0 >= n) return;
+  const int nk = ctx - n + min(n, i0 + TQ);  // keys the tile's last query sees
+  const int nchunks = (nk + kKeys - 1) / kKeys;
+  const int nblk_all = (nk + kBS - 1) / kBS;
+
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sm + kBar);  // [2], one per stage
+  uint64_t* s_done = kv_full + 2;
+  uint64_t* o_done = kv_full + 3;
+  uint64_t* q_full = kv_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 64);
+
+  if (tid == 0) {
+    for (int i = 0; i < 5; ++i) mbar_init(kv_full + i, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
+
+  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+  // Thread 0's bookkeeping of work in flight (for the drain after a timeout).
+  int tma_issued = 0, tma_waited = 0, s_commits = 0, o_commits = 0, s_waits = 0, o_waits = 0;
+
+  auto load_chunk = [&](int c) {  // thread 0: K and V of chunk c into stage c & 1
+    const int st = c & 1;
+    const int first = c * kChunkBlocks;
+    const int nb = min(kChunkBlocks, nblk_all - first);
+    mbar_arrive_expect_tx(&kv_full[st], static_cast<uint32_t>(nb * 4 * kBox));
+    for (int j = 0; j < nb; ++j) {
+      int id = __ldg(tbl + first + j);
+      if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
+        raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        id = 0;
+      }
+      const int row = (id * p.num_kv_heads + kvh) * kBS;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        tma_2d(sm + kK + (2 * st + h) * kHalf + j * kBox, &tk, 64 * h, row, &kv_full[st]);
+        tma_2d(sm + kV + (2 * st + h) * kHalf + j * kBox, &tv, 64 * h, row, &kv_full[st]);
+      }
+    }
+    ++tma_issued;
+  };
+
+  if (tid == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+    mbar_arrive_expect_tx(q_full, 2 * kHalf);
+    tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
+    tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
+    load_chunk(0);
+    if (nchunks > 1) load_chunk(1);
+  }
+
+  // This thread's row: token it of the tile, head g of the group.
+  const int r = tid;
+  const int qi = i0 + r / G;
+  const bool row_ok = qi < n;
+  const int pos = ctx - n + qi;
+  float m_used = -INFINITY;  // reference maximum of the exponentials (base 2)
+  float l_sum = 0.f;
+  bool ok = true;
+  bool q_ready = false;
+
+  const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV),
+                 sP = smem_u32(sm + kP), sPlo = smem_u32(sm + kPlo);
+
+  for (int c = 0; c < nchunks; ++c) {
+    const int st = c & 1;
+    bool lok = true;
+    if (tid == 0) {
+      if (!q_ready) lok = q_ready = mbar_wait_bounded(q_full, 0, p.err);
+      lok = lok && mbar_wait_bounded(&kv_full[st], (c >> 1) & 1, p.err);
+      if (lok) {
+        ++tma_waited;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem, sw128_desc(sQ + off, 16, 1024),
+                    sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
+        }
+        umma_commit(s_done);
+        ++s_commits;
+      }
+    }
+    lok = lok && mbar_wait_bounded(s_done, c & 1, p.err);
+    lok = __all_sync(kFullMask, lok);
+    uint32_t sv[kKeys];
+    if (lok) {
+      if (tid == 0) ++s_waits;
+      tc_fence_after();
+#pragma unroll
+      for (int q4 = 0; q4 < kKeys / 32; ++q4) {
+        uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
+        tmem_ld32(tS + 32 * q4, chunk);
+      }
+      tmem_wait_ld();
+    }
+    // MMA2 of the previous chunk has finished with P, O and its V stage.
+    if (c > 0) {
+      lok = lok && mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+      lok = __all_sync(kFullMask, lok);
+      if (lok && tid == 0) ++o_waits;
+    }
+    if (lok && tid == 0 && c + 1 < nchunks && c + 1 >= 2) load_chunk(c + 1);
+
+    if (lok) {
+      tc_fence_after();
+      // Causal mask and the chunk's maximum (base-2 units).
+      const int lim = row_ok ? pos - c * kKeys : -1;  // visible columns: j <= lim
+      float mx = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kKeys; ++j) {
+        const float v = j <= lim ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
+        sv[j] = __float_as_uint(v);
+        mx = fmaxf(mx, v);
+      }
+      float alpha = 1.f;
+      if (mx != -INFINITY) {
+        if (m_used == -INFINITY) {
+          m_used = mx;
+        } else if (mx > m_used + 8.f) {
+          alpha = exp2f(m_used - mx);
+          m_used = mx;
+        }
+      }
+      // Rescale this row of O when its reference maximum moved (c == 0: the
+      // first PV MMA overwrites O).
+      if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+#pragma unroll
+        for (int q4 = 0; q4 < kD / 32; ++q4) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * q4, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+          tmem_st32(tO + 32 * q4, o);
+        }
+        tmem_wait_st();
+      }
+      // P = 2^(s - m_used) as hi + lo bf16 parts into the swizzled K-major
+      // tiles.
+      float psum = 0.f;
+      const bool live = m_used != -INFINITY;
+      const int prow = (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+      for (int cc = 0; cc < kKeys / 8; ++cc) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float a = live ? exp2f(__uint_as_float(sv[8 * cc + 2 * k]) - m_used) : 0.f;
+          const float e = live ? exp2f(__uint_as_float(sv[8 * cc + 2 * k + 1]) - m_used) : 0.f;
+          psum += a + e;
+          const __nv_bfloat162 hi = __floats2bfloat162_rn(a, e);
+          const __nv_bfloat162 lo =
+              __floats2bfloat162_rn(a - __low2float(hi), e - __high2float(hi));
+          wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
+          wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
+        }
+        const int off = prow + (cc >> 3) * kHalf + (((cc & 7) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(sm + kPlo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+      l_sum = l_sum * alpha + psum;
+    }
+    // Keys past the last visible one in the final chunk: their V rows may hold
+    // anything (a partly filled block, or blocks not loaded); P is 0 there,
+    // but 0 * NaN is not, so those rows are zeroed once the copies have landed.
+    const int vk = nk - c * kKeys;  // valid keys in this chunk
+    if (lok && vk < kKeys) {
+      lok = mbar_wait_bounded(&kv_full[st], (c >> 1) & 1, p.err);
+      if (lok && r >= vk) {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + h) * kHalf + (r >> 3) * 1024 +
+                                                (r & 7) * 128);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) row[k] = z;
+        }
+      }
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    if (!__syncthreads_and(lok)) {
+      ok = false;
+      break;
+    }
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kKeys / 16; ++kk) {
+        const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
+        const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
+        umma_bf16(tmem + 128, sw128_desc(sP + aoff, 16, 1024), vdesc, kIdescPV,
+                  (c > 0 || kk > 0) ? 1u : 0u);
+        umma_bf16(tmem + 128, sw128_desc(sPlo + aoff, 16, 1024), vdesc, kIdescPV, 1u);
+      }
+      umma_commit(o_done);
+      ++o_commits;
+    }
+  }
+
+  if (ok) {
+    bool lok = mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
+    lok = __all_sync(kFullMask, lok);
+    if (lok) {
+      if (tid == 0) ++o_waits;
+      tc_fence_after();
+      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+      __nv_bfloat16* orow =
+          p.out + (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads + kvh * G + r % G) * kD;
+#pragma unroll
+      for (int q4 = 0; q4 < kD / 32; ++q4) {
+        uint32_t o[32];
+        tmem_ld32(tO + 32 * q4, o);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 h2 =
+                  __floats2bfloat162_rn(__uint_as_float(o[8 * k + 2 * e]) * inv,
+                                        __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            *reinterpret_cast<uint4*>(orow + 32 * q4 + 8 * k) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
+      }
+    } else {
+      ok = false;
+    }
+  }
+  if (!ok && tid == 0) {
+    // Let this CTA's own copies and MMAs in flight land before its shared and
+    // tensor memory are given up (each wait bounded).
+    for (int c = tma_waited; c < tma_issued; ++c)
+      mbar_wait_bounded(&kv_full[c & 1], (c >> 1) & 1, p.err);
+    if (s_commits > s_waits) mbar_wait_bounded(s_done, (s_commits - 1) & 1, p.err);
+    if (o_commits > o_waits) mbar_wait_bounded(o_done, (o_commits - 1) & 1, p.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- host side -------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// K or V pool as a 2-D bf16 tensor [num_blocks * Hkv * 16 rows][128], boxes of
+// 16 rows x 64 columns, 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* base, int64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {64, kBS};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// q as a 3-D bf16 tensor [T][Hq][128], boxes of (128 / G tokens) x G heads x
+// 64 columns, 128-byte swizzle: one box is one 64-column half of a CTA's rows.
+bool encode_q_map(CUtensorMap* map, const void* base, int total_q, int num_q_heads, int group) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(num_q_heads),
+                              static_cast<cuuint64_t>(total_q)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(num_q_heads) * kD * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(kRows / group)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int G>
+cudaError_t launch_prefill_g(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const PrefillParams& p, int max_query_len, int num_seqs,
+                             cudaStream_t stream) {
+  static std::atomic<uint64_t> smem_set{0};
+  auto kernel = paged_prefill_kernel<G>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(smem_set.load() & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    smem_set.fetch_or(bit);
+  }
+  const int tiles = (max_query_len + kRows / G - 1) / (kRows / G);
+  const dim3 grid(tiles, p.num_kv_heads, num_seqs);
+  return launch_pdl(kernel, grid, dim3(128), kSmemBytes, stream, tq, tk, tv, p);
+}
+
+bool aligned16(const void* ptr) { return ptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_prefill_supported(int head_dim, int group, int block_size) {
+  return head_dim == 128 && block_size == 16 && (group == 1 || group == 2 || group == 4 ||
+                                                  group == 8);
+}
+
+extern "C" pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, const int32_t* query_start_loc,
+                                int max_query_len, int num_seqs, int total_query_tokens,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, float scale, pa_stream_t stream) {
+  using namespace pa;
+  if (num_seqs < 0 || max_query_len < 0 || total_query_tokens < 0 || num_q_heads <= 0 ||
+      num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || max_blocks_per_seq <= 0 ||
+      num_blocks <= 0 || !(scale > 0.f) || num_seqs > 65535)
+    return PA_ERR_INVALID_ARG;
+  const int group = num_q_heads / num_kv_heads;
+  if (!pa_prefill_supported(head_dim, group, block_size)) return PA_ERR_UNSUPPORTED_SHAPE;
+  if (num_seqs == 0 || max_query_len == 0 || total_query_tokens == 0) return PA_OK;
+  if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !block_tables || !context_lens || !query_start_loc)
+    return PA_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * kBS;
+  if (rows > 0x7fffffffll || static_cast<int64_t>(max_blocks_per_seq) * kBS > 0x7fffffffll)
+    return PA_ERR_INVALID_ARG;
+  CUtensorMap tq, tk, tv;
+  if (!encode_q_map(&tq, q, total_query_tokens, num_q_heads, group) ||
+      !encode_pool_map(&tk, k_cache, rows) || !encode_pool_map(&tv, v_cache, rows))
+    return cuda_fail(cudaErrorInvalidValue);  // tensor-map encoding refused the pools
+  PrefillParams p{};
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start_loc;
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.total_q = total_query_tokens;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (group) {
+    case 1: e = launch_prefill_g<1>(tq, tk, tv, p, max_query_len, num_seqs, s); break;
+    case 2: e = launch_prefill_g<2>(tq, tk, tv, p, max_query_len, num_seqs, s); break;
+    case 4: e = launch_prefill_g<4>(tq, tk, tv, p, max_query_len, num_seqs, s); break;
+    default: e = launch_prefill_g<8>(tq, tk, tv, p, max_query_len, num_seqs, s); break;
+  }
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}

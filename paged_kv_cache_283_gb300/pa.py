@@ -51,6 +51,9 @@ SIGNATURES = {
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
     "pa_decode_splitk_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _i, _vp]),
+    "pa_prefill_supported": (_i, [_i, _i, _i]),
+    "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
+                        _f, _vp]),
     "pa_alloc_create": (_i, [_i, _i, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i, [_vp, _i]),
@@ -340,6 +343,34 @@ def pa_decode_splitk_noalloc(out, q, k_cache, v_cache, block_tables, context_len
                                         int(partition_size), int(max_context_len),
                                         _stream(stream))
     _check(st, "pa_decode_splitk_noalloc")
+
+
+def pa_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start_loc,
+               max_query_len, scale, stream=None):
+    """Causal attention of chunks of new tokens over the paged cache (pa.h).
+
+    q, out [T, Hq, D] bf16; query_start_loc [B + 1] int32 (device);
+    max_query_len: host bound on every chunk length.
+    """
+    torch = _torch()
+    T, hq, d = q.shape
+    if out.shape != q.shape:
+        raise ValueError("pa_prefill: out must match q")
+    nb, hkv, bs, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("pa_prefill: cache shapes")
+    B, mb = block_tables.shape
+    if context_lens.shape != (B,) or query_start_loc.shape != (B + 1,):
+        raise ValueError("pa_prefill: context_lens / query_start_loc shapes")
+    st = lib().pa_prefill(_dev(out, torch.bfloat16, "out", 3), _dev(q, torch.bfloat16, "q", 3),
+                          _dev(k_cache, torch.bfloat16, "k_cache", 4),
+                          _dev(v_cache, torch.bfloat16, "v_cache", 4),
+                          _dev(block_tables, torch.int32, "block_tables", 2), mb,
+                          _dev(context_lens, torch.int32, "context_lens", 1),
+                          _dev(query_start_loc, torch.int32, "query_start_loc", 1),
+                          int(max_query_len), B, T, hq, hkv, d, bs, nb, float(scale),
+                          _stream(stream))
+    _check(st, "pa_prefill")
 
 
 class DecodeStep:
