@@ -758,6 +758,189 @@ def run_copy_blocks(args):
     return 0
 
 
+def prefill_flops(context_lens, query_lens, num_q_heads, head_dim):
+    """Algorithmic FLOPs of causal chunked-prefill attention: the query at
+    position p takes 2·(p+1)·D for QK and as many for PV, per query head."""
+    import numpy as np
+    total = 0
+    for ctx, n in zip(np.asarray(context_lens).tolist(), np.asarray(query_lens).tolist()):
+        first = ctx - n + 1                       # keys seen by the chunk's first query
+        total += (first + ctx) * n // 2            # sum of (p + 1) over the chunk
+    return 4 * total * num_q_heads * head_dim
+
+
+def oracle_prefill_sample(max_seconds, out_json=True):
+    """Times the float64 prefill oracle on a bounded sample of the chunked-
+    prefill step: the last m query rows of its first sequence, m doubled until
+    one sample takes >= 0.2 s; repeated until ``max_seconds``.  FLOP/s."""
+    import numpy as np
+
+    from oracle import prefill as OP
+    from paged_kv_cache_283_gb300 import inputs as I
+
+    w = I.chunked_prefill()
+    order = w.free_order
+    ctx0, n0 = int(w.context_lens[0]), int(w.query_lens[0])
+    table0 = order[:-(-ctx0 // w.block_size)]
+    q0 = w.q[:n0]
+
+    def run(m):
+        OP.prefill_sequence(q0[n0 - m:], w.k_cache, w.v_cache, table0, ctx0, w.scale,
+                            w.block_size)
+
+    m = 1
+    while True:
+        t = time.perf_counter()
+        run(m)
+        dt = time.perf_counter() - t
+        if dt >= 0.2 or m >= n0:
+            break
+        m = min(n0, 2 * m)
+    reps, total = 0, 0.0
+    while total < max_seconds or reps == 0:
+        t = time.perf_counter()
+        run(m)
+        total += time.perf_counter() - t
+        reps += 1
+    flops = prefill_flops([ctx0], [m], w.num_q_heads, w.head_dim)
+    res = {"value": flops * reps / total / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+           "sample": f"last {m} of the {n0} query rows of the first chunk (float64 causal "
+                     f"attention over {ctx0} cached tokens), {reps} repetitions, {total:.1f} s"}
+    if out_json:
+        print(json.dumps(res))
+    return res
+
+
+def run_prefill(args):
+    """Chunked-prefill attention (pa_prefill) on the 16 x 512-token step."""
+    import numpy as np
+    import torch
+
+    from paged_kv_cache_283_gb300 import build as _b
+    from paged_kv_cache_283_gb300 import inputs as I
+    from paged_kv_cache_283_gb300 import pa
+
+    base = None
+    if not args.no_cpu_baseline:
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+                   MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+        r = subprocess.run([sys.executable, "-c", "import bench; bench.oracle_prefill_sample(%f)"
+                            % args.cpu_seconds], cwd=ROOT, env=env, capture_output=True,
+                           text=True, timeout=600)
+        base = (json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else
+                {"value": None, "kind": "oracle", "sample": "failed: " + r.stderr[-200:]})
+    _b.build()
+    pa.lib()
+    pa.pa_clear_device_error()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    w = I.chunked_prefill(with_data=False)
+    B = len(w.context_lens)
+    alloc = pa.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    for b, n in enumerate(w.context_lens.tolist()):
+        alloc.add_seq(b)
+        alloc.reserve(b, n)
+    mb = int(-(-w.context_lens.max() // w.block_size))
+    bt, ctx = alloc.block_tables(list(range(B)), mb)
+    assert np.array_equal(ctx, w.context_lens)
+    qsl = np.concatenate([[0], np.cumsum(w.query_lens)]).astype(np.int32)
+    T = int(qsl[-1])
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    pool_bytes = 2 * int(np.prod(shape)) * 2
+    nrep = max(2, -(-4 * l2 // pool_bytes))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(283 + 6)
+    pools = [(torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16),
+              torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16))
+             for _ in range(nrep)]
+    d_bt = torch.from_numpy(bt).to(dev)
+    d_ctx = torch.from_numpy(ctx.astype(np.int32)).to(dev)
+    d_qsl = torch.from_numpy(qsl).to(dev)
+    q = torch.randn((T, w.num_q_heads, w.head_dim), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty_like(q)
+    qmax = int(w.query_lens.max())
+    stream = torch.cuda.Stream(dev)
+
+    def call(r, qq=q, oo=out):
+        pa.pa_prefill(oo, qq, pools[r][0], pools[r][1], d_bt, d_ctx, d_qsl, qmax, w.scale)
+
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            call(k % nrep)
+    stream.synchronize()
+    assert pa.pa_get_device_error() == 0, "device error word set during warmup"
+    graphs = [_capture(lambda r=r: call(r), stream) for r in range(nrep)]
+    steps = max(args.steps // 10, 20)
+    sampler = ClockSampler(0)
+    sampler.start()
+    _time_graphs(graphs, 3, stream)
+    t0 = time.time()
+    dt = _time_graphs(graphs, steps, stream) / steps
+    t1 = time.time()
+    sampler.stop()
+    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+
+    # end to end through the public API: q from pinned host memory in, out back
+    hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    hq.copy_(q)
+    ho = torch.empty_like(hq, pin_memory=True)
+    dq2, do2 = torch.empty_like(q), torch.empty_like(q)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(steps // 2, 10)
+    with torch.cuda.stream(stream):
+        for k in range(3 + n_e2e):
+            if k == 3:
+                e0.record(stream)
+            dq2.copy_(hq, non_blocking=True)
+            call(k % nrep, dq2, do2)
+            ho.copy_(do2, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_dt = e0.elapsed_time(e1) / 1e3 / n_e2e
+    assert pa.pa_get_device_error() == 0, "device error word set during the run"
+
+    flops = prefill_flops(w.context_lens, w.query_lens, w.num_q_heads, w.head_dim)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    tflops = flops / dt / 1e12
+    peak = peaks.get("bf16_tflops")
+    res = {
+        "metric": "chunked-prefill attention TFLOP/s", "value": round(tflops, 2),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens_per_step": T, "q_heads": w.num_q_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                   "mean_context": float(np.mean(w.context_lens)),
+                   "attention": "pa_prefill (tcgen05, one CTA per 32 tokens x 4 heads)",
+                   "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
+                         % (nrep, pool_bytes / 1e6, l2 / 1e6)},
+        "flops_per_step": flops,
+        "tokens_per_s": round(T / dt, 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
+                     "peak": peak if peak else 1900.0, "unit": "TFLOP/s",
+                     "frac": round(tflops / (peak if peak else 1900.0), 4),
+                     "traffic": None, "kernel": "pa_prefill",
+                     "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+                     if peak else "fallback 1.9 PFLOP/s",
+                     "us_per_launch": round(dt * 1e6, 2)},
+        "e2e": {"value": round(flops / e2e_dt / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": q.numel() * 2, "d2h_bytes_per_step": q.numel() * 2},
+        "clocks": clocks,
+        "gpu_launches": steps,
+    }
+    if base is not None:
+        res["cpu_baseline"] = base
+    print(json.dumps(res))
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -767,8 +950,9 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
                     help="KV cache element type (int8: one fp32 scale per token and head)")
-    ap.add_argument("--op", default="step", choices=["step", "copy_blocks"],
-                    help="copy_blocks: time pa_copy_blocks on a parallel-sampling step")
+    ap.add_argument("--op", default="step", choices=["step", "copy_blocks", "prefill"],
+                    help="copy_blocks: time pa_copy_blocks on a parallel-sampling step; "
+                         "prefill: time pa_prefill on a 16 x 512-token chunked-prefill step")
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--soak-seconds", type=float, default=0.5)
@@ -783,6 +967,8 @@ def main(argv=None):
         return run_reference(args)
     if args.op == "copy_blocks":
         return run_copy_blocks(args)
+    if args.op == "prefill":
+        return run_prefill(args)
     return run_gpu(args)
 
 

@@ -56,7 +56,7 @@ constexpr int kBS = 16;                 // tokens per cache block
 constexpr int kChunkBlocks = kKeys / kBS;
 constexpr int kHalf = 128 * 128;        // one 64-column half of a 128-row bf16 tile
 constexpr int kBox = kBS * 128;         // one TMA box of K or V: 16 rows x 128 bytes
-constexpr uint32_t kTmemCols = 256;     // S: columns [0, 128), O: [128, 256)
+constexpr uint32_t kTmemCols = 512;     // S0: [0, 128), S1: [128, 256), O: [256, 384)
 
 // Shared memory, from a 1024-byte aligned base (the swizzle atom).
 constexpr int kQ = 0;                   // Q: 2 halves
@@ -179,7 +179,24 @@ __device__ __forceinline__ void tma_3d(void* dst, const CUtensorMap* map, int x,
 
 // ---- the kernel ------------------------------------------------------------
 
+// exp2 on the special-function unit (flushes subnormal results to zero; the
+// arguments here are <= 8 and the results are weights of at most 2^8).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // grid (query tiles, KV heads, sequences), 128 threads.
+//
+// Pipeline of one CTA over its key chunks c (thread 0 issues every copy and
+// MMA; K and V stages are released separately):
+//   top of c:   S[(c+1)&1] = Q K(c+1)^T        (MMA, overlaps softmax of c)
+//   softmax c:  read S[c&1]; K stage c&1 is free -> copy K(c+2);
+//               max / exponentials in registers;
+//               wait PV(c-1): P, O and V stage (c-1)&1 are free -> copy V(c+1);
+//               rescale O if needed, write P
+//   end of c:   O += P V(c)                      (MMA, overlaps softmax of c+1)
 template <int G>
 __global__ void __launch_bounds__(128, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tq,
@@ -208,14 +225,15 @@ __global__ void __launch_bounds__(128, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* kv_full = reinterpret_cast<uint64_t*>(sm + kBar);  // [2], one per stage
-  uint64_t* s_done = kv_full + 2;
-  uint64_t* o_done = kv_full + 3;
-  uint64_t* q_full = kv_full + 4;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + kBar);  // [2] per K stage
+  uint64_t* v_full = k_full + 2;                               // [2] per V stage
+  uint64_t* s_done = k_full + 4;                               // [2] per S buffer
+  uint64_t* o_done = k_full + 6;
+  uint64_t* q_full = k_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 64);
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(kv_full + i, 1);
+    for (int i = 0; i < 8; ++i) mbar_init(k_full + i, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -228,33 +246,53 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = *tmem_slot;  // S0 at +0, S1 at +128, O at +256
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem + lane_base, tO = tmem + lane_base + 128;
+  const uint32_t tO = tmem + lane_base + 256;
 
   const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
-  // Thread 0's bookkeeping of work in flight (for the drain after a timeout).
-  int tma_issued = 0, tma_waited = 0, s_commits = 0, o_commits = 0, s_waits = 0, o_waits = 0;
+  const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV),
+                 sP = smem_u32(sm + kP), sPlo = smem_u32(sm + kPlo);
 
-  auto load_chunk = [&](int c) {  // thread 0: K and V of chunk c into stage c & 1
-    const int st = c & 1;
-    const int first = c * kChunkBlocks;
-    const int nb = min(kChunkBlocks, nblk_all - first);
-    mbar_arrive_expect_tx(&kv_full[st], static_cast<uint32_t>(nb * 4 * kBox));
-    for (int j = 0; j < nb; ++j) {
-      int id = __ldg(tbl + first + j);
-      if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
-        raise_error(p.err, PA_DEVERR_BLOCK_ID);
-        id = 0;
-      }
-      const int row = (id * p.num_kv_heads + kvh) * kBS;
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_2d(sm + kK + (2 * st + h) * kHalf + j * kBox, &tk, 64 * h, row, &kv_full[st]);
-        tma_2d(sm + kV + (2 * st + h) * kHalf + j * kBox, &tv, 64 * h, row, &kv_full[st]);
-      }
+  // Thread 0's bookkeeping (chunks whose copies / MMAs were issued and waited
+  // for), for the drain after a timeout.
+  int k_iss = 0, k_wai = 0, v_iss = 0, v_wai = 0, s_iss = 0, s_wai = 0, o_iss = 0, o_wai = 0;
+  bool t0ok = true;
+
+  auto block_row = [&](int c, int j) -> int {
+    int id = __ldg(tbl + c * kChunkBlocks + j);
+    if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
+      raise_error(p.err, PA_DEVERR_BLOCK_ID);
+      id = 0;
     }
-    ++tma_issued;
+    return (id * p.num_kv_heads + kvh) * kBS;
+  };
+  // thread 0: K (or V) of chunk c into stage c & 1
+  auto load = [&](int c, bool is_v) {
+    const int st = c & 1;
+    const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
+    uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
+    unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kHalf;
+    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
+    for (int j = 0; j < nb; ++j) {
+      const int row = block_row(c, j);
+      tma_2d(dst + j * kBox, is_v ? &tv : &tk, 0, row, bar);
+      tma_2d(dst + kHalf + j * kBox, is_v ? &tv : &tk, 64, row, bar);
+    }
+    if (is_v) ++v_iss; else ++k_iss;
+  };
+  // thread 0: S[c & 1] = Q K(c)^T
+  auto qk = [&](int c) {
+    const int st = c & 1;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+      umma_bf16(tmem + st * 128, sw128_desc(sQ + off, 16, 1024),
+                sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
+    }
+    umma_commit(&s_done[st]);
+    ++s_iss;
   };
 
   if (tid == 0) {
@@ -264,8 +302,17 @@ __global__ void __launch_bounds__(128, 1)
     mbar_arrive_expect_tx(q_full, 2 * kHalf);
     tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
     tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
-    load_chunk(0);
-    if (nchunks > 1) load_chunk(1);
+    load(0, false);
+    load(0, true);
+    if (nchunks > 1) {
+      load(1, false);
+      load(1, true);
+    }
+    t0ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
+    if (t0ok) {
+      ++k_wai;
+      qk(0);
+    }
   }
 
   // This thread's row: token it of the tile, head g of the group.
@@ -273,74 +320,83 @@ __global__ void __launch_bounds__(128, 1)
   const int qi = i0 + r / G;
   const bool row_ok = qi < n;
   const int pos = ctx - n + qi;
+  const float sl2 = p.scale_log2;
   float m_used = -INFINITY;  // reference maximum of the exponentials (base 2)
   float l_sum = 0.f;
   bool ok = true;
-  bool q_ready = false;
-
-  const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV),
-                 sP = smem_u32(sm + kP), sPlo = smem_u32(sm + kPlo);
+  const int prow = (r >> 3) * 1024 + (r & 7) * 128;  // this row in a swizzled 128-row tile
 
   for (int c = 0; c < nchunks; ++c) {
     const int st = c & 1;
-    bool lok = true;
-    if (tid == 0) {
-      if (!q_ready) lok = q_ready = mbar_wait_bounded(q_full, 0, p.err);
-      lok = lok && mbar_wait_bounded(&kv_full[st], (c >> 1) & 1, p.err);
-      if (lok) {
-        ++tma_waited;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem, sw128_desc(sQ + off, 16, 1024),
-                    sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
-        }
-        umma_commit(s_done);
-        ++s_commits;
+    // (1) the next chunk's scores, computed while this chunk's softmax runs
+    if (tid == 0 && t0ok && c + 1 < nchunks) {
+      t0ok = mbar_wait_bounded(&k_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p.err);
+      if (t0ok) {
+        ++k_wai;
+        qk(c + 1);
       }
     }
-    lok = lok && mbar_wait_bounded(s_done, c & 1, p.err);
+    bool lok = tid == 0 ? t0ok : true;
+    // (2) this chunk's scores
+    lok = lok && mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
     uint32_t sv[kKeys];
     if (lok) {
-      if (tid == 0) ++s_waits;
+      if (tid == 0) ++s_wai;
       tc_fence_after();
 #pragma unroll
       for (int q4 = 0; q4 < kKeys / 32; ++q4) {
         uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
-        tmem_ld32(tS + 32 * q4, chunk);
+        tmem_ld32(tmem + lane_base + st * 128 + 32 * q4, chunk);
       }
       tmem_wait_ld();
+      // K stage st is free again
+      if (tid == 0 && c + 2 < nchunks) load(c + 2, false);
     }
-    // MMA2 of the previous chunk has finished with P, O and its V stage.
-    if (c > 0) {
-      lok = lok && mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
-      lok = __all_sync(kFullMask, lok);
-      if (lok && tid == 0) ++o_waits;
-    }
-    if (lok && tid == 0 && c + 1 < nchunks && c + 1 >= 2) load_chunk(c + 1);
-
+    // (3) causal mask, maximum and exponentials, in registers
+    float alpha = 1.f, psum = 0.f;
     if (lok) {
-      tc_fence_after();
-      // Causal mask and the chunk's maximum (base-2 units).
       const int lim = row_ok ? pos - c * kKeys : -1;  // visible columns: j <= lim
       float mx = -INFINITY;
+      if (__all_sync(kFullMask, lim >= kKeys - 1)) {
 #pragma unroll
-      for (int j = 0; j < kKeys; ++j) {
-        const float v = j <= lim ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
-        sv[j] = __float_as_uint(v);
-        mx = fmaxf(mx, v);
+        for (int j = 0; j < kKeys; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+      } else {
+#pragma unroll
+        for (int j = 0; j < kKeys; ++j) {
+          const float v = j <= lim ? __uint_as_float(sv[j]) : -INFINITY;
+          sv[j] = __float_as_uint(v);
+          mx = fmaxf(mx, v);
+        }
       }
-      float alpha = 1.f;
+      mx *= sl2;
       if (mx != -INFINITY) {
         if (m_used == -INFINITY) {
           m_used = mx;
         } else if (mx > m_used + 8.f) {
-          alpha = exp2f(m_used - mx);
+          alpha = ex2(m_used - mx);
           m_used = mx;
         }
       }
+      const bool live = m_used != -INFINITY;
+      const float neg = live ? -m_used : 0.f;
+#pragma unroll
+      for (int j = 0; j < kKeys; ++j) {
+        const float e = live ? ex2(fmaf(__uint_as_float(sv[j]), sl2, neg)) : 0.f;
+        psum += e;
+        sv[j] = __float_as_uint(e);
+      }
+      l_sum = l_sum * alpha + psum;
+    }
+    // (4) the previous PV product is done with P, O and its V stage
+    if (c > 0) {
+      lok = lok && mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+      lok = __all_sync(kFullMask, lok);
+      if (lok && tid == 0) ++o_wai;
+    }
+    if (lok) {
+      if (tid == 0 && c + 1 < nchunks && c + 1 >= 2) load(c + 1, true);
+      tc_fence_after();
       // Rescale this row of O when its reference maximum moved (c == 0: the
       // first PV MMA overwrites O).
       if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
@@ -355,22 +411,17 @@ __global__ void __launch_bounds__(128, 1)
         }
         tmem_wait_st();
       }
-      // P = 2^(s - m_used) as hi + lo bf16 parts into the swizzled K-major
-      // tiles.
-      float psum = 0.f;
-      const bool live = m_used != -INFINITY;
-      const int prow = (r >> 3) * 1024 + (r & 7) * 128;
+      // P as hi + lo bf16 parts into the swizzled K-major tiles
 #pragma unroll
       for (int cc = 0; cc < kKeys / 8; ++cc) {
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const float a = live ? exp2f(__uint_as_float(sv[8 * cc + 2 * k]) - m_used) : 0.f;
-          const float e = live ? exp2f(__uint_as_float(sv[8 * cc + 2 * k + 1]) - m_used) : 0.f;
-          psum += a + e;
+          const float a = __uint_as_float(sv[8 * cc + 2 * k]);
+          const float e = __uint_as_float(sv[8 * cc + 2 * k + 1]);
           const __nv_bfloat162 hi = __floats2bfloat162_rn(a, e);
-          const __nv_bfloat162 lo =
-              __floats2bfloat162_rn(a - __low2float(hi), e - __high2float(hi));
+          const float2 hf = __bfloat1622float2(hi);
+          const __nv_bfloat162 lo = __floats2bfloat162_rn(a - hf.x, e - hf.y);
           wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
           wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
         }
@@ -378,20 +429,18 @@ __global__ void __launch_bounds__(128, 1)
         *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
         *reinterpret_cast<uint4*>(sm + kPlo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
-      l_sum = l_sum * alpha + psum;
     }
-    // Keys past the last visible one in the final chunk: their V rows may hold
-    // anything (a partly filled block, or blocks not loaded); P is 0 there,
-    // but 0 * NaN is not, so those rows are zeroed once the copies have landed.
+    // (5) V of this chunk has landed.  Keys past the last visible one in the
+    // final chunk may hold anything in V (a partly filled block, or blocks not
+    // loaded); P is 0 there, but 0 * NaN is not, so those rows are zeroed.
     const int vk = nk - c * kKeys;  // valid keys in this chunk
-    if (lok && vk < kKeys) {
-      lok = mbar_wait_bounded(&kv_full[st], (c >> 1) & 1, p.err);
+    if (lok && (vk < kKeys || tid == 0)) {
+      lok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err);
       if (lok && r >= vk) {
         const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + h) * kHalf + (r >> 3) * 1024 +
-                                                (r & 7) * 128);
+          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + h) * kHalf + prow);
 #pragma unroll
           for (int k = 0; k < 8; ++k) row[k] = z;
         }
@@ -403,18 +452,20 @@ __global__ void __launch_bounds__(128, 1)
       ok = false;
       break;
     }
+    // (6) O += P V(c), hi and lo parts
     if (tid == 0) {
+      ++v_wai;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kKeys / 16; ++kk) {
         const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
         const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
-        umma_bf16(tmem + 128, sw128_desc(sP + aoff, 16, 1024), vdesc, kIdescPV,
+        umma_bf16(tmem + 256, sw128_desc(sP + aoff, 16, 1024), vdesc, kIdescPV,
                   (c > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(tmem + 128, sw128_desc(sPlo + aoff, 16, 1024), vdesc, kIdescPV, 1u);
+        umma_bf16(tmem + 256, sw128_desc(sPlo + aoff, 16, 1024), vdesc, kIdescPV, 1u);
       }
       umma_commit(o_done);
-      ++o_commits;
+      ++o_iss;
     }
   }
 
@@ -422,11 +473,12 @@ __global__ void __launch_bounds__(128, 1)
     bool lok = mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
     if (lok) {
-      if (tid == 0) ++o_waits;
+      if (tid == 0) ++o_wai;
       tc_fence_after();
       const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
       __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads + kvh * G + r % G) * kD;
+          p.out + (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads + kvh * G + r % G) *
+                      kD;
 #pragma unroll
       for (int q4 = 0; q4 < kD / 32; ++q4) {
         uint32_t o[32];
@@ -454,10 +506,10 @@ __global__ void __launch_bounds__(128, 1)
   if (!ok && tid == 0) {
     // Let this CTA's own copies and MMAs in flight land before its shared and
     // tensor memory are given up (each wait bounded).
-    for (int c = tma_waited; c < tma_issued; ++c)
-      mbar_wait_bounded(&kv_full[c & 1], (c >> 1) & 1, p.err);
-    if (s_commits > s_waits) mbar_wait_bounded(s_done, (s_commits - 1) & 1, p.err);
-    if (o_commits > o_waits) mbar_wait_bounded(o_done, (o_commits - 1) & 1, p.err);
+    for (int c = k_wai; c < k_iss; ++c) mbar_wait_bounded(&k_full[c & 1], (c >> 1) & 1, p.err);
+    for (int c = v_wai; c < v_iss; ++c) mbar_wait_bounded(&v_full[c & 1], (c >> 1) & 1, p.err);
+    for (int c = s_wai; c < s_iss; ++c) mbar_wait_bounded(&s_done[c & 1], (c >> 1) & 1, p.err);
+    if (o_iss > o_wai) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
   }
   tc_fence_before();
   __syncthreads();

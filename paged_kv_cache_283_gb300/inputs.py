@@ -12,7 +12,8 @@ Shapes follow the Llama 3.1 8B example of "How LLM Inference Serving Works"
 8 KV heads, head dimension 128, bf16) with blocks of 16 tokens ("Visual
 walkthrough", Step 7).  No dataset or trained weights are involved.
 
-Recipe, per workload ``idx`` (1..5):
+Recipe, per decode workload ``idx`` (1..5; the chunked-prefill step,
+``chunked_prefill``, states its own):
   rng = numpy.random.default_rng(283 + idx); draws, in this order:
   1. context lengths (or, for the shared-prefix workload, suffix lengths);
   2. the free-block order: a permutation of the pool;
@@ -185,6 +186,48 @@ def layer_inputs(w, layer):
 
 WORKLOADS = {1: tiny, 2: llama8b_batch64, 3: long_splitk, 4: shared_prefix,
              5: llama8b_32layer_batch256}
+
+
+@dataclass
+class PrefillWorkload:
+    """A chunked-prefill step: sequence b contributes query_lens[b] new tokens
+    at positions context_lens[b] - query_lens[b] .. context_lens[b] - 1."""
+    name: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    context_lens: np.ndarray
+    query_lens: np.ndarray
+    num_blocks: int
+    free_order: np.ndarray
+    scale: float
+    q: np.ndarray = None        # [T, Hq, D] bf16 bits
+    k_cache: np.ndarray = None  # [NB, Hkv, bs, D]
+    v_cache: np.ndarray = None
+
+
+def chunked_prefill(with_data=True, num_seqs=16, chunk=512):
+    """An 8192-token step of 16 prefill chunks of 512 tokens (the budget the
+    dev.to page's "Chunked prefill" section suggests for throughput on large
+    GPUs), each at an earlier context of U{0..224} whole blocks, Llama 3.1 8B
+    heads.  rng = default_rng(283 + 6): prior lengths, free-block order, q,
+    k_cache, v_cache (N(0, 1) rounded to bf16).  The K/V of the chunk's own
+    tokens are part of the pool (written by the cache write before attention)."""
+    rng = np.random.default_rng(283 + 6)
+    prior = rng.integers(0, 225, size=num_seqs).astype(np.int32) * BLOCK_SIZE
+    qlen = np.full(num_seqs, chunk, dtype=np.int32)
+    ctx = prior + qlen
+    need = int((-(-ctx.astype(np.int64) // BLOCK_SIZE)).sum())
+    nb = _pool_size(need)
+    w = PrefillWorkload("chunked prefill, 16 x 512-token chunks, prior ctx U{0..3584}", 32, 8,
+                        128, BLOCK_SIZE, ctx, qlen, nb, rng.permutation(nb).astype(np.int32),
+                        1.0 / np.sqrt(128.0))
+    if with_data:
+        w.q = normal_bf16(rng, (int(qlen.sum()), 32, 128))
+        w.k_cache = normal_bf16(rng, (nb, 8, BLOCK_SIZE, 128))
+        w.v_cache = normal_bf16(rng, (nb, 8, BLOCK_SIZE, 128))
+    return w
 
 
 def workload(idx, with_data=True):

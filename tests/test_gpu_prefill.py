@@ -103,3 +103,46 @@ def test_prefill_host_checks():
         pa.pa_prefill(torch.empty_like(dq), dq, kc, kc, t, c, qsl, 4, 0.1)  # head_dim 64
     assert pa.lib().pa_prefill_supported(128, 4, 16) == 1
     assert pa.lib().pa_prefill_supported(128, 3, 16) == 0
+
+
+def test_prefill_full_step_sampled():
+    """The 16 x 512-token chunked-prefill step the bench times, at full size;
+    the oracle checks sampled rows one by one (a row at position p is the
+    one-token chunk of the context p + 1)."""
+    from oracle.allocator import BlockAllocatorModel
+    from paged_kv_cache_283_gb300 import inputs as I
+    w = I.chunked_prefill()
+    B = len(w.context_lens)
+    m = BlockAllocatorModel(w.num_blocks, w.block_size, w.free_order)
+    for b, n in enumerate(w.context_lens.tolist()):
+        m.add_seq(b)
+        m.reserve(b, n)
+    tables = [m.block_table(b) for b in range(B)]
+    alloc = pa.BlockAllocator(w.num_blocks, w.block_size, w.free_order)
+    for b, n in enumerate(w.context_lens.tolist()):
+        alloc.add_seq(b)
+        alloc.reserve(b, n)
+    mb = max(len(t) for t in tables)
+    bt, ctx = alloc.block_tables(list(range(B)), mb)
+    for b in range(B):
+        assert list(bt[b, :len(tables[b])]) == list(tables[b])
+    qsl = np.concatenate([[0], np.cumsum(w.query_lens)]).astype(np.int32)
+    dq = dev_bf16(w.q)
+    out = torch.full_like(dq, float("nan"))
+    pa.pa_clear_device_error()
+    pa.pa_prefill(out, dq, dev_bf16(w.k_cache), dev_bf16(w.v_cache), torch.from_numpy(bt).cuda(),
+                  torch.from_numpy(ctx.astype(np.int32)).cuda(), torch.from_numpy(qsl).cuda(),
+                  int(w.query_lens.max()), w.scale)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    got = bf16_to_f64(out)
+    assert np.all(np.isfinite(got))
+    rows, refs = [], []
+    for b in range(B):
+        n, c = int(w.query_lens[b]), int(w.context_lens[b])
+        for i in (0, 1, 31, 32, 255, n - 1):
+            pos = c - n + i
+            refs.append(OP.prefill_sequence(w.q[qsl[b] + i:qsl[b] + i + 1], w.k_cache, w.v_cache,
+                                            tables[b], pos + 1, w.scale, w.block_size)[0])
+            rows.append(got[qsl[b] + i])
+    assert_close(np.stack(rows), np.stack(refs), "full chunked-prefill step, sampled rows")
