@@ -9,7 +9,7 @@
 // keys 0 .. p through the block table ("PagedAttention: Virtual Memory for
 // the KV Cache").  n = 1 is a decode step.
 //
-// Design (one CTA of 4 warps per 128 query rows):
+// Design (one CTA per 128 query rows: 8 softmax warps + 1 producer warp):
 //  * Rows are (token, head) pairs of one GQA group: 128 / G tokens x G heads,
 //    so each K/V tile loaded serves the whole group.  Q arrives by one 3-D TMA
 //    per 64-column half; K and V arrive per 16-token block by 2-D TMA (the
@@ -18,17 +18,19 @@
 //    cores read.
 //  * S = Q K^T (M = 128 rows, N = 128 keys, K = 128 dims) and O += P V
 //    (M = 128, N = 128 dims, K = 128 keys) are tcgen05.mma kind::f16 (bf16 in,
-//    fp32 accumulate) issued by one thread, with S and O in tensor memory
-//    (256 columns).  V is the MN-major operand.  Shared memory: Q 32 KiB,
-//    K and V 2 x 32 KiB each, P 2 x 32 KiB (224 KiB, one CTA per SM).
-//  * The online softmax reads its row of S from tensor memory (thread = row =
-//    TMEM lane), masks causally, keeps a running maximum that is only raised
+//    fp32 accumulate) issued by one producer thread, with S and O in tensor memory
+//    (S double-buffered: 384 of 512 columns).  V is the MN-major operand.
+//    Shared memory: Q 32 KiB, K and V 2 x 32 KiB each (160 KiB, one CTA per
+//    SM, which also holds all 512 tensor-memory columns).
+//  * The online softmax reads its row of S from tensor memory (two threads per
+//    row = TMEM lane, 64 columns each, maxima and sums combined through shared
+//    memory), masks causally, keeps a running maximum that is only raised
 //    when it grows by more than 2^8 (then O's row is rescaled in tensor
-//    memory), and writes P into shared memory in the swizzled K-major layout
-//    for the second MMA as two bf16 parts, hi = bf16(p) and lo = bf16(p - hi),
-//    each multiplied with V by its own MMA: the weights keep ~17 bits instead
-//    of bf16's 8 (a single bf16 P puts elementwise errors of several per cent
-//    on outputs that are small by cancellation).
+//    memory), and writes P back into tensor memory, over its own S, as two
+//    bf16 parts, hi = bf16(p) and lo = bf16(p - hi), each multiplied with V
+//    by its own MMA reading A from tensor memory: the weights keep ~17 bits
+//    instead of bf16's 8 (a single bf16 P puts elementwise errors of several
+//    per cent on outputs that are small by cancellation).
 //  * Every wait is bounded; on a timeout the CTA records PA_DEVERR_WAIT_TIMEOUT,
 //    lets its own copies and MMAs in flight land (bounded), frees tensor
 //    memory and returns.  Block ids and lengths in device memory are checked.
@@ -62,10 +64,11 @@ constexpr uint32_t kTmemCols = 512;     // S0: [0, 128), S1: [128, 256), O: [256
 constexpr int kQ = 0;                   // Q: 2 halves
 constexpr int kK = kQ + 2 * kHalf;      // K: 2 stages x 2 halves
 constexpr int kV = kK + 4 * kHalf;      // V: 2 stages x 2 halves
-constexpr int kP = kV + 4 * kHalf;      // P, high bf16 part: 2 halves
-constexpr int kPlo = kP + 2 * kHalf;    // P, low bf16 part: 2 halves
-constexpr int kBar = kPlo + 2 * kHalf;  // mbarriers and the TMEM address slot
-constexpr int kSmemBytes = kBar + 128 + 1024;
+constexpr int kBar = kV + 4 * kHalf;    // mbarriers and the TMEM address slot
+constexpr int kRed = kBar + 128;        // row maxima / sums of the two column halves
+constexpr int kSmemBytes = kRed + 2 * kRows * 4 + 1024;  // + alignment slack
+constexpr int kSoftmaxThreads = 256;    // two threads per row, 64 columns each
+constexpr int kThreads = kSoftmaxThreads + 32;  // + one warp for copies and MMAs
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -111,6 +114,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
 }
 
+// The same with A (M x K, K-major) read from tensor memory: bf16 pairs packed
+// in 32-bit columns, row m in lane m.
+__device__ __forceinline__ void umma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -153,6 +166,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
       "r"(v[29]), "r"(v[30]), "r"(v[31]));
 }
+// 16 consecutive columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+      "r"(v[15]));
+}
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -187,26 +218,45 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// grid (query tiles, KV heads, sequences), 128 threads.
+// Barrier of the two warps that share a TMEM lane quarter (warps w, w + 4).
+__device__ __forceinline__ void pair_sync(int warp) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+}
+
+// grid (query tiles, KV heads, sequences), 288 threads.  Warps 0-7 run the
+// softmax: thread t < 256 handles row t % 128 (TMEM lane; warps w and w + 4
+// share a lane quarter) and columns [64 h, 64 h + 64) of S and O, h = t / 128.
+// Warp 8 is the producer: its lanes issue the copies (one block per lane) and
+// its lane 0 the MMAs, so no softmax warp ever waits on the tensor core's
+// bookkeeping.
 //
-// Pipeline of one CTA over its key chunks c (thread 0 issues every copy and
-// MMA; K and V stages are released separately):
-//   top of c:   S[(c+1)&1] = Q K(c+1)^T        (MMA, overlaps softmax of c)
-//   softmax c:  read S[c&1]; K stage c&1 is free -> copy K(c+2);
-//               max / exponentials in registers;
-//               wait PV(c-1): P, O and V stage (c-1)&1 are free -> copy V(c+1);
-//               rescale O if needed, write P
-//   end of c:   O += P V(c)                      (MMA, overlaps softmax of c+1)
+// Tensor memory: S0 = columns [0, 128), S1 = [128, 256), O = [256, 384).  P of
+// chunk c replaces S of chunk c in place (hi part in the buffer's first 64
+// columns, lo part in the next 64, bf16 pairs packed per column), so P is
+// double-buffered with S.
+//
+// Producer, per chunk c:
+//   wait PV(c-1): V stage (c-1)&1 and S[(c+1)&1] (P(c-1)) are free ->
+//   copy V(c+1); wait K(c+1): S[(c+1)&1] = Q K(c+1)^T;
+//   wait QK(c): K stage c&1 is free -> copy K(c+2);
+//   wait V(c), P(c): O += P V(c).
+// Softmax warps, per chunk c: wait QK(c); read S[c&1]; row maxima (pair of
+// warps); exponentials; rescale O only if the reference maximum moved (after
+// PV(c-1)); P into S[c&1]; arrive on p_ready.
+// No softmax thread leaves the loop early (the pair barriers must stay
+// matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
   constexpr int TQ = kRows / G;  // query tokens per CTA
+  constexpr int HK = kKeys / 2;  // columns per softmax thread
+  constexpr int kProducer = kSoftmaxThreads / 32;
   griddep_wait();
   griddep_launch_dependents();
   const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   // Lengths live in device memory: check them (CTA-uniform).
   const int q0 = __ldg(p.query_start + b), q1 = __ldg(p.query_start + b + 1);
@@ -230,10 +280,17 @@ __global__ void __launch_bounds__(128, 1)
   uint64_t* s_done = k_full + 4;                               // [2] per S buffer
   uint64_t* o_done = k_full + 6;
   uint64_t* q_full = k_full + 7;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 64);
+  // [2] per S buffer, 8 warp arrivals per chunk.  One barrier per buffer: a
+  // softmax warp can finish chunk c + 1 (its scores come before PV(c)) while
+  // another is still on chunk c, and its arrival must not count for c.
+  uint64_t* p_ready = k_full + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 96);
+  float* red = reinterpret_cast<float*>(sm + kRed);            // [2][128]
 
   if (tid == 0) {
     for (int i = 0; i < 8; ++i) mbar_init(k_full + i, 1);
+    mbar_init(&p_ready[0], kSoftmaxThreads / 32);
+    mbar_init(&p_ready[1], kSoftmaxThreads / 32);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -246,247 +303,284 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S0 at +0, S1 at +128, O at +256
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tO = tmem + lane_base + 256;
+  const uint32_t tmem = *tmem_slot;
 
-  const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
-  const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV),
-                 sP = smem_u32(sm + kP), sPlo = smem_u32(sm + kPlo);
+  if (warp == kProducer) {
+    // ------------------------------------------------------------ producer
+    const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV);
+    // bookkeeping of lane 0 (chunks issued / waited for), for the drain
+    int k_iss = 0, k_wai = 0, v_iss = 0, v_wai = 0, s_iss = 0, s_wai = 0, o_iss = 0, o_wai = 0;
+    bool ok = true;  // lane 0: every wait so far succeeded
 
-  // Thread 0's bookkeeping (chunks whose copies / MMAs were issued and waited
-  // for), for the drain after a timeout.
-  int k_iss = 0, k_wai = 0, v_iss = 0, v_wai = 0, s_iss = 0, s_wai = 0, o_iss = 0, o_wai = 0;
-  bool t0ok = true;
-
-  auto block_row = [&](int c, int j) -> int {
-    int id = __ldg(tbl + c * kChunkBlocks + j);
-    if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
-      raise_error(p.err, PA_DEVERR_BLOCK_ID);
-      id = 0;
-    }
-    return (id * p.num_kv_heads + kvh) * kBS;
-  };
-  // thread 0: K (or V) of chunk c into stage c & 1
-  auto load = [&](int c, bool is_v) {
-    const int st = c & 1;
-    const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
-    uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
-    unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kHalf;
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
-    for (int j = 0; j < nb; ++j) {
-      const int row = block_row(c, j);
-      tma_2d(dst + j * kBox, is_v ? &tv : &tk, 0, row, bar);
-      tma_2d(dst + kHalf + j * kBox, is_v ? &tv : &tk, 64, row, bar);
-    }
-    if (is_v) ++v_iss; else ++k_iss;
-  };
-  // thread 0: S[c & 1] = Q K(c)^T
-  auto qk = [&](int c) {
-    const int st = c & 1;
-    tc_fence_after();
+    // K (or V) of chunk c into stage c & 1, one block per lane
+    auto load = [&](int c, bool is_v) {
+      const int st = c & 1;
+      const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
+      uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
+      unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kHalf + lane * kBox;
+      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
+      __syncwarp();
+      if (lane < nb) {
+        int id = __ldg(tbl + c * kChunkBlocks + lane);
+        if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
+          raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          id = 0;
+        }
+        const int row = (id * p.num_kv_heads + kvh) * kBS;
+        tma_2d(dst, is_v ? &tv : &tk, 0, row, bar);
+        tma_2d(dst + kHalf, is_v ? &tv : &tk, 64, row, bar);
+      }
+      __syncwarp();
+      if (is_v) ++v_iss; else ++k_iss;
+    };
+    // lane 0: S[c & 1] = Q K(c)^T
+    auto qk = [&](int c) {
+      const int st = c & 1;
+      tc_fence_after();
 #pragma unroll
-    for (int kk = 0; kk < kD / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-      umma_bf16(tmem + st * 128, sw128_desc(sQ + off, 16, 1024),
-                sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
-    }
-    umma_commit(&s_done[st]);
-    ++s_iss;
-  };
+      for (int kk = 0; kk < kD / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+        umma_bf16(tmem + st * 128, sw128_desc(sQ + off, 16, 1024),
+                  sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
+      }
+      umma_commit(&s_done[st]);
+      ++s_iss;
+    };
+    auto uniform = [&](bool v) { return __shfl_sync(kFullMask, v ? 1 : 0, 0) != 0; };
 
-  if (tid == 0) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
-    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
-    mbar_arrive_expect_tx(q_full, 2 * kHalf);
-    tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
-    tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
+    if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
+      mbar_arrive_expect_tx(q_full, 2 * kHalf);
+      tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
+      tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
+    }
     load(0, false);
     load(0, true);
     if (nchunks > 1) {
       load(1, false);
       load(1, true);
     }
-    t0ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
-    if (t0ok) {
-      ++k_wai;
-      qk(0);
-    }
-  }
-
-  // This thread's row: token it of the tile, head g of the group.
-  const int r = tid;
-  const int qi = i0 + r / G;
-  const bool row_ok = qi < n;
-  const int pos = ctx - n + qi;
-  const float sl2 = p.scale_log2;
-  float m_used = -INFINITY;  // reference maximum of the exponentials (base 2)
-  float l_sum = 0.f;
-  bool ok = true;
-  const int prow = (r >> 3) * 1024 + (r & 7) * 128;  // this row in a swizzled 128-row tile
-
-  for (int c = 0; c < nchunks; ++c) {
-    const int st = c & 1;
-    // (1) the next chunk's scores, computed while this chunk's softmax runs
-    if (tid == 0 && t0ok && c + 1 < nchunks) {
-      t0ok = mbar_wait_bounded(&k_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p.err);
-      if (t0ok) {
+    if (lane == 0) {
+      ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
+      if (ok) {
         ++k_wai;
-        qk(c + 1);
+        qk(0);
       }
     }
-    bool lok = tid == 0 ? t0ok : true;
-    // (2) this chunk's scores
-    lok = lok && mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
-    lok = __all_sync(kFullMask, lok);
-    uint32_t sv[kKeys];
-    if (lok) {
-      if (tid == 0) ++s_wai;
-      tc_fence_after();
-#pragma unroll
-      for (int q4 = 0; q4 < kKeys / 32; ++q4) {
-        uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
-        tmem_ld32(tmem + lane_base + st * 128 + 32 * q4, chunk);
+    for (int c = 0; c < nchunks && uniform(ok); ++c) {
+      const int st = c & 1;
+      if (c + 1 < nchunks) {
+        if (c > 0) {  // PV(c-1) done: V stage (c-1)&1 and P(c-1) in S[(c+1)&1] free
+          if (lane == 0) {
+            ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+            if (ok) ++o_wai;
+          }
+          if (!uniform(ok)) break;
+          if (c + 1 >= 2) load(c + 1, true);
+        }
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&k_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p.err);
+          if (ok) {
+            ++k_wai;
+            qk(c + 1);
+          }
+        }
+        if (!uniform(ok)) break;
       }
-      tmem_wait_ld();
-      // K stage st is free again
-      if (tid == 0 && c + 2 < nchunks) load(c + 2, false);
-    }
-    // (3) causal mask, maximum and exponentials, in registers
-    float alpha = 1.f, psum = 0.f;
-    if (lok) {
-      const int lim = row_ok ? pos - c * kKeys : -1;  // visible columns: j <= lim
-      float mx = -INFINITY;
-      if (__all_sync(kFullMask, lim >= kKeys - 1)) {
+      if (c + 2 < nchunks) {  // QK(c) done: K stage st free
+        if (lane == 0) {
+          ok = mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
+          if (ok) ++s_wai;
+        }
+        if (!uniform(ok)) break;
+        load(c + 2, false);
+      }
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err) &&
+             mbar_wait_bounded(&p_ready[st], (c >> 1) & 1, p.err);
+        if (ok) {
+          ++v_wai;
+          tc_fence_after();
 #pragma unroll
-        for (int j = 0; j < kKeys; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
-      } else {
-#pragma unroll
-        for (int j = 0; j < kKeys; ++j) {
-          const float v = j <= lim ? __uint_as_float(sv[j]) : -INFINITY;
-          sv[j] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
+            umma_bf16_ts(tmem + 256, tmem + st * 128 + 8 * kk, vdesc, kIdescPV,
+                         (c > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ts(tmem + 256, tmem + st * 128 + 64 + 8 * kk, vdesc, kIdescPV, 1u);
+          }
+          umma_commit(o_done);
+          ++o_iss;
         }
       }
-      mx *= sl2;
-      if (mx != -INFINITY) {
-        if (m_used == -INFINITY) {
-          m_used = mx;
-        } else if (mx > m_used + 8.f) {
-          alpha = ex2(m_used - mx);
-          m_used = mx;
-        }
-      }
-      const bool live = m_used != -INFINITY;
-      const float neg = live ? -m_used : 0.f;
-#pragma unroll
-      for (int j = 0; j < kKeys; ++j) {
-        const float e = live ? ex2(fmaf(__uint_as_float(sv[j]), sl2, neg)) : 0.f;
-        psum += e;
-        sv[j] = __float_as_uint(e);
-      }
-      l_sum = l_sum * alpha + psum;
     }
-    // (4) the previous PV product is done with P, O and its V stage
-    if (c > 0) {
-      lok = lok && mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+    // Everything this CTA issued lands before its memory is given up (the
+    // normal path waits only for the last PV, which the softmax warps wait
+    // for too; each wait is bounded).
+    if (lane == 0) {
+      for (int c = k_wai; c < k_iss; ++c) mbar_wait_bounded(&k_full[c & 1], (c >> 1) & 1, p.err);
+      for (int c = v_wai; c < v_iss; ++c) mbar_wait_bounded(&v_full[c & 1], (c >> 1) & 1, p.err);
+      for (int c = s_wai; c < s_iss; ++c) {
+        // QK of chunks whose scores only the softmax warps waited for
+        if (c < nchunks - 2 || !ok) mbar_wait_bounded(&s_done[c & 1], (c >> 1) & 1, p.err);
+      }
+      if (o_iss > o_wai) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int hcol = tid >> 7;  // column half
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO = tmem + lane_base + 256 + 64 * hcol;
+    const int r = tid & (kRows - 1);  // row: token r / G of the tile, head r % G
+    const int qi = i0 + r / G;
+    const bool row_ok = qi < n;
+    const int pos = ctx - n + qi;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY;  // reference maximum of the exponentials (base 2)
+    float l_sum = 0.f;
+    bool ok = true;  // sticky: this thread's waits all succeeded
+    const int prow = (r >> 3) * 1024 + (r & 7) * 128;  // row in a swizzled 128-row tile
+
+    for (int c = 0; c < nchunks; ++c) {
+      const int st = c & 1;
+      bool lok = ok && mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
       lok = __all_sync(kFullMask, lok);
-      if (lok && tid == 0) ++o_wai;
-    }
-    if (lok) {
-      if (tid == 0 && c + 1 < nchunks && c + 1 >= 2) load(c + 1, true);
+      uint32_t sv[HK];
+      if (lok) {
+        tc_fence_after();
+#pragma unroll
+        for (int q4 = 0; q4 < HK / 32; ++q4) {
+          uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
+          tmem_ld32(tmem + lane_base + st * 128 + HK * hcol + 32 * q4, chunk);
+        }
+        tmem_wait_ld();
+      }
+      // causal mask and this half's maximum
+      float mx = -INFINITY;
+      if (lok) {
+        const int lim = row_ok ? pos - c * kKeys - HK * hcol : -1;  // visible: j <= lim
+        if (__all_sync(kFullMask, lim >= HK - 1)) {
+#pragma unroll
+          for (int j = 0; j < HK; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < HK; ++j) {
+            const float v = j <= lim ? __uint_as_float(sv[j]) : -INFINITY;
+            sv[j] = __float_as_uint(v);
+            mx = fmaxf(mx, v);
+          }
+        }
+      }
+      // the row's maximum over both halves (warps w and w + 4); the second
+      // barrier also orders both halves' reads of S before the writes of P
+      tc_fence_before();
+      red[hcol * kRows + r] = mx;
+      pair_sync(warp);
+      mx = fmaxf(red[r], red[kRows + r]) * sl2;
+      pair_sync(warp);
       tc_fence_after();
-      // Rescale this row of O when its reference maximum moved (c == 0: the
-      // first PV MMA overwrites O).
-      if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+      float alpha = 1.f;
+      if (lok) {
+        if (mx != -INFINITY) {
+          if (m_used == -INFINITY) {
+            m_used = mx;
+          } else if (mx > m_used + 8.f) {
+            alpha = ex2(m_used - mx);
+            m_used = mx;
+          }
+        }
+        const bool live = m_used != -INFINITY;
+        const float neg = live ? -m_used : 0.f;
+        float psum = 0.f;
 #pragma unroll
-        for (int q4 = 0; q4 < kD / 32; ++q4) {
-          uint32_t o[32];
-          tmem_ld32(tO + 32 * q4, o);
-          tmem_wait_ld();
+        for (int j = 0; j < HK; ++j) {
+          const float e = live ? ex2(fmaf(__uint_as_float(sv[j]), sl2, neg)) : 0.f;
+          psum += e;
+          sv[j] = __float_as_uint(e);
+        }
+        l_sum = l_sum * alpha + psum;
+        // rescale this half of O's row when the reference maximum moved; PV(c-1)
+        // must be done with O first (c == 0: the first PV overwrites O)
+        if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
+          lok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+          lok = __all_sync(kFullMask, lok);
+          if (lok) {
+            tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-          tmem_st32(tO + 32 * q4, o);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              uint32_t o[16];
+              tmem_ld16(tO + 16 * q4, o);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+              tmem_st16(tO + 16 * q4, o);
+            }
+          }
+        }
+      }
+      if (lok) {
+        // P into S[st]: hi = bf16(p), lo = bf16(p - hi), pairs packed
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          uint32_t wh[16], wl[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float a = __uint_as_float(sv[32 * q2 + 2 * k]);
+            const float e = __uint_as_float(sv[32 * q2 + 2 * k + 1]);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(a, e);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(a - hf.x, e - hf.y);
+            wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
+            wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
+          }
+          tmem_st16(tmem + lane_base + st * 128 + 32 * hcol + 16 * q2, wh);
+          tmem_st16(tmem + lane_base + st * 128 + 64 + 32 * hcol + 16 * q2, wl);
         }
         tmem_wait_st();
       }
-      // P as hi + lo bf16 parts into the swizzled K-major tiles
-#pragma unroll
-      for (int cc = 0; cc < kKeys / 8; ++cc) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float a = __uint_as_float(sv[8 * cc + 2 * k]);
-          const float e = __uint_as_float(sv[8 * cc + 2 * k + 1]);
-          const __nv_bfloat162 hi = __floats2bfloat162_rn(a, e);
-          const float2 hf = __bfloat1622float2(hi);
-          const __nv_bfloat162 lo = __floats2bfloat162_rn(a - hf.x, e - hf.y);
-          wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
-          wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
-        }
-        const int off = prow + (cc >> 3) * kHalf + (((cc & 7) ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm + kP + off) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(sm + kPlo + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-      }
-    }
-    // (5) V of this chunk has landed.  Keys past the last visible one in the
-    // final chunk may hold anything in V (a partly filled block, or blocks not
-    // loaded); P is 0 there, but 0 * NaN is not, so those rows are zeroed.
-    const int vk = nk - c * kKeys;  // valid keys in this chunk
-    if (lok && (vk < kKeys || tid == 0)) {
-      lok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err);
-      if (lok && r >= vk) {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + h) * kHalf + prow);
+      // V of the final chunk: keys past the last visible one may hold anything
+      // (a partly filled block, or blocks not loaded); P is 0 there, but
+      // 0 * NaN is not, so those rows are zeroed once the copies have landed.
+      const int vk = nk - c * kKeys;  // valid keys in this chunk
+      if (lok && vk < kKeys) {
+        lok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err);
+        if (lok && r >= vk) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hcol) * kHalf + prow);
 #pragma unroll
           for (int k = 0; k < 8; ++k) row[k] = z;
         }
       }
+      ok = lok;
+      // hand P, O and the zeroed V rows to the producer: one arrival per warp
+      fence_proxy_async();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_ready[st]);
     }
-    fence_proxy_async();
-    tc_fence_before();
-    if (!__syncthreads_and(lok)) {
-      ok = false;
-      break;
-    }
-    // (6) O += P V(c), hi and lo parts
-    if (tid == 0) {
-      ++v_wai;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kKeys / 16; ++kk) {
-        const uint32_t aoff = (kk >> 2) * kHalf + (kk & 3) * 32;
-        const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
-        umma_bf16(tmem + 256, sw128_desc(sP + aoff, 16, 1024), vdesc, kIdescPV,
-                  (c > 0 || kk > 0) ? 1u : 0u);
-        umma_bf16(tmem + 256, sw128_desc(sPlo + aoff, 16, 1024), vdesc, kIdescPV, 1u);
-      }
-      umma_commit(o_done);
-      ++o_iss;
-    }
-  }
 
-  if (ok) {
-    bool lok = mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
+    // Epilogue: O / l, both halves' sums combined through shared memory.
+    bool lok = ok && mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
+    red[hcol * kRows + r] = l_sum;
+    asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
     if (lok) {
-      if (tid == 0) ++o_wai;
       tc_fence_after();
-      const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads + kvh * G + r % G) *
-                      kD;
+      const float lt = red[r] + red[kRows + r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* orow = p.out +
+                            (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads +
+                             kvh * G + r % G) * kD + 64 * hcol;
 #pragma unroll
-      for (int q4 = 0; q4 < kD / 32; ++q4) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * q4, o);
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t o[16];
+        tmem_ld16(tO + 16 * q4, o);
         tmem_wait_ld();
         if (row_ok) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 2; ++k) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -495,21 +589,12 @@ __global__ void __launch_bounds__(128, 1)
                                         __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
               w[e] = *reinterpret_cast<const uint32_t*>(&h2);
             }
-            *reinterpret_cast<uint4*>(orow + 32 * q4 + 8 * k) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(orow + 16 * q4 + 8 * k) =
+                make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
       }
-    } else {
-      ok = false;
     }
-  }
-  if (!ok && tid == 0) {
-    // Let this CTA's own copies and MMAs in flight land before its shared and
-    // tensor memory are given up (each wait bounded).
-    for (int c = k_wai; c < k_iss; ++c) mbar_wait_bounded(&k_full[c & 1], (c >> 1) & 1, p.err);
-    for (int c = v_wai; c < v_iss; ++c) mbar_wait_bounded(&v_full[c & 1], (c >> 1) & 1, p.err);
-    for (int c = s_wai; c < s_iss; ++c) mbar_wait_bounded(&s_done[c & 1], (c >> 1) & 1, p.err);
-    if (o_iss > o_wai) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
   }
   tc_fence_before();
   __syncthreads();
@@ -587,7 +672,7 @@ cudaError_t launch_prefill_g(const CUtensorMap& tq, const CUtensorMap& tk, const
   }
   const int tiles = (max_query_len + kRows / G - 1) / (kRows / G);
   const dim3 grid(tiles, p.num_kv_heads, num_seqs);
-  return launch_pdl(kernel, grid, dim3(128), kSmemBytes, stream, tq, tk, tv, p);
+  return launch_pdl(kernel, grid, dim3(kThreads), kSmemBytes, stream, tq, tk, tv, p);
 }
 
 bool aligned16(const void* ptr) { return ptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
