@@ -236,8 +236,8 @@ __device__ __forceinline__ void pair_sync(int warp) {
 // double-buffered with S.
 //
 // Producer, per chunk c:
-//   wait PV(c-1): V stage (c-1)&1 and S[(c+1)&1] (P(c-1)) are free ->
-//   copy V(c+1); wait K(c+1): S[(c+1)&1] = Q K(c+1)^T;
+//   wait PV(c-1): S[(c+1)&1] (P(c-1)) and V stage (c-1)&1 are free;
+//   wait K(c+1): S[(c+1)&1] = Q K(c+1)^T; copy V(c+1);
 //   wait QK(c): K stage c&1 is free -> copy K(c+2);
 //   wait V(c), P(c): O += P V(c).
 // Softmax warps, per chunk c: wait QK(c); read S[c&1]; row maxima (pair of
@@ -313,8 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k_iss = 0, k_wai = 0, v_iss = 0, v_wai = 0, s_iss = 0, s_wai = 0, o_iss = 0, o_wai = 0;
     bool ok = true;  // lane 0: every wait so far succeeded
 
+    // Block ids: lane j < 8 holds the id of block j of a chunk (checked; a bad
+    // id is never dereferenced, block 0 is read instead).  They are fetched
+    // one load ahead so that the table's latency stays off the MMA issue path.
+    auto fetch_ids = [&](int c) -> int {
+      if (c >= nchunks || lane >= min(kChunkBlocks, nblk_all - c * kChunkBlocks)) return 0;
+      int id = __ldg(tbl + c * kChunkBlocks + lane);
+      if (id < 0 || id >= p.num_blocks) {
+        raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        id = 0;
+      }
+      return id;
+    };
     // K (or V) of chunk c into stage c & 1, one block per lane
-    auto load = [&](int c, bool is_v) {
+    auto load = [&](int c, bool is_v, int id) {
       const int st = c & 1;
       const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
       uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
@@ -322,11 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
       __syncwarp();
       if (lane < nb) {
-        int id = __ldg(tbl + c * kChunkBlocks + lane);
-        if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
-          raise_error(p.err, PA_DEVERR_BLOCK_ID);
-          id = 0;
-        }
         const int row = (id * p.num_kv_heads + kvh) * kBS;
         tma_2d(dst, is_v ? &tv : &tk, 0, row, bar);
         tma_2d(dst + kHalf, is_v ? &tv : &tk, 64, row, bar);
@@ -357,12 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
       tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
     }
-    load(0, false);
-    load(0, true);
-    if (nchunks > 1) {
-      load(1, false);
-      load(1, true);
+    {
+      const int id0 = fetch_ids(0), id1 = fetch_ids(1);
+      load(0, false, id0);
+      load(0, true, id0);
+      if (nchunks > 1) {
+        load(1, false, id1);
+        load(1, true, id1);
+      }
     }
+    int id_k = fetch_ids(2);  // ids of the next K load (chunk c + 2)
+    int id_v = 0;             // ids of the next V load (chunk c + 1)
     if (lane == 0) {
       ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
       if (ok) {
@@ -373,15 +385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int c = 0; c < nchunks && uniform(ok); ++c) {
       const int st = c & 1;
       if (c + 1 < nchunks) {
-        if (c > 0) {  // PV(c-1) done: V stage (c-1)&1 and P(c-1) in S[(c+1)&1] free
-          if (lane == 0) {
-            ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
-            if (ok) ++o_wai;
-          }
-          if (!uniform(ok)) break;
-          if (c + 1 >= 2) load(c + 1, true);
+        // PV(c-1) done: P(c-1) in S[(c+1)&1] and V stage (c-1)&1 are free
+        if (lane == 0 && c > 0) {
+          ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+          if (ok) ++o_wai;
         }
-        if (lane == 0) {
+        if (lane == 0 && ok) {
           ok = mbar_wait_bounded(&k_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p.err);
           if (ok) {
             ++k_wai;
@@ -389,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!uniform(ok)) break;
+        if (c + 1 >= 2) load(c + 1, true, id_v);
       }
       if (c + 2 < nchunks) {  // QK(c) done: K stage st free
         if (lane == 0) {
@@ -396,8 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ++s_wai;
         }
         if (!uniform(ok)) break;
-        load(c + 2, false);
+        load(c + 2, false, id_k);
       }
+      id_v = id_k;             // chunk c + 2's V is loaded next iteration
+      id_k = fetch_ids(c + 3);
       if (lane == 0) {
         ok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err) &&
              mbar_wait_bounded(&p_ready[st], (c >> 1) & 1, p.err);
@@ -561,8 +573,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&p_ready[st]);
     }
 
-    // Epilogue: O / l, both halves' sums combined through shared memory.
-    bool lok = ok && mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
+    // Epilogue: O / l, both halves' sums combined through shared memory.  A
+    // softmax warp can finish the last chunk before PV of the one before it
+    // completes; o_done then still owes two phases, and a parity wait for the
+    // last one alone would match the phase before those and return early.
+    // So the two are waited for in order.
+    bool lok = ok;
+    if (nchunks >= 2) lok = lok && mbar_wait_bounded(o_done, (nchunks - 2) & 1, p.err);
+    lok = lok && mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
     red[hcol * kRows + r] = l_sum;
     asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
