@@ -319,6 +319,21 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                      int num_blocks, float scale, pa_stream_t stream);
 
+/*
+ * Step planning for chunked prefill (host; "How LLM Inference Serving Works",
+ * section "Chunked prefill").  Each step has a token budget
+ * (max_num_batched_tokens): every pending decode (one token each) is taken
+ * first, the remaining budget goes to the pending prefills in queue order, and
+ * a prefill that does not fit is cut to what is left.  With more decodes than
+ * the budget, the first `budget` decodes run and no prefill does.
+ *   prefill_remaining[i]: tokens still to prefill for queued request i;
+ *   chunk_out[i]: tokens of request i scheduled this step (0: none);
+ *   *decodes_out: decodes scheduled.
+ * PA_ERR_INVALID_ARG on a negative count or a missing pointer.
+ */
+pa_status pa_plan_step(int budget, int num_decodes, const int32_t* prefill_remaining,
+                       int num_prefills, int32_t* chunk_out, int* decodes_out);
+
 /* ------------------------------------------------------------------------ */
 /* Host block allocator [PA], [SH], [LIFE], [OOM], [WALK].  Not thread-safe;
  * one allocator per caller thread or external locking.  Deterministic: the

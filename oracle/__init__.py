@@ -28,6 +28,8 @@ Modules:
                  statistics and the log-sum-exp merge.
 * ``prefill``    causal attention of a chunk of new tokens over the paged
                  cache (chunked prefill; one token = one decode step).
+* ``scheduler``  the chunked-prefill step budget (decodes first, then
+                 prefill chunks in queue order).
 * ``quant``      the INT8 KV scheme: per-row quantisation, the INT8 cache
                  write and the INT8 decode.
 * ``cache``      the cache write (scatter of new K/V through a slot mapping).

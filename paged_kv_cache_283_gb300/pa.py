@@ -54,6 +54,7 @@ SIGNATURES = {
     "pa_prefill_supported": (_i, [_i, _i, _i]),
     "pa_prefill": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i,
                         _f, _vp]),
+    "pa_plan_step": (_i, [_i, _i, _vp, _i, _vp, _pint]),
     "pa_alloc_create": (_i, [_i, _i, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_add_seq": (_i, [_vp, _i]),
@@ -371,6 +372,19 @@ def pa_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start
                           int(max_query_len), B, T, hq, hkv, d, bs, nb, float(scale),
                           _stream(stream))
     _check(st, "pa_prefill")
+
+
+def pa_plan_step(budget, num_decodes, prefill_remaining):
+    """(decodes scheduled, numpy int32 tokens per queued prefill) for one step."""
+    import numpy as np
+    rem = np.ascontiguousarray(prefill_remaining, dtype=np.int32)
+    out = np.zeros_like(rem)
+    dec = ctypes.c_int()
+    _check(lib().pa_plan_step(int(budget), int(num_decodes),
+                              rem.ctypes.data_as(ctypes.c_void_p), int(rem.shape[0]),
+                              out.ctypes.data_as(ctypes.c_void_p), ctypes.byref(dec)),
+           "pa_plan_step")
+    return dec.value, out
 
 
 class DecodeStep:
