@@ -9,18 +9,18 @@
 // keys 0 .. p through the block table ("PagedAttention: Virtual Memory for
 // the KV Cache").  n = 1 is a decode step.
 //
-// Design (one CTA per 128 query rows: 8 softmax warps + 1 producer warp):
+// Design (one CTA per 128 query rows: 8 softmax warps, an MMA warp, a copy warp):
 //  * Rows are (token, head) pairs of one GQA group: 128 / G tokens x G heads,
 //    so each K/V tile loaded serves the whole group.  Q arrives by one 3-D TMA
 //    per 64-column half; K and V arrive per 16-token block by 2-D TMA (the
 //    block table is a gather of 16-row boxes), 8 blocks = 128 keys per chunk,
-//    two chunk stages.  TMA writes the 128-byte-swizzled layout the tensor
+//    three chunk stages each.  TMA writes the 128-byte-swizzled layout the tensor
 //    cores read.
 //  * S = Q K^T (M = 128 rows, N = 128 keys, K = 128 dims) and O += P V
 //    (M = 128, N = 128 dims, K = 128 keys) are tcgen05.mma kind::f16 (bf16 in,
-//    fp32 accumulate) issued by one producer thread, with S and O in tensor memory
+//    fp32 accumulate) issued by one thread of the MMA warp, with S and O in tensor memory
 //    (S double-buffered: 384 of 512 columns).  V is the MN-major operand.
-//    Shared memory: Q 32 KiB, K and V 2 x 32 KiB each (160 KiB, one CTA per
+//    Shared memory: Q 32 KiB, K and V 3 x 32 KiB each (224 KiB, one CTA per
 //    SM, which also holds all 512 tensor-memory columns).
 //  * The online softmax reads its row of S from tensor memory (two threads per
 //    row = TMEM lane, 64 columns each, maxima and sums combined through shared
@@ -62,13 +62,14 @@ constexpr uint32_t kTmemCols = 512;     // S0: [0, 128), S1: [128, 256), O: [256
 
 // Shared memory, from a 1024-byte aligned base (the swizzle atom).
 constexpr int kQ = 0;                   // Q: 2 halves
-constexpr int kK = kQ + 2 * kHalf;      // K: 2 stages x 2 halves
-constexpr int kV = kK + 4 * kHalf;      // V: 2 stages x 2 halves
-constexpr int kBar = kV + 4 * kHalf;    // mbarriers and the TMEM address slot
-constexpr int kRed = kBar + 128;        // row maxima / sums of the two column halves
+constexpr int kStages = 3;              // K and V ring depth (chunks)
+constexpr int kK = kQ + 2 * kHalf;      // K: 3 stages x 2 halves
+constexpr int kV = kK + 2 * kStages * kHalf;  // V: 3 stages x 2 halves
+constexpr int kBar = kV + 2 * kStages * kHalf;  // mbarriers and the TMEM address slot
+constexpr int kRed = kBar + 256;        // row maxima / sums of the two column halves
 constexpr int kSmemBytes = kRed + 2 * kRows * 4 + 1024;  // + alignment slack
 constexpr int kSoftmaxThreads = 256;    // two threads per row, 64 columns each
-constexpr int kThreads = kSoftmaxThreads + 32;  // + one warp for copies and MMAs
+constexpr int kThreads = kSoftmaxThreads + 64;  // + an MMA warp and a copy warp
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -223,26 +224,26 @@ __device__ __forceinline__ void pair_sync(int warp) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
 }
 
-// grid (query tiles, KV heads, sequences), 288 threads.  Warps 0-7 run the
+// grid (query tiles, KV heads, sequences), 320 threads.  Warps 0-7 run the
 // softmax: thread t < 256 handles row t % 128 (TMEM lane; warps w and w + 4
 // share a lane quarter) and columns [64 h, 64 h + 64) of S and O, h = t / 128.
-// Warp 8 is the producer: its lanes issue the copies (one block per lane) and
-// its lane 0 the MMAs, so no softmax warp ever waits on the tensor core's
-// bookkeeping.
+// Warp 8 issues the MMAs (lane 0), warp 9 the copies (one block per lane), so
+// that neither chain waits on the other's latencies.
 //
 // Tensor memory: S0 = columns [0, 128), S1 = [128, 256), O = [256, 384).  P of
 // chunk c replaces S of chunk c in place (hi part in the buffer's first 64
 // columns, lo part in the next 64, bf16 pairs packed per column), so P is
-// double-buffered with S.
+// double-buffered with S.  K and V run in 3-chunk rings; every stage has a
+// "full" barrier (copies landed) and a "free" barrier (committed after the
+// MMA that read it), so each wait names one use of one stage.
 //
-// Producer, per chunk c:
-//   wait PV(c-1): S[(c+1)&1] (P(c-1)) and V stage (c-1)&1 are free;
-//   wait K(c+1): S[(c+1)&1] = Q K(c+1)^T; copy V(c+1);
-//   wait QK(c): K stage c&1 is free -> copy K(c+2);
-//   wait V(c), P(c): O += P V(c).
-// Softmax warps, per chunk c: wait QK(c); read S[c&1]; row maxima (pair of
-// warps); exponentials; rescale O only if the reference maximum moved (after
-// PV(c-1)); P into S[c&1]; arrive on p_ready.
+// MMA warp, per chunk c:  wait PV(c-1) (S[(c+1)&1] holds P(c-1)) and K(c+1):
+//   S[(c+1)&1] = Q K(c+1)^T; wait V(c) and P(c): O += P V(c).
+// Copy warp, per chunk c: wait K stage of c free: copy K(c+3); wait V stage of
+//   c-1 free: copy V(c+2).
+// Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
+//   exponentials; rescale O only if the reference maximum moved (after
+//   PV(c-1)); P into S[c&1]; arrive on p_ready[c&1].
 // No softmax thread leaves the loop early (the pair barriers must stay
 // matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                          const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
   constexpr int TQ = kRows / G;  // query tokens per CTA
   constexpr int HK = kKeys / 2;  // columns per softmax thread
-  constexpr int kProducer = kSoftmaxThreads / 32;
+  constexpr int kMmaWarp = kSoftmaxThreads / 32, kCopyWarp = kMmaWarp + 1;
   griddep_wait();
   griddep_launch_dependents();
   const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -275,20 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + kBar);  // [2] per K stage
-  uint64_t* v_full = k_full + 2;                               // [2] per V stage
-  uint64_t* s_done = k_full + 4;                               // [2] per S buffer
-  uint64_t* o_done = k_full + 6;
-  uint64_t* q_full = k_full + 7;
+  uint64_t* k_full = reinterpret_cast<uint64_t*>(sm + kBar);  // [3] copies landed
+  uint64_t* v_full = k_full + 3;                               // [3]
+  uint64_t* k_free = k_full + 6;                               // [3] QK that read it done
+  uint64_t* v_free = k_full + 9;                               // [3] PV that read it done
+  uint64_t* s_done = k_full + 12;                              // [2] per S buffer
+  uint64_t* o_done = k_full + 14;
+  uint64_t* q_full = k_full + 15;
   // [2] per S buffer, 8 warp arrivals per chunk.  One barrier per buffer: a
   // softmax warp can finish chunk c + 1 (its scores come before PV(c)) while
   // another is still on chunk c, and its arrival must not count for c.
-  uint64_t* p_ready = k_full + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 96);
+  uint64_t* p_ready = k_full + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
   float* red = reinterpret_cast<float*>(sm + kRed);            // [2][128]
 
   if (tid == 0) {
-    for (int i = 0; i < 8; ++i) mbar_init(k_full + i, 1);
+    for (int i = 0; i < 16; ++i) mbar_init(k_full + i, 1);
     mbar_init(&p_ready[0], kSoftmaxThreads / 32);
     mbar_init(&p_ready[1], kSoftmaxThreads / 32);
     fence_mbar_init();
@@ -305,57 +308,38 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kProducer) {
-    // ------------------------------------------------------------ producer
+  if (warp == kCopyWarp) {
+    // ------------------------------------------------------------ copies
     const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV);
-    // bookkeeping of lane 0 (chunks issued / waited for), for the drain
-    int k_iss = 0, k_wai = 0, v_iss = 0, v_wai = 0, s_iss = 0, s_wai = 0, o_iss = 0, o_wai = 0;
-    bool ok = true;  // lane 0: every wait so far succeeded
-
-    // Block ids: lane j < 8 holds the id of block j of a chunk (checked; a bad
-    // id is never dereferenced, block 0 is read instead).  They are fetched
-    // one load ahead so that the table's latency stays off the MMA issue path.
-    auto fetch_ids = [&](int c) -> int {
+    int last_k = -1, last_v = -1;  // last chunk copied into each ring (for the drain)
+    bool ok = true;                // lane 0: every wait so far succeeded
+    auto uniform = [&](bool v) { return __shfl_sync(kFullMask, v ? 1 : 0, 0) != 0; };
+    // Lane j < 8: the raw table entry of block j of chunk c (checked at use),
+    // fetched a chunk ahead so that the table's latency stays off the copies.
+    auto fetch_id = [&](int c) -> int {
       if (c >= nchunks || lane >= min(kChunkBlocks, nblk_all - c * kChunkBlocks)) return 0;
-      int id = __ldg(tbl + c * kChunkBlocks + lane);
-      if (id < 0 || id >= p.num_blocks) {
-        raise_error(p.err, PA_DEVERR_BLOCK_ID);
-        id = 0;
-      }
-      return id;
+      return __ldg(tbl + c * kChunkBlocks + lane);
     };
-    // K (or V) of chunk c into stage c & 1, one block per lane
+    // K (or V) of chunk c into stage c % 3, one block per lane
     auto load = [&](int c, bool is_v, int id) {
-      const int st = c & 1;
+      const int st = c % kStages;
       const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
       uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
       unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kHalf + lane * kBox;
       if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
       __syncwarp();
       if (lane < nb) {
+        if (id < 0 || id >= p.num_blocks) {  // never dereferenced: block 0 is read instead
+          raise_error(p.err, PA_DEVERR_BLOCK_ID);
+          id = 0;
+        }
         const int row = (id * p.num_kv_heads + kvh) * kBS;
         tma_2d(dst, is_v ? &tv : &tk, 0, row, bar);
         tma_2d(dst + kHalf, is_v ? &tv : &tk, 64, row, bar);
       }
       __syncwarp();
-      if (is_v) ++v_iss; else ++k_iss;
+      if (is_v) last_v = c; else last_k = c;
     };
-    // lane 0: S[c & 1] = Q K(c)^T
-    auto qk = [&](int c) {
-      const int st = c & 1;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-        umma_bf16(tmem + st * 128, sw128_desc(sQ + off, 16, 1024),
-                  sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
-      }
-      umma_commit(&s_done[st]);
-      ++s_iss;
-    };
-    auto uniform = [&](bool v) { return __shfl_sync(kFullMask, v ? 1 : 0, 0) != 0; };
-
     if (lane == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
@@ -365,81 +349,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
     }
     {
-      const int id0 = fetch_ids(0), id1 = fetch_ids(1);
-      load(0, false, id0);
-      load(0, true, id0);
-      if (nchunks > 1) {
-        load(1, false, id1);
-        load(1, true, id1);
-      }
-    }
-    int id_k = fetch_ids(2);  // ids of the next K load (chunk c + 2)
-    int id_v = 0;             // ids of the next V load (chunk c + 1)
-    if (lane == 0) {
-      ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
-      if (ok) {
-        ++k_wai;
-        qk(0);
-      }
-    }
-    for (int c = 0; c < nchunks && uniform(ok); ++c) {
-      const int st = c & 1;
-      if (c + 1 < nchunks) {
-        // PV(c-1) done: P(c-1) in S[(c+1)&1] and V stage (c-1)&1 are free
-        if (lane == 0 && c > 0) {
-          ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
-          if (ok) ++o_wai;
-        }
-        if (lane == 0 && ok) {
-          ok = mbar_wait_bounded(&k_full[(c + 1) & 1], ((c + 1) >> 1) & 1, p.err);
-          if (ok) {
-            ++k_wai;
-            qk(c + 1);
-          }
-        }
-        if (!uniform(ok)) break;
-        if (c + 1 >= 2) load(c + 1, true, id_v);
-      }
-      if (c + 2 < nchunks) {  // QK(c) done: K stage st free
-        if (lane == 0) {
-          ok = mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
-          if (ok) ++s_wai;
-        }
-        if (!uniform(ok)) break;
-        load(c + 2, false, id_k);
-      }
-      id_v = id_k;             // chunk c + 2's V is loaded next iteration
-      id_k = fetch_ids(c + 3);
-      if (lane == 0) {
-        ok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err) &&
-             mbar_wait_bounded(&p_ready[st], (c >> 1) & 1, p.err);
-        if (ok) {
-          ++v_wai;
-          tc_fence_after();
+      int ids[kStages];
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
-            umma_bf16_ts(tmem + 256, tmem + st * 128 + 8 * kk, vdesc, kIdescPV,
-                         (c > 0 || kk > 0) ? 1u : 0u);
-            umma_bf16_ts(tmem + 256, tmem + st * 128 + 64 + 8 * kk, vdesc, kIdescPV, 1u);
-          }
-          umma_commit(o_done);
-          ++o_iss;
+      for (int c = 0; c < kStages; ++c) ids[c] = fetch_id(c);
+#pragma unroll
+      for (int c = 0; c < kStages; ++c) {
+        if (c < nchunks) {
+          load(c, false, ids[c]);
+          load(c, true, ids[c]);
         }
       }
     }
-    // Everything this CTA issued lands before its memory is given up (the
-    // normal path waits only for the last PV, which the softmax warps wait
-    // for too; each wait is bounded).
-    if (lane == 0) {
-      for (int c = k_wai; c < k_iss; ++c) mbar_wait_bounded(&k_full[c & 1], (c >> 1) & 1, p.err);
-      for (int c = v_wai; c < v_iss; ++c) mbar_wait_bounded(&v_full[c & 1], (c >> 1) & 1, p.err);
-      for (int c = s_wai; c < s_iss; ++c) {
-        // QK of chunks whose scores only the softmax warps waited for
-        if (c < nchunks - 2 || !ok) mbar_wait_bounded(&s_done[c & 1], (c >> 1) & 1, p.err);
+    int id_k = fetch_id(kStages);      // ids of the next K copy (chunk c + 3)
+    int id_v = 0;                      // ids of the next V copy (chunk c + 2)
+    for (int c = 0; c + 2 < nchunks && uniform(ok); ++c) {
+      if (c + 3 < nchunks) {  // QK(c) has read K stage c % 3
+        if (lane == 0) ok = mbar_wait_bounded(&k_free[c % kStages], (c / kStages) & 1, p.err);
+        if (!uniform(ok)) break;
+        load(c + 3, false, id_k);
       }
-      if (o_iss > o_wai) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
+      if (c >= 1) {           // PV(c-1) has read V stage (c-1) % 3 = (c+2) % 3
+        if (lane == 0)
+          ok = mbar_wait_bounded(&v_free[(c - 1) % kStages], ((c - 1) / kStages) & 1, p.err);
+        if (!uniform(ok)) break;
+        load(c + 2, true, id_v);
+      }
+      id_v = id_k;            // chunk c + 3's V is copied next iteration
+      id_k = fetch_id(c + 4);
     }
+    // Copies this warp issued land before the CTA's shared memory is given up
+    // (earlier uses of a stage completed before its last copy was issued).
+    if (lane == 0) {
+      for (int st = 0; st < kStages; ++st) {
+        const int ck = last_k - ((last_k - st) % kStages + kStages) % kStages;
+        const int cv = last_v - ((last_v - st) % kStages + kStages) % kStages;
+        if (ck >= 0) mbar_wait_bounded(&k_full[st], (ck / kStages) & 1, p.err);
+        if (cv >= 0) mbar_wait_bounded(&v_full[st], (cv / kStages) & 1, p.err);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------ MMAs
+    const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV);
+    int s_iss = 0, o_iss = 0;  // MMAs committed (for the drain)
+    if (lane == 0) {
+      // lane 0: S[c & 1] = Q K(c)^T
+      auto qk = [&](int c) {
+        const int sb = c & 1, st = c % kStages;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
+          umma_bf16(tmem + sb * 128, sw128_desc(sQ + off, 16, 1024),
+                    sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
+        }
+        umma_commit(&s_done[sb]);
+        umma_commit(&k_free[st]);
+        ++s_iss;
+      };
+      bool ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
+      if (ok) qk(0);
+      for (int c = 0; c < nchunks && ok; ++c) {
+        const int sb = c & 1, st = c % kStages;
+        if (c + 1 < nchunks) {
+          // PV(c-1) is done with P(c-1) in S[(c+1)&1]
+          if (c > 0) ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+          ok = ok && mbar_wait_bounded(&k_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, p.err);
+          if (!ok) break;
+          qk(c + 1);
+        }
+        ok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err) &&
+             mbar_wait_bounded(&p_ready[sb], (c >> 1) & 1, p.err);
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
+          umma_bf16_ts(tmem + 256, tmem + sb * 128 + 8 * kk, vdesc, kIdescPV,
+                       (c > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + 256, tmem + sb * 128 + 64 + 8 * kk, vdesc, kIdescPV, 1u);
+        }
+        umma_commit(o_done);
+        umma_commit(&v_free[st]);
+        ++o_iss;
+      }
+      // The MMAs issued complete before tensor and shared memory are given up
+      // (each commit covers every MMA before it).
+      if (o_iss > 0) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
+      if (s_iss > 0) mbar_wait_bounded(&s_done[(s_iss - 1) & 1], ((s_iss - 1) >> 1) & 1, p.err);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int hcol = tid >> 7;  // column half
@@ -456,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int prow = (r >> 3) * 1024 + (r & 7) * 128;  // row in a swizzled 128-row tile
 
     for (int c = 0; c < nchunks; ++c) {
-      const int st = c & 1;
-      bool lok = ok && mbar_wait_bounded(&s_done[st], (c >> 1) & 1, p.err);
+      const int sb = c & 1;
+      bool lok = ok && mbar_wait_bounded(&s_done[sb], (c >> 1) & 1, p.err);
       lok = __all_sync(kFullMask, lok);
       uint32_t sv[HK];
       if (lok) {
@@ -465,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < HK / 32; ++q4) {
           uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
-          tmem_ld32(tmem + lane_base + st * 128 + HK * hcol + 32 * q4, chunk);
+          tmem_ld32(tmem + lane_base + sb * 128 + HK * hcol + 32 * q4, chunk);
         }
         tmem_wait_ld();
       }
@@ -473,17 +471,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       float mx = -INFINITY;
       if (lok) {
         const int lim = row_ok ? pos - c * kKeys - HK * hcol : -1;  // visible: j <= lim
-        if (__all_sync(kFullMask, lim >= HK - 1)) {
+        if (!__all_sync(kFullMask, lim >= HK - 1)) {
 #pragma unroll
-          for (int j = 0; j < HK; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
-        } else {
-#pragma unroll
-          for (int j = 0; j < HK; ++j) {
-            const float v = j <= lim ? __uint_as_float(sv[j]) : -INFINITY;
-            sv[j] = __float_as_uint(v);
-            mx = fmaxf(mx, v);
-          }
+          for (int j = 0; j < HK; ++j)
+            if (j > lim) sv[j] = __float_as_uint(-INFINITY);
         }
+        // eight independent partial maxima (max is exact in any order)
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sv[k]);
+#pragma unroll
+        for (int j = 8; j < HK; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+        mx = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
       }
       // the row's maximum over both halves (warps w and w + 4); the second
       // barrier also orders both halves' reads of S before the writes of P
@@ -505,13 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool live = m_used != -INFINITY;
         const float neg = live ? -m_used : 0.f;
-        float psum = 0.f;
+        float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
 #pragma unroll
         for (int j = 0; j < HK; ++j) {
           const float e = live ? ex2(fmaf(__uint_as_float(sv[j]), sl2, neg)) : 0.f;
-          psum += e;
+          ps8[j & 7] += e;
           sv[j] = __float_as_uint(e);
         }
+        const float psum = ((ps8[0] + ps8[4]) + (ps8[1] + ps8[5])) +
+                           ((ps8[2] + ps8[6]) + (ps8[3] + ps8[7]));
         l_sum = l_sum * alpha + psum;
         // rescale this half of O's row when the reference maximum moved; PV(c-1)
         // must be done with O first (c == 0: the first PV overwrites O)
@@ -533,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lok) {
-        // P into S[st]: hi = bf16(p), lo = bf16(p - hi), pairs packed
+        // P into S[sb]: hi = bf16(p), lo = bf16(p - hi), pairs packed
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t wh[16], wl[16];
@@ -547,8 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
             wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          tmem_st16(tmem + lane_base + st * 128 + 32 * hcol + 16 * q2, wh);
-          tmem_st16(tmem + lane_base + st * 128 + 64 + 32 * hcol + 16 * q2, wl);
+          tmem_st16(tmem + lane_base + sb * 128 + 32 * hcol + 16 * q2, wh);
+          tmem_st16(tmem + lane_base + sb * 128 + 64 + 32 * hcol + 16 * q2, wl);
         }
         tmem_wait_st();
       }
@@ -557,7 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 0 * NaN is not, so those rows are zeroed once the copies have landed.
       const int vk = nk - c * kKeys;  // valid keys in this chunk
       if (lok && vk < kKeys) {
-        lok = mbar_wait_bounded(&v_full[st], (c >> 1) & 1, p.err);
+        const int st = c % kStages;
+        lok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err);
         if (lok && r >= vk) {
           const uint4 z = make_uint4(0, 0, 0, 0);
           uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hcol) * kHalf + prow);
@@ -566,11 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = lok;
-      // hand P, O and the zeroed V rows to the producer: one arrival per warp
+      // hand P, O and the zeroed V rows to the MMA warp: one arrival per warp
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_ready[st]);
+      if (lane == 0) mbar_arrive(&p_ready[sb]);
     }
 
     // Epilogue: O / l, both halves' sums combined through shared memory.  A
