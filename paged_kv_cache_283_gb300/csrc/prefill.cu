@@ -27,7 +27,7 @@
 //    memory), masks causally, keeps a running maximum that is only raised
 //    when it grows by more than 2^8 (then O's row is rescaled in tensor
 //    memory), and writes P back into tensor memory, over its own S, as two
-//    bf16 parts, hi = bf16(p) and lo = bf16(p - hi), each multiplied with V
+//    bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), each multiplied with V
 //    by its own MMA reading A from tensor memory: the weights keep ~17 bits
 //    instead of bf16's 8 (a single bf16 P puts elementwise errors of several
 //    per cent on outputs that are small by cancellation).
@@ -505,17 +505,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const bool live = m_used != -INFINITY;
-        const float neg = live ? -m_used : 0.f;
-        float ps8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // independent partial sums
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 neg2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
+        float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                         make_float2(0.f, 0.f)};  // independent partial sums
 #pragma unroll
-        for (int j = 0; j < HK; ++j) {
-          const float e = live ? ex2(fmaf(__uint_as_float(sv[j]), sl2, neg)) : 0.f;
-          ps8[j & 7] += e;
-          sv[j] = __float_as_uint(e);
+        for (int j = 0; j < HK; j += 2) {
+          const float2 x = __ffma2_rn(
+              make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sl2x2, neg2);
+          const float2 e = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
+          ps4[(j >> 1) & 3] = __fadd2_rn(ps4[(j >> 1) & 3], e);
+          sv[j] = __float_as_uint(e.x);
+          sv[j + 1] = __float_as_uint(e.y);
         }
-        const float psum = ((ps8[0] + ps8[4]) + (ps8[1] + ps8[5])) +
-                           ((ps8[2] + ps8[6]) + (ps8[3] + ps8[7]));
-        l_sum = l_sum * alpha + psum;
+        const float2 pa = __fadd2_rn(__fadd2_rn(ps4[0], ps4[2]), __fadd2_rn(ps4[1], ps4[3]));
+        l_sum = l_sum * alpha + (pa.x + pa.y);
         // rescale this half of O's row when the reference maximum moved; PV(c-1)
         // must be done with O first (c == 0: the first PV overwrites O)
         if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
@@ -536,18 +540,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (lok) {
-        // P into S[sb]: hi = bf16(p), lo = bf16(p - hi), pairs packed
+        // P into S[sb] as hi + lo bf16 parts, pairs packed: hi = p truncated to
+        // bf16 (its upper 16 bits), lo = bf16(p - hi) (p - hi is exact and
+        // below 2^-7 p, so hi + lo keeps p to ~2^-16)
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           uint32_t wh[16], wl[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
-            const float a = __uint_as_float(sv[32 * q2 + 2 * k]);
-            const float e = __uint_as_float(sv[32 * q2 + 2 * k + 1]);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(a, e);
-            const float2 hf = __bfloat1622float2(hi);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(a - hf.x, e - hf.y);
-            wh[k] = *reinterpret_cast<const uint32_t*>(&hi);
+            const uint32_t ua = sv[32 * q2 + 2 * k], ue = sv[32 * q2 + 2 * k + 1];
+            wh[k] = __byte_perm(ua, ue, 0x7632);
+            const float2 r2 = __fadd2_rn(
+                make_float2(__uint_as_float(ua), __uint_as_float(ue)),
+                make_float2(-__uint_as_float(ua & 0xFFFF0000u), -__uint_as_float(ue & 0xFFFF0000u)));
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(r2.x, r2.y);
             wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
           }
           tmem_st16(tmem + lane_base + sb * 128 + 32 * hcol + 16 * q2, wh);
