@@ -18,8 +18,8 @@
 //    cores read.
 //  * S = Q K^T (M = 128 rows, N = 128 keys, K = 128 dims) and O += P V
 //    (M = 128, N = 128 dims, K = 128 keys) are tcgen05.mma kind::f16 (bf16 in,
-//    fp32 accumulate) issued by one thread of the MMA warp, with S and O in tensor memory
-//    (S double-buffered: 384 of 512 columns).  V is the MN-major operand.
+//    fp32 accumulate) issued by one thread of the MMA warp, with S and O in
+//    tensor memory (three S buffers + O: all 512 columns).  V is the MN-major operand.
 //    Shared memory: Q 32 KiB, K and V 3 x 32 KiB each (224 KiB, one CTA per
 //    SM, which also holds all 512 tensor-memory columns).
 //  * The online softmax reads its row of S from tensor memory (two threads per
@@ -58,7 +58,9 @@ constexpr int kBS = 16;                 // tokens per cache block
 constexpr int kChunkBlocks = kKeys / kBS;
 constexpr int kHalf = 128 * 128;        // one 64-column half of a 128-row bf16 tile
 constexpr int kBox = kBS * 128;         // one TMA box of K or V: 16 rows x 128 bytes
-constexpr uint32_t kTmemCols = 512;     // S0: [0, 128), S1: [128, 256), O: [256, 384)
+constexpr uint32_t kTmemCols = 512;     // S0..S2: [0, 384) in 128-column buffers, O: [384, 512)
+constexpr int kSBuf = 3;                // S (then P) buffers in tensor memory
+constexpr uint32_t kTO = 384;           // O's first column
 
 // Shared memory, from a 1024-byte aligned base (the swizzle atom).
 constexpr int kQ = 0;                   // Q: 2 halves
@@ -230,20 +232,21 @@ __device__ __forceinline__ void pair_sync(int warp) {
 // Warp 8 issues the MMAs (lane 0), warp 9 the copies (one block per lane), so
 // that neither chain waits on the other's latencies.
 //
-// Tensor memory: S0 = columns [0, 128), S1 = [128, 256), O = [256, 384).  P of
-// chunk c replaces S of chunk c in place (hi part in the buffer's first 64
-// columns, lo part in the next 64, bf16 pairs packed per column), so P is
-// double-buffered with S.  K and V run in 3-chunk rings; every stage has a
-// "full" barrier (copies landed) and a "free" barrier (committed after the
-// MMA that read it), so each wait names one use of one stage.
+// Tensor memory: S0, S1, S2 = columns [0, 384) in 128-column buffers, O =
+// [384, 512).  P of chunk c replaces S of chunk c in place (hi part in the
+// buffer's first 64 columns, lo part in the next 64, bf16 pairs packed per
+// column); buffer c % 3.  K and V run in 3-chunk rings.  Every ring slot has
+// its own barriers ("full": copies landed; "free": committed after the MMA
+// that read it; "pv_done": PV read the P it holds), so that each wait names
+// one use of one slot and no parity wait can match an older phase.
 //
-// MMA warp, per chunk c:  wait PV(c-1) (S[(c+1)&1] holds P(c-1)) and K(c+1):
-//   S[(c+1)&1] = Q K(c+1)^T; wait V(c) and P(c): O += P V(c).
-// Copy warp, per chunk c: wait K stage of c free: copy K(c+3); wait V stage of
+// MMA warp, per chunk c:  wait PV(c-2) (S[(c+1)%3] holds P(c-2)) and K(c+1):
+//   S[(c+1)%3] = Q K(c+1)^T; wait V(c) and P(c): O += P V(c).
+// Copy warp, per chunk c: wait K slot of c free: copy K(c+3); wait V slot of
 //   c-1 free: copy V(c+2).
 // Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
 //   exponentials; rescale O only if the reference maximum moved (after
-//   PV(c-1)); P into S[c&1]; arrive on p_ready[c&1].
+//   PV(c-1)); P into S[c%3]; arrive on p_ready[c%3].
 // No softmax thread leaves the loop early (the pair barriers must stay
 // matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
@@ -280,20 +283,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = k_full + 3;                               // [3]
   uint64_t* k_free = k_full + 6;                               // [3] QK that read it done
   uint64_t* v_free = k_full + 9;                               // [3] PV that read it done
-  uint64_t* s_done = k_full + 12;                              // [2] per S buffer
-  uint64_t* o_done = k_full + 14;
-  uint64_t* q_full = k_full + 15;
-  // [2] per S buffer, 8 warp arrivals per chunk.  One barrier per buffer: a
-  // softmax warp can finish chunk c + 1 (its scores come before PV(c)) while
-  // another is still on chunk c, and its arrival must not count for c.
-  uint64_t* p_ready = k_full + 16;
+  uint64_t* s_done = k_full + 12;                              // [3] per S buffer
+  // [3] per S buffer: PV of the chunk whose P the buffer holds is done.  Its
+  // commit covers every MMA issued before, so "PV(c) done" also means every
+  // earlier PV is done; the next phase of the same barrier (PV(c + 3)) cannot
+  // complete before the waiter's own arrival for c + 3, so no parity wait on
+  // it can match a stale or a future phase.
+  uint64_t* pv_done = k_full + 15;
+  uint64_t* q_full = k_full + 18;
+  // [3] per S buffer, 8 warp arrivals per chunk.  One barrier per buffer: a
+  // softmax warp can be up to two chunks ahead of another (the scores of c + 2
+  // need only PV(c - 1)), and its arrivals must not count for an earlier chunk.
+  uint64_t* p_ready = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
   float* red = reinterpret_cast<float*>(sm + kRed);            // [2][128]
 
   if (tid == 0) {
-    for (int i = 0; i < 16; ++i) mbar_init(k_full + i, 1);
-    mbar_init(&p_ready[0], kSoftmaxThreads / 32);
-    mbar_init(&p_ready[1], kSoftmaxThreads / 32);
+    for (int i = 0; i < 19; ++i) mbar_init(k_full + i, 1);
+    for (int i = 0; i < kSBuf; ++i) mbar_init(&p_ready[i], kSoftmaxThreads / 32);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -392,15 +399,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sQ = smem_u32(sm + kQ), sK = smem_u32(sm + kK), sV = smem_u32(sm + kV);
     int s_iss = 0, o_iss = 0;  // MMAs committed (for the drain)
     if (lane == 0) {
-      // lane 0: S[c & 1] = Q K(c)^T
+      // lane 0: S[c % 3] = Q K(c)^T
+      const uint64_t qdesc = sw128_desc(sQ, 16, 1024);
       auto qk = [&](int c) {
-        const int sb = c & 1, st = c % kStages;
+        const int sb = c % kSBuf, st = c % kStages;
+        const uint64_t kdesc = sw128_desc(sK + 2 * st * kHalf, 16, 1024);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kHalf + (kk & 3) * 32;
-          umma_bf16(tmem + sb * 128, sw128_desc(sQ + off, 16, 1024),
-                    sw128_desc(sK + 2 * st * kHalf + off, 16, 1024), kIdescQK, kk > 0);
+          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;  // descriptor units
+          umma_bf16(tmem + sb * 128, qdesc + off, kdesc + off, kIdescQK, kk > 0);
         }
         umma_commit(&s_done[sb]);
         umma_commit(&k_free[st]);
@@ -409,40 +417,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
       if (ok) qk(0);
       for (int c = 0; c < nchunks && ok; ++c) {
-        const int sb = c & 1, st = c % kStages;
+        const int sb = c % kSBuf, st = c % kStages;
         if (c + 1 < nchunks) {
-          // PV(c-1) is done with P(c-1) in S[(c+1)&1]
-          if (c > 0) ok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+          // PV(c-2) is done with P(c-2) in S[(c+1)%3]
+          if (c >= 2)
+            ok = mbar_wait_bounded(&pv_done[(c + 1) % kSBuf], ((c - 2) / kSBuf) & 1, p.err);
           ok = ok && mbar_wait_bounded(&k_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, p.err);
           if (!ok) break;
           qk(c + 1);
         }
         ok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err) &&
-             mbar_wait_bounded(&p_ready[sb], (c >> 1) & 1, p.err);
+             mbar_wait_bounded(&p_ready[sb], (c / kSBuf) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
+        const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf, kHalf, 1024);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf + kk * 2048, kHalf, 1024);
-          umma_bf16_ts(tmem + 256, tmem + sb * 128 + 8 * kk, vdesc, kIdescPV,
+          umma_bf16_ts(tmem + kTO, tmem + sb * 128 + 8 * kk, vdesc + kk * (2048 >> 4), kIdescPV,
                        (c > 0 || kk > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + 256, tmem + sb * 128 + 64 + 8 * kk, vdesc, kIdescPV, 1u);
+          umma_bf16_ts(tmem + kTO, tmem + sb * 128 + 64 + 8 * kk, vdesc + kk * (2048 >> 4),
+                       kIdescPV, 1u);
         }
-        umma_commit(o_done);
+        umma_commit(&pv_done[sb]);
         umma_commit(&v_free[st]);
         ++o_iss;
       }
       // The MMAs issued complete before tensor and shared memory are given up
       // (each commit covers every MMA before it).
-      if (o_iss > 0) mbar_wait_bounded(o_done, (o_iss - 1) & 1, p.err);
-      if (s_iss > 0) mbar_wait_bounded(&s_done[(s_iss - 1) & 1], ((s_iss - 1) >> 1) & 1, p.err);
+      if (o_iss > 0)
+        mbar_wait_bounded(&pv_done[(o_iss - 1) % kSBuf], ((o_iss - 1) / kSBuf) & 1, p.err);
+      if (s_iss > 0)
+        mbar_wait_bounded(&s_done[(s_iss - 1) % kSBuf], ((s_iss - 1) / kSBuf) & 1, p.err);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax
     const int hcol = tid >> 7;  // column half
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_base + 256 + 64 * hcol;
+    const uint32_t tO = tmem + lane_base + kTO + 64 * hcol;
     const int r = tid & (kRows - 1);  // row: token r / G of the tile, head r % G
     const int qi = i0 + r / G;
     const bool row_ok = qi < n;
@@ -454,8 +466,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int prow = (r >> 3) * 1024 + (r & 7) * 128;  // row in a swizzled 128-row tile
 
     for (int c = 0; c < nchunks; ++c) {
-      const int sb = c & 1;
-      bool lok = ok && mbar_wait_bounded(&s_done[sb], (c >> 1) & 1, p.err);
+      const int sb = c % kSBuf;
+      bool lok = ok && mbar_wait_bounded(&s_done[sb], (c / kSBuf) & 1, p.err);
       lok = __all_sync(kFullMask, lok);
       uint32_t sv[HK];
       if (lok) {
@@ -521,9 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 pa = __fadd2_rn(__fadd2_rn(ps4[0], ps4[2]), __fadd2_rn(ps4[1], ps4[3]));
         l_sum = l_sum * alpha + (pa.x + pa.y);
         // rescale this half of O's row when the reference maximum moved; PV(c-1)
-        // must be done with O first (c == 0: the first PV overwrites O)
+        // (and so every earlier PV) must be done with O first (c == 0: the
+        // first PV overwrites O)
         if (c > 0 && __any_sync(kFullMask, alpha != 1.f)) {
-          lok = mbar_wait_bounded(o_done, (c - 1) & 1, p.err);
+          lok = mbar_wait_bounded(&pv_done[(c - 1) % kSBuf], ((c - 1) / kSBuf) & 1, p.err);
           lok = __all_sync(kFullMask, lok);
           if (lok) {
             tc_fence_after();
@@ -583,14 +596,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&p_ready[sb]);
     }
 
-    // Epilogue: O / l, both halves' sums combined through shared memory.  A
-    // softmax warp can finish the last chunk before PV of the one before it
-    // completes; o_done then still owes two phases, and a parity wait for the
-    // last one alone would match the phase before those and return early.
-    // So the two are waited for in order.
-    bool lok = ok;
-    if (nchunks >= 2) lok = lok && mbar_wait_bounded(o_done, (nchunks - 2) & 1, p.err);
-    lok = lok && mbar_wait_bounded(o_done, (nchunks - 1) & 1, p.err);
+    // Epilogue: O / l, both halves' sums combined through shared memory, once
+    // the last PV (and so every PV) is done.
+    bool lok = ok && mbar_wait_bounded(&pv_done[(nchunks - 1) % kSBuf],
+                                       ((nchunks - 1) / kSBuf) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
     red[hcol * kRows + r] = l_sum;
     asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
