@@ -30,6 +30,8 @@ Modules:
                  cache (chunked prefill; one token = one decode step).
 * ``scheduler``  the chunked-prefill step budget (decodes first, then
                  prefill chunks in queue order).
+* ``fp8``        the FP8 (E4M3) KV scheme: the format from its definition,
+                 per-row quantisation, the FP8 cache write and decode.
 * ``quant``      the INT8 KV scheme: per-row quantisation, the INT8 cache
                  write and the INT8 decode.
 * ``cache``      the cache write (scatter of new K/V through a slot mapping).
