@@ -43,12 +43,16 @@ NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context only
 # ---------------------------------------------------------------------------
 # algorithmic bytes (what one step must move at least once)
 
+# entry-point name suffix per KV cache element type
+KV_SUFFIX = {"bf16": "", "int8": "_int8", "fp8": "_fp8"}
+
+
 def decode_bytes(ctx, num_seqs, hq, hkv, d, bs, kv_dtype="bf16"):
     """K/V of every attended token + q + out + block-table entries + lengths
     (an INT8 cache stores d codes and one fp32 scale per token and KV head)."""
     import numpy as np
     ctx = np.asarray(ctx, dtype=np.int64)
-    per = (d + 4) if kv_dtype == "int8" else 2 * d
+    per = (d + 4) if kv_dtype in ("int8", "fp8") else 2 * d
     kv = int(ctx.sum()) * hkv * per * 2
     qo = 2 * num_seqs * hq * d * 2
     tables = 4 * int((-(-ctx // bs)).sum()) + 4 * num_seqs
@@ -57,7 +61,7 @@ def decode_bytes(ctx, num_seqs, hq, hkv, d, bs, kv_dtype="bf16"):
 
 def cache_write_bytes(num_tokens, hkv, d, kv_dtype="bf16"):
     """Read the new tokens' K and V, write them into the pool, read the slots."""
-    written = (d + 4) if kv_dtype == "int8" else 2 * d
+    written = (d + 4) if kv_dtype in ("int8", "fp8") else 2 * d
     return 2 * num_tokens * hkv * (2 * d + written) + 8 * num_tokens
 
 
@@ -168,6 +172,16 @@ def oracle_step_sample(idx, max_seconds, out_json=True, kv="bf16"):
                                       slots[:nseq], w.block_size, inplace=True)
             OQ.decode_int8(w.q[:nseq], kc8, vc8, ks8, vs8, tables[:nseq],
                            w.context_lens[:nseq], w.scale, w.block_size)
+    elif kv == "fp8":
+        from oracle import fp8 as OF
+        kc8, ks8 = OF.quantize_fp8(w.k_cache)
+        vc8, vs8 = OF.quantize_fp8(w.v_cache)
+
+        def run(nseq):  # noqa: F811
+            OF.reshape_and_cache_fp8(w.key[:nseq], w.value[:nseq], kc8, vc8, ks8, vs8,
+                                     slots[:nseq], w.block_size, inplace=True)
+            OF.decode_fp8(w.q[:nseq], kc8, vc8, ks8, vs8, tables[:nseq],
+                          w.context_lens[:nseq], w.scale, w.block_size)
 
     nseq = 1
     while True:
@@ -354,21 +368,30 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
         k0, v0 = bf(w.k_cache), bf(w.v_cache)
         replicas = [[(k0, v0)]] + [[(k0.clone(), v0.clone())] for _ in range(nrep - 1)]
         qs, keys, vals = [bf(w.q)], [bf(w.key)], [bf(w.value)]
-    if kv_dtype == "int8":
-        # synthetic INT8 pools of the same shape: codes uniform in [-127, 127],
-        # scales as N(0, 1) rows give (about 3.5 / 127)
+    if kv_dtype in ("int8", "fp8"):
+        # synthetic 1-byte pools of the same shape: INT8 codes uniform in
+        # [-127, 127], scales as N(0, 1) rows give (about 3.5 / 127); FP8 codes
+        # uniform over the finite E4M3 codes (never 0x7F / 0xFF), scales about
+        # 3.5 / 448
         gen = torch.Generator(device=device)
         gen.manual_seed(283 + idx)
+
+        def codes(shape):
+            if kv_dtype == "int8":
+                return torch.randint(-127, 128, shape, generator=gen, device=device,
+                                     dtype=torch.int8)
+            mag = torch.randint(0, 0x7F, shape, generator=gen, device=device, dtype=torch.int32)
+            sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32)
+            return (mag | (sign << 7)).to(torch.uint8)
+
+        lo = 0.02 if kv_dtype == "int8" else 0.006
 
         def int8_pool():
             nb = w.num_blocks
             shape = (nb, w.num_kv_heads, w.block_size, w.head_dim)
-            return (torch.randint(-127, 128, shape, generator=gen, device=device,
-                                  dtype=torch.int8),
-                    torch.randint(-127, 128, shape, generator=gen, device=device,
-                                  dtype=torch.int8),
-                    torch.rand(shape[:3], generator=gen, device=device) * 0.01 + 0.02,
-                    torch.rand(shape[:3], generator=gen, device=device) * 0.01 + 0.02)
+            return (codes(shape), codes(shape),
+                    torch.rand(shape[:3], generator=gen, device=device) * lo / 2 + lo,
+                    torch.rand(shape[:3], generator=gen, device=device) * lo / 2 + lo)
         pool_bytes = 2 * w.num_blocks * w.num_kv_heads * w.block_size * (w.head_dim + 4)
         if layers > 1:
             replicas = [[int8_pool() for _ in range(layers)]]
@@ -396,21 +419,17 @@ def _attn_fns(st, attn, partition):
         ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
                                  int(w.context_lens.max()), partition, st["q"][0].device)
 
-    i8 = st.get("kv") == "int8"
+    sfx = KV_SUFFIX[st.get("kv", "bf16")]
+    f_split = getattr(pa, "pa_decode_splitk" + sfx)
+    f_whole = getattr(pa, "pa_decode" + sfx)
+    f_write = getattr(pa, "pa_reshape_and_cache" + sfx)
 
     def dominant(layer, *pool):
         q = st["q"][layer]
         if attn == "splitk":
-            if i8:
-                pa.pa_decode_splitk_int8(*ws, q, *pool, st["bt"], st["ctx"], w.scale,
-                                         partition_size=partition)
-            else:
-                pa.pa_decode_splitk(*ws, q, *pool, st["bt"], st["ctx"], w.scale,
-                                    partition_size=partition)
-        elif i8:
-            pa.pa_decode_int8(outs[layer], q, *pool, st["bt"], st["ctx"], w.scale)
+            f_split(*ws, q, *pool, st["bt"], st["ctx"], w.scale, partition_size=partition)
         else:
-            pa.pa_decode(outs[layer], q, *pool, st["bt"], st["ctx"], w.scale)
+            f_whole(outs[layer], q, *pool, st["bt"], st["ctx"], w.scale)
 
     def attend(layer, *pool):
         dominant(layer, *pool)
@@ -419,11 +438,7 @@ def _attn_fns(st, attn, partition):
 
     def step(r):
         for layer, pool in enumerate(st["replicas"][r]):
-            if i8:
-                pa.pa_reshape_and_cache_int8(st["key"][layer], st["value"][layer], *pool,
-                                             st["slots"])
-            else:
-                pa.pa_reshape_and_cache(st["key"][layer], st["value"][layer], *pool, st["slots"])
+            f_write(st["key"][layer], st["value"][layer], *pool, st["slots"])
             attend(layer, *pool)
 
     return step, dominant, outs
@@ -572,9 +587,9 @@ def run_gpu(args):
                 "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(
                     ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
-                    + ("_int8" if args.kv == "int8" else ""), w.name, args.partition),
+                    + KV_SUFFIX[args.kv], w.name, args.partition),
                 "kernel": ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
-                + ("_int8" if args.kv == "int8" else ""),
+                + KV_SUFFIX[args.kv],
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
                 else "fallback 6.8 TB/s",
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_dt * 1e6, 2)}
@@ -589,8 +604,8 @@ def run_gpu(args):
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(np.mean(w.context_lens)), "new_tokens_per_step": w.num_seqs,
             "attention": ("pa_decode_splitk%s+pa_splitk_reduce, partition %d"
-                          % ("_int8" if args.kv == "int8" else "", args.partition))
-            if attn == "splitk" else ("pa_decode_int8" if args.kv == "int8" else "pa_decode"),
+                          % (KV_SUFFIX[args.kv], args.partition))
+            if attn == "splitk" else "pa_decode" + KV_SUFFIX[args.kv],
             "kv_cache": args.kv,
             "graph": "one CUDA graph per step (cache write + attention)",
             "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
@@ -948,8 +963,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4, 5])
-    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8"],
-                    help="KV cache element type (int8: one fp32 scale per token and head)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "int8", "fp8"],
+                    help="KV cache element type (int8 / fp8 E4M3: one fp32 scale per token "
+                         "and head)")
     ap.add_argument("--op", default="step", choices=["step", "copy_blocks", "prefill"],
                     help="copy_blocks: time pa_copy_blocks on a parallel-sampling step; "
                          "prefill: time pa_prefill on a 16 x 512-token chunked-prefill step")

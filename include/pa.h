@@ -10,7 +10,7 @@
  *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
  *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
- *   *_int8                 the cache write and decode over an INT8 KV cache
+ *   *_int8, *_fp8          the cache write and decode over an INT8 / FP8 KV cache
  *   pa_prefill             causal attention of chunks of new tokens (prefill)
  *   pa_alloc_*             fixed-size block allocator with reference counts,
  *                          copy-on-write and automatic prefix caching (host
@@ -216,6 +216,44 @@ pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l,
                                 int num_q_heads, int num_kv_heads, int head_dim,
                                 int block_size, int num_blocks, float scale,
                                 int partition_size, pa_stream_t stream);
+
+/*
+ * FP8 KV cache (the other 1-byte format of "Visual walkthrough", Step 1).  The
+ * pages give no scheme; here E4M3 as NVIDIA's FP8 "e4m3" (bias 7, 3 mantissa
+ * bits, no infinities, 0x7F / 0xFF NaN, largest finite 448), one fp32 scale per
+ * (token, KV head) row:
+ *   scale = max|x| / 448,  code = E4M3(x / scale) round to nearest even,
+ *   saturated to +-448 (fp32 arithmetic; scale 0 and codes 0 for an all-zero row).
+ * Pools, scales, the V tile's unit permutation and sizes exactly as the INT8
+ * cache, with uint8 codes.  Decode keeps q unquantised: scores are
+ * scale * q . (decode(k_code) * k_scale) in fp32 (the codes are exact in fp32);
+ * PV as the INT8 decode (weights times v_scale, tf32 hi + lo on the tensor
+ * cores, exact codes).  A token past the context is masked by position; its
+ * codes may be NaN and are never multiplied.  head_dim 64 or 128.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value,
+                                   uint8_t* k_cache, uint8_t* v_cache,
+                                   float* k_scales, float* v_scales,
+                                   const int64_t* slot_mapping, int num_tokens,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, pa_stream_t stream);
+pa_status pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache,
+                        const uint8_t* v_cache, const float* k_scales,
+                        const float* v_scales, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens,
+                        int num_seqs, int num_q_heads, int num_kv_heads,
+                        int head_dim, int block_size, int num_blocks, float scale,
+                        pa_stream_t stream);
+/* Split-K partition pass over an FP8 cache; merge with pa_splitk_reduce. */
+pa_status pa_decode_splitk_fp8(float* ws_out, float* ws_m, float* ws_l,
+                               int max_partitions, const void* q,
+                               const uint8_t* k_cache, const uint8_t* v_cache,
+                               const float* k_scales, const float* v_scales,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs,
+                               int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, float scale,
+                               int partition_size, pa_stream_t stream);
 
 /* Bytes of fp32 workspace pa_decode_splitk needs for contexts up to
  * max_context_len: ws_out [B, Hq, P, D] + ws_m [B, Hq, P] + ws_l [B, Hq, P]

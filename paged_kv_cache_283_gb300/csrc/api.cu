@@ -154,11 +154,14 @@ pa_status pa_copy_blocks(void* const* k_caches, void* const* v_caches, int num_l
   return PA_OK;
 }
 
-pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* k_cache,
-                                    int8_t* v_cache, float* k_scales, float* v_scales,
-                                    const int64_t* slot_mapping, int num_tokens,
-                                    int num_kv_heads, int head_dim, int block_size,
-                                    int num_blocks, pa_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+pa_status cache_write_1byte(const void* key, const void* value, void* k_cache, void* v_cache,
+                            float* k_scales, float* v_scales, const int64_t* slot_mapping,
+                            int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int fp8, pa_stream_t stream) {
   if (num_tokens < 0 || num_kv_heads <= 0 || block_size <= 0 || num_blocks <= 0)
     return PA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED_SHAPE;
@@ -169,10 +172,11 @@ pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* 
   CacheWriteParams p{};
   p.key = static_cast<const __nv_bfloat16*>(key);
   p.value = static_cast<const __nv_bfloat16*>(value);
-  p.k8 = k_cache;
-  p.v8 = v_cache;
+  p.k8 = static_cast<int8_t*>(k_cache);
+  p.v8 = static_cast<int8_t*>(v_cache);
   p.k_scales = k_scales;
   p.v_scales = v_scales;
+  p.fp8 = fp8;
   p.slot_mapping = slot_mapping;
   p.err = device_error_word();
   if (!p.err) return cuda_fail(cudaGetLastError());
@@ -184,6 +188,29 @@ pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* 
   cudaError_t e = launch_reshape_and_cache_int8(p, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_reshape_and_cache_int8(const void* key, const void* value, int8_t* k_cache,
+                                    int8_t* v_cache, float* k_scales, float* v_scales,
+                                    const int64_t* slot_mapping, int num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int num_blocks, pa_stream_t stream) {
+  return cache_write_1byte(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                           num_tokens, num_kv_heads, head_dim, block_size, num_blocks, 0, stream);
+}
+
+pa_status pa_reshape_and_cache_fp8(const void* key, const void* value, uint8_t* k_cache,
+                                   uint8_t* v_cache, float* k_scales, float* v_scales,
+                                   const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                   int head_dim, int block_size, int num_blocks,
+                                   pa_stream_t stream) {
+  return cache_write_1byte(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                           num_tokens, num_kv_heads, head_dim, block_size, num_blocks, 1, stream);
+}
+
 
 namespace {
 
@@ -321,14 +348,13 @@ pa_status pa_splitk_reduce(void* out, const float* ws_out, const float* ws_m, co
 
 }  // extern "C"
 
-extern "C" {
+namespace {
 
-pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
-                         const float* k_scales, const float* v_scales,
-                         const int32_t* block_tables, int max_blocks_per_seq,
-                         const int32_t* context_lens, int num_seqs, int num_q_heads,
-                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                         float scale, pa_stream_t stream) {
+pa_status decode_1byte(void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                       int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int num_blocks, float scale, int fp8, pa_stream_t stream) {
   pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, scale);
@@ -338,10 +364,11 @@ pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache, const 
   DecodeParams p = make_decode_params(q, nullptr, nullptr, block_tables, max_blocks_per_seq,
                                       context_lens, num_seqs, num_q_heads, num_kv_heads,
                                       num_blocks, scale);
-  p.k8 = k_cache;
-  p.v8 = v_cache;
+  p.k8 = static_cast<const int8_t*>(k_cache);
+  p.v8 = static_cast<const int8_t*>(v_cache);
   p.k_scales = k_scales;
   p.v_scales = v_scales;
+  p.fp8 = fp8;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.max_partitions = 1;
   p.partition_blocks = max_blocks_per_seq;
@@ -352,13 +379,13 @@ pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache, const 
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
 }
 
-pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l, int max_partitions,
-                                const void* q, const int8_t* k_cache, const int8_t* v_cache,
-                                const float* k_scales, const float* v_scales,
-                                const int32_t* block_tables, int max_blocks_per_seq,
-                                const int32_t* context_lens, int num_seqs, int num_q_heads,
-                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                                float scale, int partition_size, pa_stream_t stream) {
+pa_status decode_splitk_1byte(float* ws_out, float* ws_m, float* ws_l, int max_partitions,
+                              const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scales, const float* v_scales,
+                              const int32_t* block_tables, int max_blocks_per_seq,
+                              const int32_t* context_lens, int num_seqs, int num_q_heads,
+                              int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                              float scale, int partition_size, int fp8, pa_stream_t stream) {
   pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, scale);
@@ -373,10 +400,11 @@ pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l, int max
   DecodeParams p = make_decode_params(q, nullptr, nullptr, block_tables, max_blocks_per_seq,
                                       context_lens, num_seqs, num_q_heads, num_kv_heads,
                                       num_blocks, scale);
-  p.k8 = k_cache;
-  p.v8 = v_cache;
+  p.k8 = static_cast<const int8_t*>(k_cache);
+  p.v8 = static_cast<const int8_t*>(v_cache);
   p.k_scales = k_scales;
   p.v_scales = v_scales;
+  p.fp8 = fp8;
   p.ws_o = ws_out;
   p.ws_m = ws_m;
   p.ws_l = ws_l;
@@ -387,6 +415,57 @@ pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l, int max
   cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true,
                                 reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_int8(void* out, const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                         const float* k_scales, const float* v_scales,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, pa_stream_t stream) {
+  return decode_1byte(out, q, k_cache, v_cache, k_scales, v_scales, block_tables,
+                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, 0, stream);
+}
+
+pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l, int max_partitions,
+                                const void* q, const int8_t* k_cache, const int8_t* v_cache,
+                                const float* k_scales, const float* v_scales,
+                                const int32_t* block_tables, int max_blocks_per_seq,
+                                const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                float scale, int partition_size, pa_stream_t stream) {
+  return decode_splitk_1byte(ws_out, ws_m, ws_l, max_partitions, q, k_cache, v_cache, k_scales,
+                             v_scales, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             partition_size, 0, stream);
+}
+
+pa_status pa_decode_fp8(void* out, const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                        const float* k_scales, const float* v_scales, const int32_t* block_tables,
+                        int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int num_blocks, float scale, pa_stream_t stream) {
+  return decode_1byte(out, q, k_cache, v_cache, k_scales, v_scales, block_tables,
+                      max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, 1, stream);
+}
+
+pa_status pa_decode_splitk_fp8(float* ws_out, float* ws_m, float* ws_l, int max_partitions,
+                               const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                               const float* k_scales, const float* v_scales,
+                               const int32_t* block_tables, int max_blocks_per_seq,
+                               const int32_t* context_lens, int num_seqs, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                               float scale, int partition_size, pa_stream_t stream) {
+  return decode_splitk_1byte(ws_out, ws_m, ws_l, max_partitions, q, k_cache, v_cache, k_scales,
+                             v_scales, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                             partition_size, 1, stream);
 }
 
 }  // extern "C"

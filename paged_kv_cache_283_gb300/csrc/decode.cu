@@ -82,10 +82,10 @@ struct Pipe<128, SPLIT, I8> {
 // kernel needs fewer registers and more warps to hide its latencies: four
 // 4-warp CTAs (two 8-warp ones) per SM, <= 128 registers, each warp with 3
 // stages of 4.2 KiB in flight (head_dim 128).
-template <int NW, int G, bool I8>
+template <int NW, int G, int Q>
 constexpr int min_blocks() {
-  if constexpr (I8) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
-  else return (NW <= 4 && G <= 4) ? 3 : 1;
+  if constexpr (Q == 1) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
+  else return (NW <= 4 && G <= 4) ? 3 : 1;  // bf16; FP8 keeps the bf16 QK registers
 }
 
 template <int D, int G, int NW, int S, bool I8>
@@ -107,9 +107,14 @@ struct SmemLayout {
   static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
   static_assert(STAGE % 16 == 0 && KT % 16 == 0, "bulk copy sizes");
 };
-template <int D, int G, int NW, int S, bool SPLIT, bool I8>
-__global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, I8>()))
+// Q: the cache's element type: 0 = bf16, 1 = INT8, 2 = FP8 (E4M3).  INT8 and
+// FP8 share the 1-byte-code tile layout (codes + per-token scales) and the
+// tensor-core PV; INT8 alone quantises q and takes QK in integers.
+template <int D, int G, int NW, int S, bool SPLIT, int Q>
+__global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     paged_decode_kernel(const DecodeParams p) {
+  constexpr bool I8 = Q != 0;   // 1-byte codes + scales
+  constexpr bool QI = Q == 1;   // INT8 QK
   using Geo = Geometry<D, G>;
   using Lay = SmemLayout<D, G, NW, S, I8>;
   constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, I8>()))
   float2 q2[G][4];
   int qc[G][IG::QW];  // int8 cache: this lane's q codes, 4 per word
   float qsc[G];       // int8 cache: q scale times scale * log2(e)
-  if constexpr (!I8) {
+  if constexpr (!QI) {
     const __nv_bfloat16* qb =
         p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
     uint4 qw[G];
@@ -300,12 +305,12 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, I8>()))
   float l_run = 0.f;        // this lane's share of that head's exp-sum
   // The lane geometry of the scores and softmax state: the bf16 step's, or
   // the int8 QK geometry.
-  constexpr int SL = I8 ? IG::QL : L;
-  constexpr int SHL = I8 ? IG::HEAD_LANES : Geo::HEAD_LANES;
-  const int ssub = I8 ? qsub : sub;
-  const int srg = I8 ? qrg : rg;
-  const int my_head = I8 ? (qsub * IG::R) / IG::P : (sub * R) / P;
-  const int my_i0 = I8 ? (qsub * IG::R) % IG::P : (sub * R) % P;
+  constexpr int SL = QI ? IG::QL : L;
+  constexpr int SHL = QI ? IG::HEAD_LANES : Geo::HEAD_LANES;
+  const int ssub = QI ? qsub : sub;
+  const int srg = QI ? qrg : rg;
+  const int my_head = QI ? (qsub * IG::R) / IG::P : (sub * R) / P;
+  const int my_i0 = QI ? (qsub * IG::R) % IG::P : (sub * R) % P;
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i);
@@ -330,12 +335,21 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, I8>()))
     } else {
       const float* ksc = reinterpret_cast<const float*>(stage + 2 * Lay::KT);
       const float* vsc = ksc + BS;
-      if (nvalid == BS)
-        tile_step_i8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                 m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
-      else
-        tile_step_i8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                  m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
+      if constexpr (QI) {
+        if (nvalid == BS)
+          tile_step_i8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
+                                   m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
+        else
+          tile_step_i8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
+                                    m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
+      } else {
+        if (nvalid == BS)
+          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, q2, acc8, m_run,
+                                   l_run, nvalid, lane, sub, rg, my_head, my_i0);
+        else
+          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, q2, acc8, m_run,
+                                    l_run, nvalid, lane, sub, rg, my_head, my_i0);
+      }
     }
     consumed = i + 1;
     __syncwarp();  // every lane is done with this stage and with ps / alpha_s
@@ -459,33 +473,34 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
   return e;
 }
 
-template <int D, int G, bool SPLIT, bool I8>
+template <int D, int G, bool SPLIT, int Q>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
+  constexpr bool I8 = Q != 0;
   constexpr int NW = Pipe<D, SPLIT, I8>::NW, S = Pipe<D, SPLIT, I8>::S;
   using Lay = SmemLayout<D, G, NW, S, I8>;
   static std::atomic<uint64_t> smem_set{0};
-  auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, I8>;
+  auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, Q>;
   cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
   if (e != cudaSuccess) return e;
   const dim3 grid(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
   return launch_pdl(kernel, grid, dim3(NW * 32), Lay::TOTAL, stream, p);
 }
 
-template <int D, int G, bool I8>
+template <int D, int G, int Q>
 cudaError_t launch_decode_g(const DecodeParams& p, bool split, cudaStream_t stream) {
-  return split ? launch_decode_t<D, G, true, I8>(p, stream)
-               : launch_decode_t<D, G, false, I8>(p, stream);
+  return split ? launch_decode_t<D, G, true, Q>(p, stream)
+               : launch_decode_t<D, G, false, Q>(p, stream);
 }
 
-template <int D, bool I8>
+template <int D, int Q>
 cudaError_t launch_decode_d(const DecodeParams& p, int group, bool split, cudaStream_t stream) {
   switch (group) {
     case 2:
-      return launch_decode_g<D, 2, I8>(p, split, stream);
+      return launch_decode_g<D, 2, Q>(p, split, stream);
     case 4:
-      return launch_decode_g<D, 4, I8>(p, split, stream);
+      return launch_decode_g<D, 4, Q>(p, split, stream);
     case 8:
-      return launch_decode_g<D, 8, I8>(p, split, stream);
+      return launch_decode_g<D, 8, Q>(p, split, stream);
     default:
       return cudaErrorInvalidValue;
   }
@@ -500,13 +515,15 @@ bool decode_shape_supported(int head_dim, int group, int block_size) {
 
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool split,
                           cudaStream_t stream) {
-  const bool i8 = p.k8 != nullptr;
+  const int q = p.k8 == nullptr ? 0 : (p.fp8 ? 2 : 1);
   if (head_dim == 128)
-    return i8 ? launch_decode_d<128, true>(p, group, split, stream)
-              : launch_decode_d<128, false>(p, group, split, stream);
+    return q == 0 ? launch_decode_d<128, 0>(p, group, split, stream)
+                  : q == 1 ? launch_decode_d<128, 1>(p, group, split, stream)
+                           : launch_decode_d<128, 2>(p, group, split, stream);
   if (head_dim == 64)
-    return i8 ? launch_decode_d<64, true>(p, group, split, stream)
-              : launch_decode_d<64, false>(p, group, split, stream);
+    return q == 0 ? launch_decode_d<64, 0>(p, group, split, stream)
+                  : q == 1 ? launch_decode_d<64, 1>(p, group, split, stream)
+                           : launch_decode_d<64, 2>(p, group, split, stream);
   return cudaErrorInvalidValue;
 }
 

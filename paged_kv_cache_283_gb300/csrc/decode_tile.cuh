@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -161,7 +163,7 @@ namespace pa {
 // registers, so a pass covers 32/QL rows and the butterfly that completes the
 // partial dots has only log2(QL) levels (QL = 4: 2 levels; the bf16 step
 // needs 4).  The K and q scales are applied once per score.  PV runs on the
-// tensor cores (pv_i8_mma) with the V scale folded into each softmax weight.
+// tensor cores (pv_q_mma) with the V scale folded into each softmax weight.
 template <int D, int G>
 struct I8Geometry {
   static constexpr int BS = kBlockSize;
@@ -236,10 +238,10 @@ __device__ __forceinline__ void int8x4_to_tf32(uint32_t w, uint32_t (&f)[4]) {
   f[3] = __float_as_uint(hi.y);
 }
 
-// PV of one INT8 tile on the tensor cores: out^T[dim][head] += V^T[dim][token]
+// PV of one INT8 or FP8 tile on the tensor cores: out^T[dim][head] += V^T[dim][token]
 // · W[token][head] with m16n8k8 tf32 MMAs (M = 16 dims, N = 8 heads, the
-// group padded with zeros, K = 8 tokens), two K steps per tile.  V codes are
-// small integers, exact in tf32; each weight W (softmax weight times the
+// group padded with zeros, K = 8 tokens), two K steps per tile.  V codes
+// (small integers, or E4M3 values) are exact in tf32; each weight W (softmax weight times the
 // token's V scale) is split into two tf32 parts, hi + lo, one MMA each, so
 // the products keep ~21 bits.  Lane (gid = lane / 4, tig = lane % 4) owns, in
 // MMA c, dims d0 = (D/8)·gid + 2c (row gid) and d0 + 1 (row gid + 8), and
@@ -257,10 +259,33 @@ __device__ __forceinline__ const unsigned char* v_i8_row_run(const unsigned char
   return vt + ((line << 3) + ((unit & 7) ^ ((2 * line) & 7))) * 16 + ((RUN * gid) & 15);
 }
 
-template <int D, int G>
-__device__ __forceinline__ void pv_i8_mma(const unsigned char* __restrict__ vt,
-                                          const float* __restrict__ ps, float (&acc)[D / 16][4],
-                                          int lane) {
+// 2 E4M3 codes (16 bits, first code in the low byte) to floats, exact (every
+// E4M3 value is exact in f16 and f32).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t h) {
+  const __half2_raw r =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
+  __half2 v;
+  v = *reinterpret_cast<const __half2*>(&r);
+  return __half22float2(v);
+}
+
+// 4 E4M3 codes (one word) to float bit patterns for the tf32 MMA (exact: 3
+// mantissa bits fit tf32's 10).
+__device__ __forceinline__ void e4m3x4_to_tf32(uint32_t w, uint32_t (&f)[4]) {
+  const float2 lo = e4m3x2_to_float2(w), hi = e4m3x2_to_float2(w >> 16);
+  f[0] = __float_as_uint(lo.x);
+  f[1] = __float_as_uint(lo.y);
+  f[2] = __float_as_uint(hi.x);
+  f[3] = __float_as_uint(hi.y);
+}
+
+// F8 = false: INT8 codes; true: E4M3 codes.  With E4M3 a code can be NaN, and
+// a token past the context (nvalid) has weight 0 but whatever codes the pool
+// holds there, so its codes are replaced by 0 (0 * NaN would not be 0).
+template <int D, int G, bool F8, bool FULL>
+__device__ __forceinline__ void pv_q_mma(const unsigned char* __restrict__ vt,
+                                         const float* __restrict__ ps, float (&acc)[D / 16][4],
+                                         int lane, int nvalid) {
   constexpr int NWORD = D / 32;  // code words per lane and token
   const int gid = lane >> 2, tig = lane & 3;
   uint32_t whi[4], wlo[4];  // W[token tig + 4j][head gid] = hi + lo
@@ -272,8 +297,9 @@ __device__ __forceinline__ void pv_i8_mma(const unsigned char* __restrict__ vt,
   }
 #pragma unroll
   for (int ks = 0; ks < 2; ++ks) {
-    const unsigned char* r0 = v_i8_row_run<D>(vt, 8 * ks + tig, gid);
-    const unsigned char* r1 = v_i8_row_run<D>(vt, 8 * ks + tig + 4, gid);
+    const int t0 = 8 * ks + tig, t1 = t0 + 4;
+    const unsigned char* r0 = v_i8_row_run<D>(vt, t0, gid);
+    const unsigned char* r1 = v_i8_row_run<D>(vt, t1, gid);
     uint32_t w0[NWORD], w1[NWORD];
     if constexpr (NWORD == 4) {
       const uint4 x = *reinterpret_cast<const uint4*>(r0);
@@ -286,11 +312,23 @@ __device__ __forceinline__ void pv_i8_mma(const unsigned char* __restrict__ vt,
       w0[0] = x.x; w0[1] = x.y;
       w1[0] = y.x; w1[1] = y.y;
     }
+    if constexpr (F8 && !FULL) {
+#pragma unroll
+      for (int j = 0; j < NWORD; ++j) {
+        if (t0 >= nvalid) w0[j] = 0u;
+        if (t1 >= nvalid) w1[j] = 0u;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < NWORD; ++j) {
       uint32_t f0[4], f1[4];
-      int8x4_to_tf32(w0[j], f0);
-      int8x4_to_tf32(w1[j], f1);
+      if constexpr (F8) {
+        e4m3x4_to_tf32(w0[j], f0);
+        e4m3x4_to_tf32(w1[j], f1);
+      } else {
+        int8x4_to_tf32(w0[j], f0);
+        int8x4_to_tf32(w1[j], f1);
+      }
       // word j holds dims 4j .. 4j+3 of the lane's run: MMAs 2j and 2j + 1
       mma_tf32(acc[2 * j], f0[0], f0[1], f1[0], f1[1], whi[2 * ks], whi[2 * ks + 1]);
       mma_tf32(acc[2 * j + 1], f0[2], f0[3], f1[2], f1[3], whi[2 * ks], whi[2 * ks + 1]);
@@ -387,7 +425,97 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
       acc[c][3] *= a1;
     }
   }
-  pv_i8_mma<D, G>(vt, ps, acc, lane);
+  pv_q_mma<D, G, false, FULL>(vt, ps, acc, lane, nvalid);
+}
+
+// One FP8 (E4M3) tile: QK in the bf16 step's geometry (lane (rg, sub) holds
+// dims [8 sub, 8 sub + 8) of q, pre-scaled by scale * log2 e, in fp32) on the
+// decoded codes, times each token's K scale; the same softmax; PV on the
+// tensor cores with the V scale folded into the weights.
+template <int D, int G, bool FULL>
+__device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ kt,
+                                             const unsigned char* __restrict__ vt,
+                                             const float* __restrict__ ksc,
+                                             const float* __restrict__ vsc, float* ps,
+                                             float* alpha_s, const float2 (&q2)[G][4],
+                                             float (&acc)[D / 16][4], float& m_run, float& l_run,
+                                             int nvalid, int lane, int sub, int rg, int my_head,
+                                             int my_i0) {
+  using Geo = Geometry<D, G>;
+  constexpr int L = Geo::L, ROWS = Geo::ROWS, P = Geo::P, NV = Geo::NV, R = Geo::R;
+
+  // QK: partial dots over this lane's 8 dims, value index g * P + i.
+  float sc[NV];
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    const int t = i * ROWS + rg;
+    const uint2 w = *reinterpret_cast<const uint2*>(kt + t * D + sub * 8);
+    const float2 k0 = e4m3x2_to_float2(w.x), k1 = e4m3x2_to_float2(w.x >> 16);
+    const float2 k2 = e4m3x2_to_float2(w.y), k3 = e4m3x2_to_float2(w.y >> 16);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float2 a = __fmul2_rn(q2[g][0], k0);
+      a = __ffma2_rn(q2[g][1], k1, a);
+      a = __ffma2_rn(q2[g][2], k2, a);
+      a = __ffma2_rn(q2[g][3], k3, a);
+      sc[g * P + i] = a.x + a.y;
+    }
+  }
+  // the transposing butterfly of tile_step
+#pragma unroll
+  for (int m = L / 2, n = NV; m >= 1; m >>= 1, n >>= 1) {
+    const bool up = (lane & m) != 0;
+#pragma unroll
+    for (int k = 0; k < n / 2; ++k) {
+      const float send = up ? sc[k] : sc[k + n / 2];
+      const float keep = up ? sc[k + n / 2] : sc[k];
+      sc[k] = keep + __shfl_xor_sync(kFullMask, send, m);
+    }
+  }
+
+  float s[R];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int t = (my_i0 + r) * ROWS + rg;
+    // a token past the context is masked by position (its codes and scale may
+    // be anything, NaN included)
+    s[r] = (FULL || t < nvalid) ? sc[r] * ksc[t] : -INFINITY;
+    mx = fmaxf(mx, s[r]);
+  }
+#pragma unroll
+  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+#pragma unroll
+  for (int m = L; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
+  const float m_new = fmaxf(m_run, mx);
+  const float alpha = exp2f(m_run - m_new);
+  float psum = 0.f;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int t = (my_i0 + r) * ROWS + rg;
+    const float pr = exp2f(s[r] - m_new);
+    psum += pr;
+    ps[t * G + my_head] = pr * ((FULL || t < nvalid) ? vsc[t] : 0.f);  // V scale folded in
+  }
+  l_run = l_run * alpha + psum;
+  m_run = m_new;
+  if (sub % Geo::HEAD_LANES == 0 && rg == 0) alpha_s[my_head] = alpha;
+  const bool rescale = __any_sync(kFullMask, alpha != 1.0f);
+  __syncwarp();
+
+  if (rescale) {
+    const int h0 = 2 * (lane & 3);
+    const float a0 = h0 < G ? alpha_s[h0] : 1.f;
+    const float a1 = h0 + 1 < G ? alpha_s[h0 + 1] : 1.f;
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      acc[c][0] *= a0;
+      acc[c][1] *= a1;
+      acc[c][2] *= a0;
+      acc[c][3] *= a1;
+    }
+  }
+  pv_q_mma<D, G, true, FULL>(vt, ps, acc, lane, nvalid);
 }
 
 }  // namespace pa

@@ -22,8 +22,9 @@ struct DecodeParams {
   const __nv_bfloat16* v_cache;
   const int8_t* k8;        // int8 cache: codes [NB, Hkv, bs, D] (null for a bf16 cache)
   const int8_t* v8;
-  const float* k_scales;   // int8 cache: one scale per (block, head, token)
+  const float* k_scales;   // int8 / fp8 cache: one scale per (block, head, token)
   const float* v_scales;
+  int fp8;                 // 1-byte cache: codes are FP8 (E4M3), not INT8
   const int32_t* block_tables;
   const int32_t* context_lens;
   unsigned* err;
@@ -62,10 +63,11 @@ struct CacheWriteParams {
   int head_dim;
   int block_size;
   int64_t num_slots;  // num_blocks * block_size
-  int8_t* k8;         // int8 cache (null for bf16): codes [NB, Hkv, bs, D]
+  int8_t* k8;         // int8 / fp8 cache (null for bf16): codes [NB, Hkv, bs, D]
   int8_t* v8;
   float* k_scales;    // [NB, Hkv, bs]
   float* v_scales;
+  int fp8;            // codes are FP8 (E4M3), not INT8
 };
 
 // Pools of up to kCopyMaxLayers layers go to one copy_blocks launch.

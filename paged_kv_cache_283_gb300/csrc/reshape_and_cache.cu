@@ -12,6 +12,7 @@
 // fully coalesced 16-byte accesses.  Bad slots are never written: they set
 // PA_DEVERR_SLOT.
 
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -53,7 +54,10 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const CacheWrite
 // INT8 cache write: one warp per (token, KV head) row quantises it with one
 // scale (scale = amax / 127, code = round-half-even(x / scale), fp32, as in
 // pa.h) and writes D codes and the scale.  Each lane owns D / 32 values.
-template <int D>
+// F8: the same with FP8 (E4M3) codes: scale = amax / 448 (E4M3's largest
+// finite value), code = E4M3 of fp32(x / scale), round to nearest even,
+// saturated (cvt.rn.satfinite).
+template <int D, bool F8>
 __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(const CacheWriteParams p) {
   griddep_wait();
   griddep_launch_dependents();
@@ -93,13 +97,23 @@ __global__ void __launch_bounds__(256) reshape_and_cache_int8_kernel(const Cache
     for (int i = 0; i < PER; ++i) amax = fmaxf(amax, fabsf(f[i]));
 #pragma unroll
     for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
-    const float scale = __fdiv_rn(amax, 127.0f);
+    const float scale = __fdiv_rn(amax, F8 ? 448.0f : 127.0f);
     uint32_t packed = 0;
     if (scale > 0.f) {
+      if constexpr (F8) {
 #pragma unroll
-      for (int i = 0; i < PER; ++i) {
-        const float c = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[i], scale))));
-        packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * i);
+        for (int i = 0; i < PER; i += 2) {
+          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
+              make_float2(__fdiv_rn(f[i], scale), __fdiv_rn(f[i + 1], scale)), __NV_SATFINITE,
+              __NV_E4M3);
+          packed |= static_cast<uint32_t>(c2) << (8 * i);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+          const float c = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[i], scale))));
+          packed |= (static_cast<uint32_t>(static_cast<int>(c)) & 0xffu) << (8 * i);
+        }
       }
     }
     // K rows are plain; V tiles have their 16-byte units permuted within each
@@ -126,12 +140,13 @@ cudaError_t launch_reshape_and_cache_int8(const CacheWriteParams& p, cudaStream_
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = (rows + 7) / 8;
   if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(blocks));
   if (p.head_dim == 128)
-    return launch_pdl(reshape_and_cache_int8_kernel<128>, dim3(static_cast<unsigned>(blocks)),
-                      dim3(256), 0, stream, p);
+    return p.fp8 ? launch_pdl(reshape_and_cache_int8_kernel<128, true>, grid, dim3(256), 0, stream, p)
+                 : launch_pdl(reshape_and_cache_int8_kernel<128, false>, grid, dim3(256), 0, stream, p);
   if (p.head_dim == 64)
-    return launch_pdl(reshape_and_cache_int8_kernel<64>, dim3(static_cast<unsigned>(blocks)),
-                      dim3(256), 0, stream, p);
+    return p.fp8 ? launch_pdl(reshape_and_cache_int8_kernel<64, true>, grid, dim3(256), 0, stream, p)
+                 : launch_pdl(reshape_and_cache_int8_kernel<64, false>, grid, dim3(256), 0, stream, p);
   return cudaErrorInvalidValue;
 }
 

@@ -44,6 +44,12 @@ SIGNATURES = {
                             _f, _vp]),
     "pa_decode_splitk_int8": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
                                    _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "pa_reshape_and_cache_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                                      _vp]),
+    "pa_decode_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
+                           _f, _vp]),
+    "pa_decode_splitk_fp8": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                  _i, _i, _i, _i, _i, _f, _i, _vp]),
     "pa_decode": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _vp]),
     "pa_splitk_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
@@ -214,13 +220,15 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, strea
     _check(st, "pa_decode")
 
 
-def _int8_pools(k_cache, v_cache, k_scales, v_scales):
+def _int8_pools(k_cache, v_cache, k_scales, v_scales, fp8=False):
     torch = _torch()
     nb, hkv, bs, d = k_cache.shape
     if v_cache.shape != k_cache.shape or k_scales.shape != (nb, hkv, bs) or \
             v_scales.shape != k_scales.shape:
-        raise ValueError("int8 cache: pools [NB, Hkv, bs, D] int8, scales [NB, Hkv, bs] fp32")
-    return (_dev(k_cache, torch.int8, "k_cache", 4), _dev(v_cache, torch.int8, "v_cache", 4),
+        raise ValueError("1-byte cache: pools [NB, Hkv, bs, D] int8 (INT8) or uint8 (FP8 E4M3 "
+                         "codes), scales [NB, Hkv, bs] fp32")
+    code = torch.uint8 if fp8 else torch.int8
+    return (_dev(k_cache, code, "k_cache", 4), _dev(v_cache, code, "v_cache", 4),
             _dev(k_scales, torch.float32, "k_scales", 3),
             _dev(v_scales, torch.float32, "v_scales", 3)), (nb, hkv, bs, d)
 
@@ -240,10 +248,11 @@ def pa_reshape_and_cache_int8(key, value, k_cache, v_cache, k_scales, v_scales, 
     _check(st, "pa_reshape_and_cache_int8")
 
 
-def _decode_int8_common(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens):
+def _decode_int8_common(q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens,
+                        fp8=False):
     torch = _torch()
     B, hq, d = q.shape
-    pools, (nb, hkv, bs, d2) = _int8_pools(k_cache, v_cache, k_scales, v_scales)
+    pools, (nb, hkv, bs, d2) = _int8_pools(k_cache, v_cache, k_scales, v_scales, fp8)
     if d != d2 or block_tables.dim() != 2 or block_tables.shape[0] != B or \
             context_lens.shape != (B,):
         raise ValueError("int8 decode: inconsistent shapes")
@@ -322,6 +331,49 @@ def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition
     return (torch.empty((num_seqs, num_q_heads, maxp, head_dim), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device))
+
+
+def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
+                             stream=None):
+    """key/value [T, Hkv, D] bf16 quantised into FP8 (E4M3) pools (uint8 codes) + fp32 scales."""
+    torch = _torch()
+    T, hkv, d = key.shape
+    (pk, pv, pks, pvs), (nb, hkv2, bs, d2) = _int8_pools(k_cache, v_cache, k_scales, v_scales,
+                                                         True)
+    if value.shape != key.shape or (hkv, d) != (hkv2, d2) or slot_mapping.shape != (T,):
+        raise ValueError("pa_reshape_and_cache_fp8: inconsistent shapes")
+    st = lib().pa_reshape_and_cache_fp8(
+        _dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3), pk, pv,
+        pks, pvs, _dev(slot_mapping, torch.int64, "slot_mapping", 1), T, hkv, d, bs, nb,
+        _stream(stream))
+    _check(st, "pa_reshape_and_cache_fp8")
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens,
+                  scale, stream=None):
+    torch = _torch()
+    (pq, pk, pv, pks, pvs, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_int8_common(
+        q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, True)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode_fp8: out must match q")
+    st = lib().pa_decode_fp8(_dev(out, torch.bfloat16, "out", 3), pq, pk, pv, pks, pvs, pt, mb,
+                             pc, B, hq, hkv, d, bs, nb, float(scale), _stream(stream))
+    _check(st, "pa_decode_fp8")
+
+
+def pa_decode_splitk_fp8(ws_out, ws_m, ws_l, q, k_cache, v_cache, k_scales, v_scales,
+                         block_tables, context_lens, scale, partition_size=512, stream=None):
+    torch = _torch()
+    (pq, pk, pv, pks, pvs, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_int8_common(
+        q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, True)
+    maxp = ws_m.shape[2]
+    if ws_out.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape or ws_m.shape[:2] != (B, hq):
+        raise ValueError("pa_decode_splitk_fp8: workspace shapes")
+    st = lib().pa_decode_splitk_fp8(
+        _dev(ws_out, torch.float32, "ws_out", 4), _dev(ws_m, torch.float32, "ws_m", 3),
+        _dev(ws_l, torch.float32, "ws_l", 3), maxp, pq, pk, pv, pks, pvs, pt, mb, pc, B, hq, hkv,
+        d, bs, nb, float(scale), int(partition_size), _stream(stream))
+    _check(st, "pa_decode_splitk_fp8")
 
 
 def pa_decode_splitk_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale,
@@ -410,10 +462,11 @@ class DecodeStep:
             raise ValueError("DecodeStep: inconsistent key / cache shapes")
         if slot_mapping.shape != (T,):
             raise ValueError("DecodeStep: slot_mapping must be [num_tokens]")
-        self.int8 = k_cache.dtype == torch.int8
+        self.fp8 = k_cache.dtype == torch.uint8        # FP8 (E4M3) codes
+        self.int8 = k_cache.dtype == torch.int8 or self.fp8  # a 1-byte cache with scales
         if self.int8:
             (pq, pk, pv, pks, pvs, pt, pc), (B, hq, _, _, _, _, mb) = _decode_int8_common(
-                q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens)
+                q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, self.fp8)
         else:
             (pq, pk, pv, pt, pc), (B, hq, _, _, _, _, mb) = _decode_common(
                 q, k_cache, v_cache, block_tables, context_lens)
@@ -451,7 +504,10 @@ class DecodeStep:
         else:
             self._dc = (po, pq) + kvp + (pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale))
         L = lib()
-        if self.int8:
+        if self.fp8:
+            self._f_write, self._f_split, self._f_whole = (
+                L.pa_reshape_and_cache_fp8, L.pa_decode_splitk_fp8, L.pa_decode_fp8)
+        elif self.int8:
             self._f_write, self._f_split, self._f_whole = (
                 L.pa_reshape_and_cache_int8, L.pa_decode_splitk_int8, L.pa_decode_int8)
         else:
