@@ -84,8 +84,8 @@ struct Pipe<128, SPLIT, I8> {
 // stages of 4.2 KiB in flight (head_dim 128).
 template <int NW, int G, int Q>
 constexpr int min_blocks() {
-  if constexpr (Q == 1) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
-  else return (NW <= 4 && G <= 4) ? 3 : 1;  // bf16; FP8 keeps the bf16 QK registers
+  if constexpr (Q != 0) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
+  else return (NW <= 4 && G <= 4) ? 3 : 1;  // bf16
 }
 
 template <int D, int G, int NW, int S, bool I8>
@@ -109,7 +109,8 @@ struct SmemLayout {
 };
 // Q: the cache's element type: 0 = bf16, 1 = INT8, 2 = FP8 (E4M3).  INT8 and
 // FP8 share the 1-byte-code tile layout (codes + per-token scales) and the
-// tensor-core PV; INT8 alone quantises q and takes QK in integers.
+// tensor-core PV; INT8 quantises q and takes QK in integers, FP8 takes QK on
+// the tensor cores as well (f16 MMAs on the exactly converted codes).
 template <int D, int G, int NW, int S, bool SPLIT, int Q>
 __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     paged_decode_kernel(const DecodeParams p) {
@@ -151,7 +152,54 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   float2 q2[G][4];
   int qc[G][IG::QW];  // int8 cache: this lane's q codes, 4 per word
   float qsc[G];       // int8 cache: q scale times scale * log2(e)
-  if constexpr (!QI) {
+  uint32_t qf[D / 16][2];  // fp8 cache: q's MMA fragments (tile_step_f8), f16 pairs
+  float2 qfac;             // fp8 cache: per-head factor of heads 2 tig, 2 tig + 1
+  if constexpr (Q == 2) {
+    // Lane (gid, tig) holds head gid's dims [(D/4) tig, +D/4) (zeros for gid >= G),
+    // times 2^k with k per head chosen so that the head's largest |q| lands in
+    // [2^14, 2^15): every bf16 value then converts to f16 exactly unless it is
+    // below 2^-14 (an absolute error under 2^-25 of that maximum), and the
+    // products with codes (|x| <= 448) stay far inside fp32.  qfac carries
+    // 2^-k * scale * log2 e back onto the scores.
+    constexpr int E = D / 4;
+    const int gid = lane >> 2, tig = lane & 3;
+    float f[E];
+    float amax = 0.f;
+    if (gid < G) {
+      const __nv_bfloat16* qh =
+          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + gid) * D +
+          E * tig;
+#pragma unroll
+      for (int u = 0; u < E / 8; ++u) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+        const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
+        f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
+        f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < E; ++k) f[k] = 0.f;
+    }
+#pragma unroll
+    for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+    // biased exponent of amax (0 for 0 and subnormals); k = 14 - unbiased
+    const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    const int kexp = min(127, max(-126, 141 - ebits));
+    const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
+#pragma unroll
+    for (int s2 = 0; s2 < D / 16; ++s2) {
+      const __half2 lo = __floats2half2_rn(f[4 * s2] * up, f[4 * s2 + 1] * up);
+      const __half2 hi = __floats2half2_rn(f[4 * s2 + 2] * up, f[4 * s2 + 3] * up);
+      qf[s2][0] = *reinterpret_cast<const uint32_t*>(&lo);
+      qf[s2][1] = *reinterpret_cast<const uint32_t*>(&hi);
+    }
+    const float fac = gid < G ? ldexpf(p.scale_log2, -kexp) : 0.f;
+    qfac = make_float2(__shfl_sync(kFullMask, fac, 8 * tig),
+                       __shfl_sync(kFullMask, fac, 8 * tig + 4));
+  } else if constexpr (Q == 0) {
     const __nv_bfloat16* qb =
         p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
     uint4 qw[G];
@@ -303,6 +351,8 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     for (int k = 0; k < 4; ++k) acc8[c][k] = 0.f;
   float m_run = -INFINITY;  // running max of this lane's head, base-2 units
   float l_run = 0.f;        // this lane's share of that head's exp-sum
+  float2 m_run2 = make_float2(-INFINITY, -INFINITY);  // fp8 cache: heads 2 tig, 2 tig + 1
+  float2 l_run2 = make_float2(0.f, 0.f);
   // The lane geometry of the scores and softmax state: the bf16 step's, or
   // the int8 QK geometry.
   constexpr int SL = QI ? IG::QL : L;
@@ -344,11 +394,11 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
                                     m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
       } else {
         if (nvalid == BS)
-          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, q2, acc8, m_run,
-                                   l_run, nvalid, lane, sub, rg, my_head, my_i0);
+          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, qf, qfac, acc8, m_run2,
+                                   l_run2, nvalid, lane);
         else
-          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, q2, acc8, m_run,
-                                    l_run, nvalid, lane, sub, rg, my_head, my_i0);
+          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, qf, qfac, acc8, m_run2,
+                                    l_run2, nvalid, lane);
       }
     }
     consumed = i + 1;
@@ -360,10 +410,18 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   for (int i = consumed; i < issued; ++i) mbar_wait_bounded(&bars[i % S], (i / S) & 1, p.err);
 
   // Per-warp totals: l over the lanes of each head, acc over row groups.
+  if constexpr (Q == 2) {
 #pragma unroll
-  for (int m = 1; m < SHL; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+    for (int m = 4; m < 32; m <<= 1) {
+      l_run2.x += __shfl_xor_sync(kFullMask, l_run2.x, m);
+      l_run2.y += __shfl_xor_sync(kFullMask, l_run2.y, m);
+    }
+  } else {
 #pragma unroll
-  for (int m = SL; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+    for (int m = 1; m < SHL; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+#pragma unroll
+    for (int m = SL; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+  }
   // Merge warps through shared memory (each warp writes into its own, now
   // idle, tile ring): [G][D] acc, then m[G], l[G].
   float* mrg = reinterpret_cast<float*>(wbase);
@@ -400,7 +458,17 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       }
     }
   }
-  if (srg == 0 && ssub % SHL == 0) {
+  if constexpr (Q == 2) {
+    const int h0 = 2 * lane;  // lanes 0-3 (gid 0): heads 2 tig, 2 tig + 1
+    if (lane < 4 && h0 < G) {
+      mrg[G * D + h0] = m_run2.x;
+      mrg[G * D + G + h0] = l_run2.x;
+    }
+    if (lane < 4 && h0 + 1 < G) {
+      mrg[G * D + h0 + 1] = m_run2.y;
+      mrg[G * D + G + h0 + 1] = l_run2.y;
+    }
+  } else if (srg == 0 && ssub % SHL == 0) {
     mrg[G * D + my_head] = m_run;
     mrg[G * D + G + my_head] = l_run;
   }

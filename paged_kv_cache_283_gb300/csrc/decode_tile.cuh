@@ -428,91 +428,106 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
   pv_q_mma<D, G, false, FULL>(vt, ps, acc, lane, nvalid);
 }
 
-// One FP8 (E4M3) tile: QK in the bf16 step's geometry (lane (rg, sub) holds
-// dims [8 sub, 8 sub + 8) of q, pre-scaled by scale * log2 e, in fp32) on the
-// decoded codes, times each token's K scale; the same softmax; PV on the
-// tensor cores with the V scale folded into the weights.
+// One m16n8k16 f16 tensor-core step, fp32 accumulate: c += a · b.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2 E4M3 codes (16 bits, first code in the low byte) to an f16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t h) {
+  const __half2_raw r =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// One FP8 (E4M3) tile.  QK on the tensor cores: S[token][head] = K · qᵀ with
+// m16n8k16 f16 MMAs (M = the tile's 16 tokens, N = 8 heads, the group padded
+// with zeros, K = 16 dims a step).  The codes are exact in f16; q arrives as
+// f16 pairs already multiplied by a power of two per head (exact for bf16 q,
+// see the kernel's prologue) and qfac undoes it together with scale * log2 e.
+// Lane (gid = lane / 4, tig = lane % 4) feeds tokens gid and gid + 8 and reads
+// the D/4 code bytes at dims [(D/4)·tig, +D/4) of each; its step-s fragment
+// columns 2tig, 2tig+1 | 2tig+8, 2tig+9 are dims (D/4)·tig + 4s + 0, 1 | 2, 3,
+// the same dims q's fragment (qf[s], head gid) holds, so the dims reach the
+// MMA in a different order than in memory but every one exactly once.  The
+// accumulator puts scores (token gid | gid + 8, head 2tig | 2tig + 1) in the
+// lane, which are the heads its PV accumulators hold (pv_q_mma), so the
+// online softmax state (m_run, l_run: heads 2tig, 2tig + 1) and the rescale
+// stay in the lane; l_run is this lane's share, summed over gid at the end.
 template <int D, int G, bool FULL>
 __device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ kt,
                                              const unsigned char* __restrict__ vt,
                                              const float* __restrict__ ksc,
                                              const float* __restrict__ vsc, float* ps,
-                                             float* alpha_s, const float2 (&q2)[G][4],
-                                             float (&acc)[D / 16][4], float& m_run, float& l_run,
-                                             int nvalid, int lane, int sub, int rg, int my_head,
-                                             int my_i0) {
-  using Geo = Geometry<D, G>;
-  constexpr int L = Geo::L, ROWS = Geo::ROWS, P = Geo::P, NV = Geo::NV, R = Geo::R;
-
-  // QK: partial dots over this lane's 8 dims, value index g * P + i.
-  float sc[NV];
+                                             const uint32_t (&qf)[D / 16][2], float2 qfac,
+                                             float (&acc)[D / 16][4], float2& m_run,
+                                             float2& l_run, int nvalid, int lane) {
+  constexpr int KS = D / 16;  // MMA steps = code words per lane and row
+  const int gid = lane >> 2, tig = lane & 3;
+  uint32_t w0[KS], w1[KS];  // codes of tokens gid and gid + 8
+  {
+    const unsigned char* r0 = kt + gid * D + (D / 4) * tig;
+    const unsigned char* r1 = r0 + 8 * D;
 #pragma unroll
-  for (int i = 0; i < P; ++i) {
-    const int t = i * ROWS + rg;
-    const uint2 w = *reinterpret_cast<const uint2*>(kt + t * D + sub * 8);
-    const float2 k0 = e4m3x2_to_float2(w.x), k1 = e4m3x2_to_float2(w.x >> 16);
-    const float2 k2 = e4m3x2_to_float2(w.y), k3 = e4m3x2_to_float2(w.y >> 16);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float2 a = __fmul2_rn(q2[g][0], k0);
-      a = __ffma2_rn(q2[g][1], k1, a);
-      a = __ffma2_rn(q2[g][2], k2, a);
-      a = __ffma2_rn(q2[g][3], k3, a);
-      sc[g * P + i] = a.x + a.y;
+    for (int u = 0; u < KS / 4; ++u) {
+      const uint4 x = *reinterpret_cast<const uint4*>(r0 + 16 * u);
+      const uint4 y = *reinterpret_cast<const uint4*>(r1 + 16 * u);
+      w0[4 * u] = x.x; w0[4 * u + 1] = x.y; w0[4 * u + 2] = x.z; w0[4 * u + 3] = x.w;
+      w1[4 * u] = y.x; w1[4 * u + 1] = y.y; w1[4 * u + 2] = y.z; w1[4 * u + 3] = y.w;
     }
   }
-  // the transposing butterfly of tile_step
+  // two independent accumulation chains, summed at the end
+  float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-  for (int m = L / 2, n = NV; m >= 1; m >>= 1, n >>= 1) {
-    const bool up = (lane & m) != 0;
-#pragma unroll
-    for (int k = 0; k < n / 2; ++k) {
-      const float send = up ? sc[k] : sc[k + n / 2];
-      const float keep = up ? sc[k + n / 2] : sc[k];
-      sc[k] = keep + __shfl_xor_sync(kFullMask, send, m);
-    }
-  }
+  for (int s = 0; s < KS; ++s)
+    mma_f16(c[s & 1], e4m3x2_to_f16x2(w0[s]), e4m3x2_to_f16x2(w1[s]),
+            e4m3x2_to_f16x2(w0[s] >> 16), e4m3x2_to_f16x2(w1[s] >> 16), qf[s][0], qf[s][1]);
 
-  float s[R];
-  float mx = -INFINITY;
+  // scores in base-2 units; a token past the context is masked by position
+  // (its codes and scale may be anything, NaN included)
+  const bool ok0 = FULL || gid < nvalid, ok1 = FULL || gid + 8 < nvalid;
+  const float k0 = ok0 ? ksc[gid] : 0.f, k1 = ok1 ? ksc[gid + 8] : 0.f;
+  float s[4];
+  s[0] = ok0 ? (c[0][0] + c[1][0]) * k0 * qfac.x : -INFINITY;
+  s[1] = ok0 ? (c[0][1] + c[1][1]) * k0 * qfac.y : -INFINITY;
+  s[2] = ok1 ? (c[0][2] + c[1][2]) * k1 * qfac.x : -INFINITY;
+  s[3] = ok1 ? (c[0][3] + c[1][3]) * k1 * qfac.y : -INFINITY;
+  float2 mx = make_float2(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
 #pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int t = (my_i0 + r) * ROWS + rg;
-    // a token past the context is masked by position (its codes and scale may
-    // be anything, NaN included)
-    s[r] = (FULL || t < nvalid) ? sc[r] * ksc[t] : -INFINITY;
-    mx = fmaxf(mx, s[r]);
+  for (int m = 4; m < 32; m <<= 1) {
+    mx.x = fmaxf(mx.x, __shfl_xor_sync(kFullMask, mx.x, m));
+    mx.y = fmaxf(mx.y, __shfl_xor_sync(kFullMask, mx.y, m));
   }
-#pragma unroll
-  for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
-#pragma unroll
-  for (int m = L; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
-  const float m_new = fmaxf(m_run, mx);
-  const float alpha = exp2f(m_run - m_new);
-  float psum = 0.f;
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const int t = (my_i0 + r) * ROWS + rg;
-    const float pr = exp2f(s[r] - m_new);
-    psum += pr;
-    ps[t * G + my_head] = pr * ((FULL || t < nvalid) ? vsc[t] : 0.f);  // V scale folded in
-  }
-  l_run = l_run * alpha + psum;
+  const float2 m_new = make_float2(fmaxf(m_run.x, mx.x), fmaxf(m_run.y, mx.y));
+  const float2 alpha = make_float2(exp2f(m_run.x - m_new.x), exp2f(m_run.y - m_new.y));
+  const float p0 = exp2f(s[0] - m_new.x), p1 = exp2f(s[1] - m_new.y);
+  const float p2 = exp2f(s[2] - m_new.x), p3 = exp2f(s[3] - m_new.y);
+  l_run = make_float2(l_run.x * alpha.x + (p0 + p2), l_run.y * alpha.y + (p1 + p3));
   m_run = m_new;
-  if (sub % Geo::HEAD_LANES == 0 && rg == 0) alpha_s[my_head] = alpha;
-  const bool rescale = __any_sync(kFullMask, alpha != 1.0f);
+  // weights with the V scale folded in; 0 past the context
+  const float v0 = ok0 ? vsc[gid] : 0.f, v1 = ok1 ? vsc[gid + 8] : 0.f;
+  const int h0 = 2 * tig;
+  if (h0 < G) {
+    ps[gid * G + h0] = p0 * v0;
+    ps[(gid + 8) * G + h0] = p2 * v1;
+  }
+  if (h0 + 1 < G) {
+    ps[gid * G + h0 + 1] = p1 * v0;
+    ps[(gid + 8) * G + h0 + 1] = p3 * v1;
+  }
+  const bool rescale = __any_sync(kFullMask, alpha.x != 1.0f || alpha.y != 1.0f);
   __syncwarp();
-
   if (rescale) {
-    const int h0 = 2 * (lane & 3);
-    const float a0 = h0 < G ? alpha_s[h0] : 1.f;
-    const float a1 = h0 + 1 < G ? alpha_s[h0 + 1] : 1.f;
 #pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-      acc[c][0] *= a0;
-      acc[c][1] *= a1;
-      acc[c][2] *= a0;
-      acc[c][3] *= a1;
+    for (int cc = 0; cc < D / 16; ++cc) {
+      acc[cc][0] *= alpha.x;
+      acc[cc][1] *= alpha.y;
+      acc[cc][2] *= alpha.x;
+      acc[cc][3] *= alpha.y;
     }
   }
   pv_q_mma<D, G, true, FULL>(vt, ps, acc, lane, nvalid);

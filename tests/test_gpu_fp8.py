@@ -112,3 +112,23 @@ def test_fp8_edge_contexts_nan_tail(d, hq, hkv, split):
     got, ref = _fp8_step(w, split, nan_tail=True)
     assert_close(got, ref, f"fp8 edge d={d} hq={hq} split={split}")
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 64, 8), (64, 4, 2)])
+@pytest.mark.parametrize("split", [None, 64])
+def test_fp8_q_magnitudes(d, hq, hkv, split):
+    """q heads far outside f16's range (|q| ~ 1e5 and ~ 1e-6), an all-zero head
+    and a head whose elements span 1e-3 .. 1e3: the scores must keep their
+    relative precision whatever the magnitude of q."""
+    w = I.random_case(4000 + d + hq, len(EDGE), EDGE, hq, hkv, d)
+    rng = np.random.default_rng(d + hq)
+    q = (w.q.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    q[:, 0::4] *= 1e5
+    q[:, 1::4] *= 1e-6
+    q[:, 2] = 0.0
+    q[:, 3::4] *= 10.0 ** rng.uniform(-3, 3, size=q[:, 3::4].shape)
+    w.q = I.f32_to_bf16_bits(q.astype(np.float32))
+    pa.pa_clear_device_error()
+    got, ref = _fp8_step(w, split)
+    assert_close(got, ref, f"fp8 q magnitudes d={d} hq={hq} split={split}")
+    assert pa.pa_get_device_error() == 0
