@@ -407,7 +407,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
     return st
 
 
-def _attn_fns(st, attn, partition):
+def _attn_fns(st, attn, partition, fused=True):
     import torch
 
     from paged_kv_cache_283_gb300 import pa
@@ -418,6 +418,25 @@ def _attn_fns(st, attn, partition):
     if attn == "splitk":
         ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
                                  int(w.context_lens.max()), partition, st["q"][0].device)
+
+    if fused:
+        # one pa_decode_step launch per layer: cache write + attention (+ merge)
+        counters = (pa.step_counters(w.num_seqs, w.num_kv_heads, st["q"][0].device)
+                    if attn == "splitk" else None)
+
+        def fused_layer(layer, *pool):
+            scales = {"k_scales": pool[2], "v_scales": pool[3]} if len(pool) == 4 else {}
+            pa.pa_decode_step(outs[layer], st["q"][layer], pool[0], pool[1], st["bt"], st["ctx"],
+                              w.scale, key=st["key"][layer], value=st["value"][layer],
+                              slot_mapping=st["slots"],
+                              partition_size=partition if attn == "splitk" else 0,
+                              workspace=ws, counters=counters, **scales)
+
+        def fused_step(r):
+            for layer, pool in enumerate(st["replicas"][r]):
+                fused_layer(layer, *pool)
+
+        return fused_step, fused_layer, outs
 
     sfx = KV_SUFFIX[st.get("kv", "bf16")]
     f_split = getattr(pa, "pa_decode_splitk" + sfx)
@@ -530,7 +549,8 @@ def run_gpu(args):
     attn = args.attn
     if attn == "auto":
         attn = "splitk" if args.workload in (2, 3, 5) else "decode"
-    step, dominant, outs = _attn_fns(st, attn, args.partition)
+    fused = args.step == "fused"
+    step, dominant, outs = _attn_fns(st, attn, args.partition, fused)
 
     # eager warmup (sets kernel attributes, checks the error word)
     with torch.cuda.stream(stream):
@@ -540,7 +560,7 @@ def run_gpu(args):
     assert pa.pa_get_device_error() == 0, "device error word set during warmup"
 
     graphs = [_capture(lambda r=r: step(r), stream) for r in range(len(st["replicas"]))]
-    launches_per_step = w.layers * (2 if attn == "decode" else 3)
+    launches_per_step = w.layers * (1 if fused else (2 if attn == "decode" else 3))
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -579,20 +599,37 @@ def run_gpu(args):
                                                  args.kv))
     dom_bytes = decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads, w.num_kv_heads,
                              w.head_dim, w.block_size, args.kv)
+    if fused:  # the fused kernel also does the cache write
+        dom_bytes += cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim, args.kv)
     dt_max, value = combine_ranks(dt, step_bytes, args.steps, world, device)
     hbm_peak = peaks.get("hbm_gbs")
     achieved = dom_bytes / dom_dt / 1e9
+    if fused:
+        kname = ("pa_decode_step" + KV_SUFFIX[args.kv]
+                 + (" (split-K %d, merged in-kernel)" % args.partition if attn == "splitk"
+                    else " (whole sequence)"))
+        kkey = "pa_decode_step" + KV_SUFFIX[args.kv] + ("_splitk" if attn == "splitk" else "")
+    else:
+        kname = kkey = ("pa_decode_splitk" if attn == "splitk" else "pa_decode") + KV_SUFFIX[
+            args.kv]
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak if hbm_peak else 6800.0, "unit": "GB/s",
                 "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(
-                    ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
-                    + KV_SUFFIX[args.kv], w.name, args.partition),
-                "kernel": ("pa_decode_splitk" if attn == "splitk" else "pa_decode")
-                + KV_SUFFIX[args.kv],
+                    kkey, w.name, args.partition),
+                "kernel": kname,
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
                 else "fallback 6.8 TB/s",
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_dt * 1e6, 2)}
+    sfx = KV_SUFFIX[args.kv]
+    if fused:
+        attention = ("pa_decode_step%s: cache write + split-K (partition %d) + merge in one launch"
+                     % (sfx, args.partition) if attn == "splitk" else
+                     "pa_decode_step%s: cache write + whole-sequence decode in one launch" % sfx)
+    else:
+        attention = ("pa_reshape_and_cache%s, pa_decode_splitk%s, pa_splitk_reduce, partition %d"
+                     % (sfx, sfx, args.partition) if attn == "splitk" else
+                     "pa_reshape_and_cache%s, pa_decode%s" % (sfx, sfx))
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup,
@@ -603,11 +640,10 @@ def run_gpu(args):
             "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(np.mean(w.context_lens)), "new_tokens_per_step": w.num_seqs,
-            "attention": ("pa_decode_splitk%s+pa_splitk_reduce, partition %d"
-                          % (KV_SUFFIX[args.kv], args.partition))
-            if attn == "splitk" else "pa_decode" + KV_SUFFIX[args.kv],
+            "attention": attention,
             "kv_cache": args.kv,
             "graph": "one CUDA graph per step (cache write + attention)",
+            "step": args.step,
             "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
                   % (len(st["replicas"]), st["pool_bytes"] / 1e6, l2 / 1e6)
             if len(st["replicas"]) > 1 else "32 distinct per-layer pools per step",
@@ -677,7 +713,8 @@ def _e2e(st, attn, args, stream):
                                 views[("ctx", 0)], out[l], w.scale, split=attn == "splitk",
                                 partition_size=args.partition, workspace=ws, stream=stream,
                                 k_scales=pool[2] if len(pool) == 4 else None,
-                                v_scales=pool[3] if len(pool) == 4 else None)
+                                v_scales=pool[3] if len(pool) == 4 else None,
+                                fused=args.step == "fused")
                   for l, pool in enumerate(st["replicas"][r])] for r in range(nrep)]
         sets.append({"host": host, "staged": staged, "out": out, "hout": hout, "steps": steps,
                      "in_done": torch.cuda.Event(), "computed": torch.cuda.Event(),
@@ -718,7 +755,9 @@ def _e2e(st, attn, args, stream):
     return {"value": round(step_bytes * n / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(sets[0]["hout"].numel() * 2),
             "ms_per_step": dt / n * 1e3,
-            "how": "pa.DecodeStep per layer (pre-marshalled C calls); every step one pinned "
+            "how": "pa.DecodeStep per layer (pre-marshalled C calls; %s); every step one pinned "
+                   % ("one pa_decode_step launch" if args.step == "fused"
+                      else "separate cache-write / attention / merge launches") +
                    "host->device copy of all inputs and one device->host copy of the output, "
                    "double-buffered on two copy streams; wall clock around all steps"}
 
@@ -970,6 +1009,10 @@ def main(argv=None):
                     help="copy_blocks: time pa_copy_blocks on a parallel-sampling step; "
                          "prefill: time pa_prefill on a 16 x 512-token chunked-prefill step")
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])
+    ap.add_argument("--step", default="fused", choices=["fused", "separate"],
+                    help="fused: one pa_decode_step launch per layer (cache write + attention "
+                         "+ split-K merge); separate: the cache write, partition pass and "
+                         "merge as three launches")
     ap.add_argument("--partition", type=int, default=512)
     ap.add_argument("--soak-seconds", type=float, default=0.5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -9,6 +9,7 @@
  *                          sequence's blocks, found through its block table
  *   pa_decode_splitk       the same, one CTA per 512-token (configurable)
  *   pa_splitk_reduce       partition, then a log-sum-exp merge of partitions
+ *   pa_decode_step         cache write + decode (+ merge) in one launch
  *   pa_copy_blocks         copy-on-write: copy shared blocks a branch writes into
  *   *_int8, *_fp8          the cache write and decode over an INT8 / FP8 KV cache
  *   pa_prefill             causal attention of chunks of new tokens (prefill)
@@ -326,6 +327,63 @@ pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache
                                    int head_dim, int block_size, int num_blocks,
                                    float scale, int partition_size, int max_context_len,
                                    pa_stream_t stream);
+
+/*
+ * Fused decode step [LIFE], [KV], [PA]: each sequence's new token written
+ * into the cache and every query attended, in ONE kernel launch.  Computes
+ * exactly what
+ *   pa_reshape_and_cache(key, value, ..., slot_mapping, num_tokens = num_seqs)
+ * followed by pa_decode (partition_size == 0) or by pa_decode_splitk +
+ * pa_splitk_reduce (partition_size > 0) compute, under one condition on the
+ * slots: slot_mapping[b] (device int64 [num_seqs]) is negative (nothing to
+ * write) or the slot of position n - 1 of sequence b, n = context_lens[b],
+ *   block_tables[b][(n - 1) / block_size] * block_size + (n - 1) % block_size,
+ * i.e. the new token is the last one its own query attends to, as in a
+ * decode step.  The CTA that reads that position writes the row first; a slot
+ * that is not that position's (or n == 0 with a slot >= 0) is not written and
+ * sets PA_DEVERR_SLOT, since another CTA could be reading it.
+ *   key, value: device bf16 [num_seqs, num_kv_heads, head_dim], one new token
+ *     per sequence; key, value and slot_mapping are all NULL to skip the
+ *     write (attention only).
+ *   partition_size == 0: one CTA per (sequence, KV head); ws_* / counters /
+ *     max_partitions are ignored (may be NULL / 0).
+ *   partition_size > 0: split-K as pa_decode_splitk (same workspace and
+ *     limits).  With max_partitions <= 16 the partitions are merged inside
+ *     the same launch (the last CTA of each (sequence, KV head) to finish
+ *     merges them; a sequence with one partition writes out directly); with
+ *     more, the merge is a second launch, as pa_splitk_reduce.  counters:
+ *     device uint32 [num_seqs * num_kv_heads], all zero before the first call;
+ *     each call leaves them zero again, unless it sets PA_DEVERR_WAIT_TIMEOUT
+ *     (then zero them before the next call).  Concurrent calls must not
+ *     share counters or workspace.
+ * Pools, scales and other arguments as pa_decode / pa_decode_splitk and the
+ * _int8 / _fp8 cache writes (the 1-byte variants quantise the new rows by the
+ * same rule, bit-identically).
+ */
+pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value,
+                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, int partition_size, float* ws_out, float* ws_m,
+                         float* ws_l, unsigned* counters, int max_partitions,
+                         pa_stream_t stream);
+pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const void* value,
+                              const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
+                              float* k_scales, float* v_scales, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float scale, int partition_size, float* ws_out,
+                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
+                              pa_stream_t stream);
+pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const void* value,
+                             const int64_t* slot_mapping, uint8_t* k_cache, uint8_t* v_cache,
+                             float* k_scales, float* v_scales, const int32_t* block_tables,
+                             int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int partition_size, float* ws_out,
+                             float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
+                             pa_stream_t stream);
 
 /*
  * Paged (chunked) prefill attention ("How LLM Inference Serving Works",

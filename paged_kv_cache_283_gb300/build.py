@@ -24,7 +24,7 @@ SOURCES = ["api.cu", "decode.cu", "splitk_reduce.cu", "reshape_and_cache.cu", "c
            "scheduler.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
            os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh"),
-           os.path.join(CSRC, "sha256.h")]
+           os.path.join(CSRC, "sha256.h"), os.path.join(CSRC, "cache_row.cuh")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                    "-Xptxas", "-v", "--expt-relaxed-constexpr"]

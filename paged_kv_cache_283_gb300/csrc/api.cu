@@ -469,3 +469,134 @@ pa_status pa_decode_splitk_fp8(float* ws_out, float* ws_m, float* ws_l, int max_
 }
 
 }  // extern "C"
+
+namespace {
+
+// pa_decode_step*: the cache write of each sequence's new token and its
+// attention in one launch (kv: 0 bf16, 1 INT8, 2 FP8).
+pa_status decode_step_impl(void* out, const void* q, const void* key, const void* value,
+                           const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                           float* k_scales, float* v_scales, const int32_t* block_tables,
+                           int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, float scale, int partition_size, float* ws_out,
+                           float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
+                           int kv, pa_stream_t stream) {
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale);
+  if (s != PA_OK) return s;
+  const bool write = key != nullptr || value != nullptr || slot_mapping != nullptr;
+  const bool split = partition_size != 0;
+  if (partition_size < 0 || (split && (partition_size % block_size != 0 || max_partitions <= 0 ||
+                                       max_partitions > 65535)))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  if (!ok_ptr(out, 16)) return PA_ERR_INVALID_ARG;
+  if (write && (!ok_ptr(key, 16) || !ok_ptr(value, 16) || !ok_ptr(slot_mapping, 8)))
+    return PA_ERR_INVALID_ARG;
+  if (split && (!ok_ptr(ws_out, 16) || !ok_ptr(ws_m, 4) || !ok_ptr(ws_l, 4) ||
+                !ok_ptr(counters, 4)))
+    return PA_ERR_INVALID_ARG;
+  if (kv != 0 && (!ok_ptr(k_scales, 16) || !ok_ptr(v_scales, 16))) return PA_ERR_INVALID_ARG;
+  DecodeParams p = make_decode_params(q, kv ? nullptr : k_cache, kv ? nullptr : v_cache,
+                                      block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                      num_q_heads, num_kv_heads, num_blocks, scale);
+  if (kv != 0) {
+    p.k8 = static_cast<const int8_t*>(k_cache);
+    p.v8 = static_cast<const int8_t*>(v_cache);
+    p.k_scales = k_scales;
+    p.v_scales = v_scales;
+    p.fp8 = kv == 2;
+  }
+  p.out = static_cast<__nv_bfloat16*>(out);
+  if (write) {
+    p.new_key = static_cast<const __nv_bfloat16*>(key);
+    p.new_value = static_cast<const __nv_bfloat16*>(value);
+    p.slot_mapping = slot_mapping;
+  }
+  // Up to kMergeInKernelParts partitions per sequence are merged by the last
+  // CTA of each (sequence, KV head); beyond that one CTA's merge would sit on
+  // the critical path of the launch's tail, and the merge runs as its own
+  // launch (pa_splitk_reduce's kernel) over all SMs instead.
+  constexpr int kMergeInKernelParts = 16;
+  const bool merge_apart = split && max_partitions > kMergeInKernelParts;
+  if (split) {
+    p.ws_o = ws_out;
+    p.ws_m = ws_m;
+    p.ws_l = ws_l;
+    p.counters = merge_apart ? nullptr : counters;
+    p.max_partitions = max_partitions;
+    p.partition_blocks = partition_size / block_size;
+  } else {
+    p.max_partitions = 1;
+    p.partition_blocks = max_blocks_per_seq;
+  }
+  p.err = device_error_word();
+  if (!p.err) return cuda_fail(cudaGetLastError());
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, split, st);
+  if (e == cudaSuccess && merge_apart) {
+    ReduceParams r{};
+    r.out = p.out;
+    r.ws_o = ws_out;
+    r.ws_m = ws_m;
+    r.ws_l = ws_l;
+    r.context_lens = context_lens;
+    r.err = p.err;
+    r.num_seqs = num_seqs;
+    r.num_q_heads = num_q_heads;
+    r.max_partitions = max_partitions;
+    r.partition_size = partition_size;
+    e = launch_splitk_reduce(r, head_dim, st);
+  }
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value,
+                         const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                         const int32_t* block_tables, int max_blocks_per_seq,
+                         const int32_t* context_lens, int num_seqs, int num_q_heads,
+                         int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                         float scale, int partition_size, float* ws_out, float* ws_m,
+                         float* ws_l, unsigned* counters, int max_partitions,
+                         pa_stream_t stream) {
+  return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, nullptr, nullptr,
+                          block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                          num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                          ws_out, ws_m, ws_l, counters, max_partitions, 0, stream);
+}
+
+pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const void* value,
+                              const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
+                              float* k_scales, float* v_scales, const int32_t* block_tables,
+                              int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, float scale, int partition_size, float* ws_out,
+                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
+                              pa_stream_t stream) {
+  return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, k_scales, v_scales,
+                          block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                          num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                          ws_out, ws_m, ws_l, counters, max_partitions, 1, stream);
+}
+
+pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const void* value,
+                             const int64_t* slot_mapping, uint8_t* k_cache, uint8_t* v_cache,
+                             float* k_scales, float* v_scales, const int32_t* block_tables,
+                             int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, float scale, int partition_size, float* ws_out,
+                             float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
+                             pa_stream_t stream) {
+  return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, k_scales, v_scales,
+                          block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                          num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
+                          ws_out, ws_m, ws_l, counters, max_partitions, 2, stream);
+}
+
+}  // extern "C"

@@ -37,6 +37,7 @@
 
 #include <atomic>
 
+#include "cache_row.cuh"
 #include "decode_tile.cuh"
 #include "device.cuh"
 #include "internal.h"
@@ -103,10 +104,129 @@ struct SmemLayout {
   // int8 cache: the CTA's quantised q, codes [G][D] then scales [G]
   static constexpr int QOFF = NW * WARP;
   static constexpr int QREG = I8 ? ((G * D + G * 4 + 127) / 128) * 128 : 0;
-  static constexpr int TOTAL = NW * WARP + QREG;
+  // fused decode step: the new row staged for the patch (bf16: K and V rows;
+  // 1-byte: K codes, V codes, the two scales)
+  static constexpr int PATCHOFF = NW * WARP + QREG;
+  static constexpr int PATCH = 4 * D + 32;
+  static constexpr int TOTAL = PATCHOFF + PATCH;
   static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
   static_assert(STAGE % 16 == 0 && KT % 16 == 0, "bulk copy sizes");
 };
+// Fused decode step: the new token of sequence b (position ctx - 1) goes to
+// its slot, K and V rows of KV head kvh.  Called by the one warp that will
+// read that position (the warp owning the sequence's last block, in the CTA
+// whose range holds it).  The rows go to the pool with plain stores, and a
+// copy of them (for the 1-byte caches: the codes and scales as stored) goes
+// to `stage` in shared memory: the warp patches them into its tile once the
+// tile's own copy of that block has landed, so nothing waits for the stores
+// (the copy may read the old or the new row; either is overwritten).  The
+// slot must be the one the block table gives for that position, since any
+// other slot could be read by another CTA while it is written: otherwise
+// nothing is written and PA_DEVERR_SLOT is raised.  Negative slots are
+// padding.  Returns whether the row was written (then the tile needs the
+// patch).  The pools are held const in the parameters for the readers; this
+// is their one writer.
+template <int D, int Q>
+__device__ __forceinline__ bool fused_cache_write(const DecodeParams& p, int b, int kvh, int ctx,
+                                                  const int32_t* tbl, int lane,
+                                                  unsigned char* stage) {
+  const int64_t slot = __ldg(p.slot_mapping + b);
+  const size_t src = (static_cast<size_t>(b) * p.num_kv_heads + kvh) * D;
+  constexpr int C = D / 8;  // 16-byte chunks of a bf16 row
+  uint4 x = make_uint4(0, 0, 0, 0);
+  uint32_t kw[D / 64], vw[D / 64];
+  if constexpr (Q == 0) {  // lanes [0, C) hold K chunks, [C, 2C) V chunks
+    if (lane < 2 * C)
+      x = __ldg(reinterpret_cast<const uint4*>((lane >= C ? p.new_value : p.new_key) + src) +
+                (lane % C));
+  } else {
+    load_row_words<D>(p.new_key + src, lane, kw);
+    load_row_words<D>(p.new_value + src, lane, vw);
+  }
+  if (slot < 0) return false;
+  int64_t want = -1;
+  if (ctx >= 1) {
+    const int id = __ldg(tbl + (ctx - 1) / kBlockSize);
+    if (id >= 0 && id < p.num_blocks)
+      want = static_cast<int64_t>(id) * kBlockSize + (ctx - 1) % kBlockSize;
+  }
+  if (slot != want) {
+    if (lane == 0) raise_error(p.err, PA_DEVERR_SLOT);
+    return false;
+  }
+  const int off = static_cast<int>(slot % kBlockSize);
+  const int64_t srow = ((slot / kBlockSize) * p.num_kv_heads + kvh) * kBlockSize + off;
+  if constexpr (Q == 0) {
+    if (lane < 2 * C) {
+      __nv_bfloat16* dst =
+          const_cast<__nv_bfloat16*>(lane >= C ? p.v_cache : p.k_cache) + srow * D;
+      reinterpret_cast<uint4*>(dst)[lane % C] = x;
+      reinterpret_cast<uint4*>(stage)[lane] = x;  // [K row | V row]
+    }
+  } else {
+    constexpr int PER = D / 32;
+    float ks, vs;
+    const uint32_t kc = quantise_row<D, Q == 2>(kw, &ks);
+    const uint32_t vc = quantise_row<D, Q == 2>(vw, &vs);
+    int8_t* k8 = const_cast<int8_t*>(p.k8) + srow * D;
+    int8_t* v8 = const_cast<int8_t*>(p.v8) + srow * D;
+    const int vcol = v_code_col<D>(off, lane * PER);
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint32_t*>(k8 + lane * PER) = kc;
+      *reinterpret_cast<uint32_t*>(v8 + vcol) = vc;
+      *reinterpret_cast<uint32_t*>(stage + lane * PER) = kc;      // K codes
+      *reinterpret_cast<uint32_t*>(stage + D + lane * PER) = vc;  // V codes, logical order
+    } else {
+      *reinterpret_cast<uint16_t*>(k8 + lane * PER) = static_cast<uint16_t>(kc);
+      *reinterpret_cast<uint16_t*>(v8 + vcol) = static_cast<uint16_t>(vc);
+      *reinterpret_cast<uint16_t*>(stage + lane * PER) = static_cast<uint16_t>(kc);
+      *reinterpret_cast<uint16_t*>(stage + D + lane * PER) = static_cast<uint16_t>(vc);
+    }
+    if (lane == 0) {
+      const_cast<float*>(p.k_scales)[srow] = ks;
+      const_cast<float*>(p.v_scales)[srow] = vs;
+      reinterpret_cast<float*>(stage + 2 * D)[0] = ks;
+      reinterpret_cast<float*>(stage + 2 * D)[1] = vs;
+    }
+  }
+  return true;
+}
+
+// Patches the staged new row (fused_cache_write) into row `off` of a landed
+// tile: K tile, V tile, and for the 1-byte caches the two scales.  The stage
+// holds the 1-byte V codes in logical order; the tile, as stored.
+template <int D, int Q>
+__device__ __forceinline__ void patch_tile(unsigned char* tile, int kt_bytes,
+                                           const unsigned char* stage, int off, int lane) {
+  if constexpr (Q == 0) {
+    constexpr int C = D / 8;
+    if (lane < 2 * C)
+      reinterpret_cast<uint4*>(tile + (lane >= C ? kt_bytes : 0) + off * D * 2)[lane % C] =
+          reinterpret_cast<const uint4*>(stage)[lane];
+  } else {
+    constexpr int PER = D / 32;
+    // the lane's PER codes of the K row, and of the V row at their stored place
+    // (v_code_col may move them into the neighbouring row's bytes at D = 64)
+    const int vcol = v_code_col<D>(off, lane * PER);
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint32_t*>(tile + off * D + lane * PER) =
+          *reinterpret_cast<const uint32_t*>(stage + lane * PER);
+      *reinterpret_cast<uint32_t*>(tile + kt_bytes + off * D + vcol) =
+          *reinterpret_cast<const uint32_t*>(stage + D + lane * PER);
+    } else {
+      *reinterpret_cast<uint16_t*>(tile + off * D + lane * PER) =
+          *reinterpret_cast<const uint16_t*>(stage + lane * PER);
+      *reinterpret_cast<uint16_t*>(tile + kt_bytes + off * D + vcol) =
+          *reinterpret_cast<const uint16_t*>(stage + D + lane * PER);
+    }
+    if (lane == 0) {
+      float* sc = reinterpret_cast<float*>(tile + 2 * kt_bytes);  // 16 K then 16 V scales
+      sc[off] = reinterpret_cast<const float*>(stage + 2 * D)[0];
+      sc[kBlockSize + off] = reinterpret_cast<const float*>(stage + 2 * D)[1];
+    }
+  }
+}
+
 // Q: the cache's element type: 0 = bf16, 1 = INT8, 2 = FP8 (E4M3).  INT8 and
 // FP8 share the 1-byte-code tile layout (codes + per-token scales) and the
 // tensor-core PV; INT8 quantises q and takes QK in integers, FP8 takes QK on
@@ -272,11 +392,34 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   const int nblk = (ctx + BS - 1) / BS;
   int jb = 0, je = nblk;
   const int pidx = part;  // partition this CTA computes
+  // partitions of this sequence that have a CTA (split-K)
+  const int nparts = SPLIT ? min((nblk + p.partition_blocks - 1) / p.partition_blocks,
+                                 p.max_partitions)
+                           : 1;
+  // Fused cache write: done by the warp that reads position ctx - 1 (the
+  // owner of the sequence's last block, in the CTA whose range holds it),
+  // once its first copies are out; it patches its tile with the new row at
+  // iteration patch_it.
+  const bool writer_cta = p.slot_mapping != nullptr &&
+                          (!SPLIT || part == (nblk > 0 ? (nblk - 1) / p.partition_blocks : 0));
+  const int last_blk = nblk > 0 ? nblk - 1 - (SPLIT ? static_cast<int>(part_first) : 0) : 0;
   if constexpr (SPLIT) {
     if (part == 0 && threadIdx.x == 0 &&
         (nblk + p.partition_blocks - 1) / p.partition_blocks > p.max_partitions)
       raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
-    if (part_first >= nblk) return;  // past the end of this sequence; CTA-uniform, nothing issued
+    if (part_first >= nblk) {  // past the end of this sequence; CTA-uniform, nothing issued
+      if (writer_cta && threadIdx.x == 0 && __ldg(p.slot_mapping + b) >= 0)
+        raise_error(p.err, PA_DEVERR_SLOT);  // a new token for an empty sequence
+      if (p.counters != nullptr && nblk == 0 && part == 0) {
+        // merged output of an empty sequence: zeros, as the merge gives
+        for (int idx = threadIdx.x; idx < G * (D / 8); idx += NW * 32) {
+          const int hq = kvh * G + idx / (D / 8);
+          *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(b) * p.num_q_heads + hq) * D +
+                                    (idx % (D / 8)) * 8) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      return;
+    }
     jb = static_cast<int>(part_first);
     je = min(nblk, jb + p.partition_blocks);
   }
@@ -364,6 +507,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i);
+  int patch_it = -1;
+  if (writer_cta && warp == last_blk % NW &&
+      fused_cache_write<D, Q>(p, b, kvh, ctx, tbl, lane, smem + Lay::PATCHOFF))
+    patch_it = last_blk / NW;
 
   int consumed = 0;
   for (int i = 0; i < nw; ++i) {
@@ -373,6 +520,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     const int j = jb + warp + i * NW;
     const int nvalid = min(BS, ctx - j * BS);
     const unsigned char* stage = tiles + st * Lay::STAGE;
+    if (i == patch_it) {  // the new token's row (fused decode step)
+      patch_tile<D, Q>(tiles + st * Lay::STAGE, Lay::KT, smem + Lay::PATCHOFF, nvalid - 1, lane);
+      __syncwarp();
+    }
     if constexpr (!I8) {
       const uint4* kt = reinterpret_cast<const uint4*>(stage);
       const uint4* vt = reinterpret_cast<const uint4*>(stage + Lay::KT);
@@ -408,6 +559,18 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   // Only after a timed-out wait: let copies still in flight land (bounded)
   // before this CTA's shared memory can be reused.
   for (int i = consumed; i < issued; ++i) mbar_wait_bounded(&bars[i % S], (i / S) & 1, p.err);
+
+  // In-kernel split-K merge: count this CTA in now (the count's round trip
+  // overlaps the merge of the warps below).  Counter word: arrivals in the
+  // low 16 bits, partitions published in the high 16 bits.
+  const bool merging = SPLIT && p.counters != nullptr && nparts > 1;
+  unsigned* cnt = merging ? p.counters + static_cast<size_t>(b) * p.num_kv_heads + kvh : nullptr;
+  unsigned arrival = 0;
+  if (merging && threadIdx.x == 0)
+    asm volatile("atom.relaxed.gpu.global.add.u32 %0, [%1], 1;"
+                 : "=r"(arrival)
+                 : "l"(cnt)
+                 : "memory");
 
   // Per-warp totals: l over the lanes of each head, acc over row groups.
   if constexpr (Q == 2) {
@@ -474,6 +637,9 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   }
   __syncthreads();
 
+  // A merged split-K launch whose sequence has one partition writes the
+  // output directly (the merge of one partition is the identity).
+  const bool direct = !SPLIT || (p.counters != nullptr && nparts == 1);
   for (int idx = threadIdx.x; idx < G * (D / 8); idx += NW * 32) {
     const int g = idx / (D / 8);
     const int d0 = (idx % (D / 8)) * 8;
@@ -507,7 +673,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       for (int k = 0; k < 8; ++k) o[k] *= inv;
     }
     const int hq = kvh * G + g;
-    if constexpr (SPLIT) {
+    if (SPLIT && !direct) {
       const size_t row =
           (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions + pidx;
       float4* dst = reinterpret_cast<float4*>(p.ws_o + row * D + d0);
@@ -524,6 +690,79 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       *reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(b) * p.num_q_heads + hq) * D + d0) =
           *reinterpret_cast<const uint4*>(h);
     }
+  }
+
+  if constexpr (SPLIT) {
+    if (!merging) return;
+    // Every CTA but the last to arrive publishes its rows (a release on the
+    // counter) and leaves; the last waits until all the others have
+    // published -- they arrived before it, so they are running and finish
+    // without waiting on anything -- then merges all partitions by the
+    // log-sum-exp identity (as pa_splitk_reduce) and zeroes the counter for
+    // the next launch.  The wait is bounded like every other.
+    __shared__ unsigned s_last;
+    __syncthreads();  // every thread's workspace rows are written
+    if (threadIdx.x == 0) {
+      if ((arrival & 0xFFFFu) + 1u != static_cast<unsigned>(nparts)) {
+        asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(cnt), "r"(0x10000u)
+                     : "memory");
+        s_last = 0u;
+      } else {
+        const uint64_t t0 = global_timer_ns();
+        bool ok = true;
+        for (;;) {
+          unsigned v;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+          if ((v >> 16) + 1u >= static_cast<unsigned>(nparts)) break;
+          if (global_timer_ns() - t0 > 2000000000ull) {
+            raise_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
+            ok = false;
+            break;
+          }
+          __nanosleep(64);
+        }
+        s_last = ok ? 1u : 0u;
+      }
+    }
+    __syncthreads();
+    if (!s_last) return;
+    for (int idx = threadIdx.x; idx < G * (D / 4); idx += NW * 32) {
+      const int hq = kvh * G + idx / (D / 4);
+      const int d0 = (idx % (D / 4)) * 4;
+      const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions;
+      // one pass, rescaling to the running maximum (natural-log units)
+      float M = -INFINITY, Ls = 0.f;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i = 0; i < nparts; ++i) {
+        const float m = __ldcg(p.ws_m + row0 + i);
+        const float l = __ldcg(p.ws_l + row0 + i);
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (row0 + i) * D + d0));
+        if (m > M) {
+          const float c = expf(M - m);  // 0 on the first partition
+          Ls *= c;
+          a.x *= c;
+          a.y *= c;
+          a.z *= c;
+          a.w *= c;
+          M = m;
+        }
+        const float w = l * expf(m - M);
+        Ls += w;
+        a.x += w * o.x;
+        a.y += w * o.y;
+        a.z += w * o.z;
+        a.w += w * o.w;
+      }
+      const float inv = 1.0f / Ls;  // every partition has a token: Ls >= 1
+      const __nv_bfloat162 h0 = __float22bfloat162_rn(make_float2(a.x * inv, a.y * inv));
+      const __nv_bfloat162 h1 = __float22bfloat162_rn(make_float2(a.z * inv, a.w * inv));
+      uint2 packed;
+      packed.x = *reinterpret_cast<const uint32_t*>(&h0);
+      packed.y = *reinterpret_cast<const uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * p.num_q_heads + hq) * D + d0) =
+          packed;
+    }
+    if (threadIdx.x == 0) *cnt = 0u;
   }
 }
 

@@ -126,6 +126,13 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, unsign
 // finished and its writes are visible), so the result is the same as with
 // plain stream order whatever the previous kernel is.  griddep_launch_dependents()
 // lets the next kernel be scheduled as soon as this grid has started.
+// Orders this thread's earlier generic-proxy writes to global memory before
+// its (and, after a barrier, the CTA's) later asynchronous-proxy accesses,
+// such as bulk copies reading what was just written.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

@@ -36,6 +36,13 @@ struct DecodeParams {
   int max_partitions;    // split-K only
   int partition_blocks;  // split-K only: blocks per partition
   float scale_log2;      // scale * log2(e): scores are kept in base-2 units
+  // Fused decode step (pa_decode_step*), null when off.  The pools above are
+  // then written as well (the CTA reading each new token's position writes
+  // that token's K and V rows first).
+  const __nv_bfloat16* new_key;    // [B, Hkv, D]: each sequence's new token
+  const __nv_bfloat16* new_value;
+  const int64_t* slot_mapping;     // [B]: the slot of position context_lens[b] - 1, or < 0
+  unsigned* counters;              // split-K: [B, Hkv] arrivals; the last CTA merges
 };
 
 struct ReduceParams {

@@ -55,6 +55,12 @@ SIGNATURES = {
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
                               _i, _i, _f, _i, _vp]),
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
+    "pa_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
+                            _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+    "pa_decode_step_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                 _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+    "pa_decode_step_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
     "pa_decode_splitk_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _i, _vp]),
     "pa_prefill_supported": (_i, [_i, _i, _i]),
@@ -333,6 +339,76 @@ def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device))
 
 
+def step_counters(num_seqs, num_kv_heads, device="cuda"):
+    """Zeroed arrival counters [num_seqs * num_kv_heads] for a split-K pa_decode_step."""
+    torch = _torch()
+    return torch.zeros(num_seqs * num_kv_heads, dtype=torch.int32, device=device)
+
+
+def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
+               slot_mapping, partition_size, workspace, counters, k_scales, v_scales):
+    """(C function, argument tuple without the stream) for pa_decode_step*."""
+    torch = _torch()
+    fp8 = k_cache.dtype == torch.uint8
+    one = fp8 or k_cache.dtype == torch.int8
+    if one:
+        if k_scales is None or v_scales is None:
+            raise ValueError("pa_decode_step: a 1-byte cache needs k_scales and v_scales")
+        (pq, pk, pv, pks, pvs, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_int8_common(
+            q, k_cache, v_cache, k_scales, v_scales, block_tables, context_lens, fp8)
+        pools = (pk, pv, pks, pvs)
+    else:
+        (pq, pk, pv, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_common(
+            q, k_cache, v_cache, block_tables, context_lens)
+        pools = (pk, pv)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode_step: out must match q")
+    none = ctypes.c_void_p(None)
+    if key is None and value is None and slot_mapping is None:
+        kvs = (none, none, none)
+    elif key is None or value is None or slot_mapping is None:
+        raise ValueError("pa_decode_step: key, value and slot_mapping go together")
+    else:
+        if key.shape != (B, hkv, d) or value.shape != key.shape or slot_mapping.shape != (B,):
+            raise ValueError("pa_decode_step: key / value [B, Hkv, D], slot_mapping [B]")
+        kvs = (_dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3),
+               _dev(slot_mapping, torch.int64, "slot_mapping", 1))
+    ps = int(partition_size)
+    if ps > 0:
+        if workspace is None or counters is None:
+            raise ValueError("pa_decode_step: split-K needs a workspace and counters")
+        ws_o, ws_m, ws_l = workspace
+        maxp = ws_m.shape[2]
+        if ws_o.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape or \
+                ws_m.shape[:2] != (B, hq) or counters.shape != (B * hkv,):
+            raise ValueError("pa_decode_step: workspace / counters shapes")
+        wsa = (_dev(ws_o, torch.float32, "ws_out", 4), _dev(ws_m, torch.float32, "ws_m", 3),
+               _dev(ws_l, torch.float32, "ws_l", 3), _dev(counters, torch.int32, "counters", 1),
+               maxp)
+    else:
+        wsa = (none, none, none, none, 0)
+    fn = lib().pa_decode_step_fp8 if fp8 else (lib().pa_decode_step_int8 if one
+                                                else lib().pa_decode_step)
+    args = (_dev(out, torch.bfloat16, "out", 3), pq) + kvs + pools + (
+        pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), ps) + wsa
+    return fn, args
+
+
+def pa_decode_step(out, q, k_cache, v_cache, block_tables, context_lens, scale, key=None,
+                   value=None, slot_mapping=None, partition_size=512, workspace=None,
+                   counters=None, k_scales=None, v_scales=None, stream=None):
+    """Cache write of each sequence's new token (key / value [B, Hkv, D] at
+    slot_mapping [B], which must be the slot of position context_lens[b] - 1)
+    and the decode, in one launch.  partition_size 0: whole-sequence CTAs;
+    > 0: split-K merged in the same launch (workspace = splitk_workspace(...),
+    counters = step_counters(...)).  The cache dtype picks bf16 / INT8 (int8)
+    / FP8 (uint8 codes, with k_scales / v_scales)."""
+    fn, args = _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key,
+                          value, slot_mapping, partition_size, workspace, counters, k_scales,
+                          v_scales)
+    _check(fn(*args, _stream(stream)), "pa_decode_step")
+
+
 def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,
                              stream=None):
     """key/value [T, Hkv, D] bf16 quantised into FP8 (E4M3) pools (uint8 codes) + fp32 scales."""
@@ -442,7 +518,10 @@ def pa_plan_step(budget, num_decodes, prefill_remaining):
 class DecodeStep:
     """One decode step of one layer on fixed device buffers: the cache write
     of the batch's new tokens, then paged attention (split-K pass + merge, or
-    the whole-sequence kernel).
+    the whole-sequence kernel).  fused=True (the default) makes it one
+    pa_decode_step launch (each slot must then be its sequence's position
+    context_lens[b] - 1); fused=False, the separate cache-write, partition
+    and merge launches.
 
     Every argument is checked and marshalled once, here; each call then makes
     two or three bare C calls, which keeps the host ahead of the GPU when a
@@ -454,8 +533,30 @@ class DecodeStep:
     def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                  context_lens, out, scale, split=True, partition_size=512,
                  max_context_len=None, workspace=None, stream=None, k_scales=None,
-                 v_scales=None):
+                 v_scales=None, fused=True, counters=None):
         torch = _torch()
+        self.fused = bool(fused)
+        if self.fused:
+            # one pa_decode_step* launch: write + attention (+ merge)
+            self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+            self.split = bool(split)
+            B, hq, d = q.shape
+            hkv = k_cache.shape[1]
+            if self.split:
+                if workspace is None:
+                    mc = (int(max_context_len) if max_context_len is not None
+                          else block_tables.shape[1] * k_cache.shape[2])
+                    workspace = splitk_workspace(B, hq, d, mc, partition_size, q.device)
+                if counters is None:
+                    counters = step_counters(B, hkv, q.device)
+            self.workspace, self.counters = workspace, counters
+            self._fn, self._args = _step_args(
+                out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
+                slot_mapping, partition_size if self.split else 0, workspace, counters,
+                k_scales, v_scales)
+            self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables,
+                          context_lens, out, workspace, counters, k_scales, v_scales]
+            return
         T, hkv, d = key.shape
         nb, hkv2, bs, d2 = k_cache.shape
         if value.shape != key.shape or v_cache.shape != k_cache.shape or (hkv, d) != (hkv2, d2):
@@ -516,6 +617,11 @@ class DecodeStep:
 
     def __call__(self, stream=None):
         s = self._stream if stream is None and self._stream is not None else _stream(stream)
+        if self.fused:
+            st = self._fn(*self._args, s)
+            if st != PA_OK:
+                _check(st, "DecodeStep: pa_decode_step")
+            return
         st = self._f_write(*self._rc, s)
         if st != PA_OK:
             _check(st, "DecodeStep: cache write")

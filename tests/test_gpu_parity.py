@@ -363,8 +363,9 @@ def test_splitk_schedule_mixes(split):
     _assert_no_device_error()
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("split", [False, True])
-def test_decode_step_object_matches_oracle(split):
+def test_decode_step_object_matches_oracle(split, fused):
     # pa.DecodeStep: the same cache write + attention with pre-marshalled
     # calls; called twice with new inputs written into the same buffers
     w = I.random_case(777, 6, [300, 17, 1, 2049, 512, 96], 32, 8, 128)
@@ -374,7 +375,8 @@ def test_decode_step_object_matches_oracle(split):
     slots, bt, ctx = _dev_i64(sl_p), _dev_i32(bt_p), _dev_i32(w.context_lens)
     out = torch.empty_like(q)
     step = pa.DecodeStep(key, val, kc, vc, slots, q, bt, ctx, out, w.scale, split=split,
-                         partition_size=256, max_context_len=int(w.context_lens.max()))
+                         partition_size=256, max_context_len=int(w.context_lens.max()),
+                         fused=fused)
     kc_o, vc_o = w.k_cache.copy(), w.v_cache.copy()
     rng = np.random.default_rng(778)
     for it in range(2):
@@ -390,5 +392,5 @@ def test_decode_step_object_matches_oracle(split):
         torch.cuda.synchronize()
         kc_o, vc_o = OC.reshape_and_cache(nk, nv, kc_o, vc_o, sl_m, 16, inplace=True)
         ref = OA.decode(nq, kc_o, vc_o, bt_m, w.context_lens, w.scale, 16)
-        assert_close(bf16_to_f64(out), ref, f"DecodeStep split={split} call {it}")
+        assert_close(bf16_to_f64(out), ref, f"DecodeStep split={split} fused={fused} call {it}")
     _assert_no_device_error()

@@ -1,0 +1,233 @@
+"""The fused decode step (pa_decode_step, _int8, _fp8: cache write + decode +
+split-K merge in one launch) against the float64 oracle: the pools after the
+call bit-exact against the oracle's cache write, the outputs within the
+parity tolerance of the oracle's decode over the written cache.  Also: padding
+slots, empty sequences, a slot that is not its sequence's position (refused,
+PA_DEVERR_SLOT), attention without a write, the arrival counters left at zero,
+and repeated calls."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+from oracle import attention as OA
+from oracle import cache as OC
+from oracle import fp8 as OF
+from oracle import quant as OQ
+from paged_kv_cache_283_gb300 import inputs as I
+from paged_kv_cache_283_gb300 import pa
+
+from gpu_helpers import assert_close, bf16_to_f64, both_tables, dev_bf16, host_bits, \
+    swizzle_v_int8
+
+pytestmark = pytest.mark.gpu
+
+
+def _i32(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).cuda()
+
+
+def _i64(a):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int64)).cuda()
+
+
+class _Case:
+    """One workload on both sides: oracle pools (numpy) and device pools."""
+
+    def __init__(self, w, kv):
+        self.w, self.kv = w, kv
+        self.bt_m, self.sl_m, self.bt_p, self.sl_p = both_tables(w)
+        if kv == "bf16":
+            self.host = [w.k_cache.copy(), w.v_cache.copy()]
+            self.dev = [dev_bf16(w.k_cache), dev_bf16(w.v_cache)]
+        else:
+            quant = OF.quantize_fp8 if kv == "fp8" else OQ.quantize_int8
+            kq, ks = quant(w.k_cache)
+            vq, vs = quant(w.v_cache)
+            self.host = [kq, vq, ks, vs]
+            self.dev = [torch.from_numpy(kq).cuda(), torch.from_numpy(swizzle_v_int8(vq)).cuda(),
+                        torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()]
+
+    def oracle_write(self, key, val, slots):
+        w = self.w
+        if self.kv == "bf16":
+            self.host = list(OC.reshape_and_cache(key, val, self.host[0], self.host[1], slots,
+                                                  w.block_size))
+        else:
+            write = OF.reshape_and_cache_fp8 if self.kv == "fp8" else OQ.reshape_and_cache_int8
+            self.host = list(write(key, val, *self.host, slots, w.block_size))
+
+    def oracle_decode(self, q, ctx=None):
+        w = self.w
+        ctx = w.context_lens if ctx is None else ctx
+        if self.kv == "bf16":
+            return OA.decode(q, self.host[0], self.host[1], self.bt_m, ctx, w.scale,
+                             w.block_size)
+        dec = OF.decode_fp8 if self.kv == "fp8" else OQ.decode_int8
+        return dec(q, *self.host, self.bt_m, ctx, w.scale, w.block_size)
+
+    def device_pools(self):
+        """Device pools in the oracle's (logical) layout, for bit comparison."""
+        if self.kv == "bf16":
+            return [host_bits(self.dev[0]), host_bits(self.dev[1])]
+        return [self.dev[0].cpu().numpy(), swizzle_v_int8(self.dev[1].cpu().numpy()),
+                self.dev[2].cpu().numpy(), self.dev[3].cpu().numpy()]
+
+    def run(self, q, key, val, slots, split, ctx=None, counters=None, workspace=None):
+        w = self.w
+        out = torch.empty_like(q)
+        ctx_d = _i32(w.context_lens if ctx is None else ctx)
+        kw = {}
+        if self.kv != "bf16":
+            kw = {"k_scales": self.dev[2], "v_scales": self.dev[3]}
+        if split:
+            if workspace is None:
+                workspace = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
+                                                max(1, int(w.context_lens.max())), split)
+            if counters is None:
+                counters = pa.step_counters(w.num_seqs, w.num_kv_heads)
+        pa.pa_decode_step(out, q, self.dev[0], self.dev[1], _i32(self.bt_p), ctx_d, w.scale,
+                          key=key, value=val, slot_mapping=slots, partition_size=split or 0,
+                          workspace=workspace, counters=counters, **kw)
+        torch.cuda.synchronize()
+        return out, counters
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
+@pytest.mark.parametrize("idx", [1, 2])
+@pytest.mark.parametrize("split", [0, 512, 128, 16])
+def test_fused_step_matches_oracle(kv, idx, split):
+    """split 512 and 128 (at most 16 partitions): merged in the launch; split
+    16 (up to 128 partitions): merged by a second launch."""
+    w = I.workload(idx)
+    c = _Case(w, kv)
+    pa.pa_clear_device_error()
+    out, counters = c.run(dev_bf16(w.q), dev_bf16(w.key), dev_bf16(w.value), _i64(c.sl_p), split)
+    c.oracle_write(w.key, w.value, c.sl_m)
+    for got, want in zip(c.device_pools(), c.host):
+        assert np.array_equal(got, want), "pool bytes after the fused cache write"
+    assert_close(bf16_to_f64(out), c.oracle_decode(w.q), f"fused {kv} workload {idx} split={split}")
+    if split:
+        assert int(counters.abs().sum().item()) == 0, "arrival counters left nonzero"
+    assert pa.pa_get_device_error() == 0
+
+
+EDGE = [1, 15, 16, 17, 33, 512, 513, 2112]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8", "fp8"])
+@pytest.mark.parametrize("d,hq,hkv", [(128, 32, 8), (128, 64, 8), (64, 4, 2)])
+@pytest.mark.parametrize("split", [0, 256, 64])
+def test_fused_step_edges(kv, d, hq, hkv, split):
+    """Edge contexts (one token, block and partition boundaries) with some
+    sequences' slots as padding (-1): those keep the pool's old row."""
+    w = I.random_case(6000 + d + hq, len(EDGE), EDGE, hq, hkv, d)
+    c = _Case(w, kv)
+    slots_m = c.sl_m.copy()
+    slots_m[[1, 5]] = -1
+    slots_p = c.sl_p.copy()
+    slots_p[[1, 5]] = -1
+    pa.pa_clear_device_error()
+    out, counters = c.run(dev_bf16(w.q), dev_bf16(w.key), dev_bf16(w.value), _i64(slots_p), split)
+    c.oracle_write(w.key, w.value, slots_m)
+    for got, want in zip(c.device_pools(), c.host):
+        assert np.array_equal(got, want)
+    assert_close(bf16_to_f64(out), c.oracle_decode(w.q), f"fused edges {kv} d={d} split={split}")
+    if split:
+        assert int(counters.abs().sum().item()) == 0
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("split", [0, 48])
+def test_fused_step_empty_sequences_and_no_write(split):
+    """Empty sequences give zeros; with no key / value / slots the call is a
+    plain decode and the pools are untouched."""
+    ctx = np.array([0, 40, 0, 200, 7], dtype=np.int32)
+    w = I.random_case(6100 + split, len(ctx), np.maximum(ctx, 1), 16, 4, 128)
+    c = _Case(w, "bf16")
+    before = [x.copy() for x in c.host]
+    pa.pa_clear_device_error()
+    out, counters = c.run(dev_bf16(w.q), None, None, None, split, ctx=ctx)
+    for got, want in zip(c.device_pools(), before):
+        assert np.array_equal(got, want), "a call without a write changed the pools"
+    ref = c.oracle_decode(w.q, ctx)
+    assert np.all(ref[ctx == 0] == 0)
+    assert_close(bf16_to_f64(out), ref, f"fused empty/no-write split={split}")
+    if split:
+        assert int(counters.abs().sum().item()) == 0
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("split", [0, 64])
+def test_fused_step_refuses_foreign_slot(split):
+    """A slot that is not its sequence's position n - 1 is not written and
+    raises PA_DEVERR_SLOT; the other sequences are unaffected."""
+    w = I.random_case(6200, 4, [100, 300, 17, 64], 32, 8, 128)
+    c = _Case(w, "bf16")
+    slots_p = c.sl_p.copy()
+    slots_m = c.sl_m.copy()
+    slots_p[2] = slots_p[0] + 1 if slots_p[0] % 16 != 15 else slots_p[0] - 1  # another position
+    slots_m[2] = -1  # the oracle: sequence 2's new token is not written
+    pa.pa_clear_device_error()
+    out, _ = c.run(dev_bf16(w.q), dev_bf16(w.key), dev_bf16(w.value), _i64(slots_p), split)
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_SLOT
+    pa.pa_clear_device_error()
+    c.oracle_write(w.key, w.value, slots_m)
+    for got, want in zip(c.device_pools(), c.host):
+        assert np.array_equal(got, want)
+    assert_close(bf16_to_f64(out), c.oracle_decode(w.q), f"foreign slot split={split}")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_fused_step_repeated_calls(kv):
+    """Three calls on the same buffers (counters and workspace reused): each
+    writes its token and attends over the cache as the oracle has it then."""
+    w = I.random_case(6300, 6, [300, 17, 1, 2049, 512, 96], 32, 8, 128)
+    c = _Case(w, kv)
+    ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()), 256)
+    counters = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    rng = np.random.default_rng(6301)
+    key, val, q = dev_bf16(w.key), dev_bf16(w.value), dev_bf16(w.q)
+    slots = _i64(c.sl_p)
+    pa.pa_clear_device_error()
+    for it in range(3):
+        nk, nv, nq = (w.key, w.value, w.q) if it == 0 else (
+            I.normal_bf16(rng, w.key.shape), I.normal_bf16(rng, w.value.shape),
+            I.normal_bf16(rng, w.q.shape))
+        key.copy_(dev_bf16(nk))
+        val.copy_(dev_bf16(nv))
+        q.copy_(dev_bf16(nq))
+        out, _ = c.run(q, key, val, slots, 256, counters=counters, workspace=ws)
+        c.oracle_write(nk, nv, c.sl_m)
+        assert_close(bf16_to_f64(out), c.oracle_decode(nq), f"fused {kv} call {it}")
+        assert int(counters.abs().sum().item()) == 0
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fused_step_long_context_matches_separate_kernels():
+    """The long-context workload (8K..128K tokens, up to 256 partitions, so
+    the merge is a second launch) against pa_decode_splitk + pa_splitk_reduce
+    on the same written cache (that path is pinned to the oracle elsewhere)."""
+    w = I.long_splitk()
+    bt_m, sl_m, bt_p, sl_p = both_tables(w)
+    kc, vc = dev_bf16(w.k_cache), dev_bf16(w.v_cache)
+    q, key, val = dev_bf16(w.q), dev_bf16(w.key), dev_bf16(w.value)
+    bt, ctx, slots = _i32(bt_p), _i32(w.context_lens), _i64(sl_p)
+    ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()), 512)
+    counters = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    pa.pa_clear_device_error()
+    out = torch.empty_like(q)
+    pa.pa_decode_step(out, q, kc, vc, bt, ctx, w.scale, key=key, value=val, slot_mapping=slots,
+                      partition_size=512, workspace=ws, counters=counters)
+    ref = torch.empty_like(q)
+    pa.pa_decode_splitk(*ws, q, kc, vc, bt, ctx, w.scale, partition_size=512)
+    pa.pa_splitk_reduce(ref, *ws, ctx, partition_size=512)
+    torch.cuda.synchronize()
+    a, b = out.float(), ref.float()
+    assert torch.all((a - b).abs() <= 2.0 ** -7 * b.abs() + 1e-6), "fused vs separate merge"
+    # and the written rows are the new tokens
+    kh = host_bits(kc)
+    for bi, si in enumerate(sl_p):
+        assert np.array_equal(kh[si // 16, :, si % 16], w.key[bi])
+    assert int(counters.abs().sum().item()) == 0
+    assert pa.pa_get_device_error() == 0
