@@ -550,6 +550,16 @@ def run_gpu(args):
     if attn == "auto":
         attn = "splitk" if args.workload in (2, 3, 5) else "decode"
     fused = args.step == "fused"
+    partition_choice = "given"
+    if args.partition is None:
+        if args.workload == 3:
+            args.partition = 512  # the long-context configuration fixes 512-token partitions
+            partition_choice = "fixed by the workload"
+        else:
+            args.partition = pa.splitk_partition_size(
+                w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, args.kv,
+                torch.cuda.get_device_properties(device).multi_processor_count)
+            partition_choice = "pa_splitk_partition_size (makespan model)"
     step, dominant, outs = _attn_fns(st, attn, args.partition, fused)
 
     # eager warmup (sets kernel attributes, checks the error word)
@@ -644,6 +654,8 @@ def run_gpu(args):
             "kv_cache": args.kv,
             "graph": "one CUDA graph per step (cache write + attention)",
             "step": args.step,
+            "partition": args.partition if attn == "splitk" else None,
+            "partition_choice": partition_choice if attn == "splitk" else None,
             "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
                   % (len(st["replicas"]), st["pool_bytes"] / 1e6, l2 / 1e6)
             if len(st["replicas"]) > 1 else "32 distinct per-layer pools per step",
@@ -1013,7 +1025,9 @@ def main(argv=None):
                     help="fused: one pa_decode_step launch per layer (cache write + attention "
                          "+ split-K merge); separate: the cache write, partition pass and "
                          "merge as three launches")
-    ap.add_argument("--partition", type=int, default=512)
+    ap.add_argument("--partition", type=int, default=None,
+                    help="split-K partition size in tokens (default: 512 for the long-context "
+                         "workload, else chosen by pa_splitk_partition_size)")
     ap.add_argument("--soak-seconds", type=float, default=0.5)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -416,6 +416,22 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
                      int num_blocks, float scale, pa_stream_t stream);
 
 /*
+ * Split-K partition size for a decode batch (host): the size, from {256, 384,
+ * 512, 640, 768, 1024, 1536, 2048, 4096} tokens, that minimises a model of the
+ * split-K launch's time -- its CTAs handed in grid order to the first free
+ * CTA slot (num_sms x the kernel's CTAs per SM), each costing a time per
+ * token, a fixed start-up and, for sequences of several partitions, a merge
+ * share -- with ties going to the larger size; a 1-byte cache (issue-bound
+ * kernels) whose batch has fewer (sequence, KV head) units than CTA slots
+ * takes 512.  context_lens: host int32
+ * [num_seqs]; kv_kind 0 = bf16 cache, 1 = INT8, 2 = FP8; num_sms the device's
+ * multiprocessor count.  Returns 0 on invalid arguments.  The result is a
+ * performance choice only: any partition size gives the same attention.
+ */
+int pa_splitk_partition_size(const int32_t* context_lens, int num_seqs, int num_q_heads,
+                             int num_kv_heads, int head_dim, int kv_kind, int num_sms);
+
+/*
  * Step planning for chunked prefill (host; "How LLM Inference Serving Works",
  * section "Chunked prefill").  Each step has a token budget
  * (max_num_batched_tokens): every pending decode (one token each) is taken

@@ -21,7 +21,7 @@ LIB = os.path.join(HERE, "libpa.so")
 
 SOURCES = ["api.cu", "decode.cu", "splitk_reduce.cu", "reshape_and_cache.cu", "copy_blocks.cu",
            "noalloc.cu", "prefill.cu", "allocator.cpp", "sha256.cpp",
-           "scheduler.cpp"]
+           "scheduler.cpp", "splitk_plan.cpp"]
 HEADERS = [os.path.join(ROOT, "include", "pa.h"), os.path.join(CSRC, "internal.h"),
            os.path.join(CSRC, "device.cuh"), os.path.join(CSRC, "decode_tile.cuh"),
            os.path.join(CSRC, "sha256.h"), os.path.join(CSRC, "cache_row.cuh")]

@@ -392,10 +392,6 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   const int nblk = (ctx + BS - 1) / BS;
   int jb = 0, je = nblk;
   const int pidx = part;  // partition this CTA computes
-  // partitions of this sequence that have a CTA (split-K)
-  const int nparts = SPLIT ? min((nblk + p.partition_blocks - 1) / p.partition_blocks,
-                                 p.max_partitions)
-                           : 1;
   // Fused cache write: done by the warp that reads position ctx - 1 (the
   // owner of the sequence's last block, in the CTA whose range holds it),
   // once its first copies are out; it patches its tile with the new row at
@@ -507,10 +503,11 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i);
-  int patch_it = -1;
-  if (writer_cta && warp == last_blk % NW &&
-      fused_cache_write<D, Q>(p, b, kvh, ctx, tbl, lane, smem + Lay::PATCHOFF))
-    patch_it = last_blk / NW;
+  // this warp patches its tile of the sequence's last block (the only
+  // block with ctx - j * BS <= BS)
+  const bool patch_row =
+      writer_cta && warp == last_blk % NW &&
+      fused_cache_write<D, Q>(p, b, kvh, ctx, tbl, lane, smem + Lay::PATCHOFF);
 
   int consumed = 0;
   for (int i = 0; i < nw; ++i) {
@@ -520,7 +517,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     const int j = jb + warp + i * NW;
     const int nvalid = min(BS, ctx - j * BS);
     const unsigned char* stage = tiles + st * Lay::STAGE;
-    if (i == patch_it) {  // the new token's row (fused decode step)
+    if (patch_row && nvalid == ctx - j * BS) {  // the new token's row (fused decode step)
       patch_tile<D, Q>(tiles + st * Lay::STAGE, Lay::KT, smem + Lay::PATCHOFF, nvalid - 1, lane);
       __syncwarp();
     }
@@ -560,6 +557,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   // before this CTA's shared memory can be reused.
   for (int i = consumed; i < issued; ++i) mbar_wait_bounded(&bars[i % S], (i / S) & 1, p.err);
 
+  // partitions of this sequence that have a CTA (split-K)
+  const int nparts = SPLIT ? min((nblk + p.partition_blocks - 1) / p.partition_blocks,
+                                 p.max_partitions)
+                           : 1;
   // In-kernel split-K merge: count this CTA in now (the count's round trip
   // overlaps the merge of the warps below).  Counter word: arrivals in the
   // low 16 bits, partitions published in the high 16 bits.

@@ -55,6 +55,7 @@ SIGNATURES = {
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
                               _i, _i, _f, _i, _vp]),
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
+    "pa_splitk_partition_size": (_i, [_vp, _i, _i, _i, _i, _i, _i]),
     "pa_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                             _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
     "pa_decode_step_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
@@ -337,6 +338,24 @@ def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition
     return (torch.empty((num_seqs, num_q_heads, maxp, head_dim), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device),
             torch.empty((num_seqs, num_q_heads, maxp), dtype=torch.float32, device=device))
+
+
+def splitk_partition_size(context_lens, num_q_heads, num_kv_heads, head_dim, kv="bf16",
+                          num_sms=None):
+    """The split-K partition size pa_splitk_partition_size chooses for a batch
+    (context_lens: host int array).  num_sms defaults to the current CUDA
+    device's multiprocessor count."""
+    import numpy as np
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    if num_sms is None:
+        torch = _torch()
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    kind = {"bf16": 0, "int8": 1, "fp8": 2}[kv]
+    r = lib().pa_splitk_partition_size(ctx.ctypes.data_as(ctypes.c_void_p), ctx.shape[0],
+                                       num_q_heads, num_kv_heads, head_dim, kind, int(num_sms))
+    if r <= 0:
+        raise ValueError("pa_splitk_partition_size: invalid arguments")
+    return int(r)
 
 
 def step_counters(num_seqs, num_kv_heads, device="cuda"):

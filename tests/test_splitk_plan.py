@@ -1,0 +1,105 @@
+"""pa_splitk_partition_size (host): the split-K partition size chosen for a
+decode batch by the launch-time model pa.h states.  The model is restated
+here in Python (CTAs in grid order onto the first free slot; per-token,
+per-CTA and merge costs; a second merge launch past 16 partitions) and the
+library's choice must equal the restatement's on varied batches; plus the
+properties any such choice has."""
+import ctypes
+import heapq
+
+import numpy as np
+import pytest
+
+from paged_kv_cache_283_gb300 import pa
+
+CANDIDATES = (256, 384, 512, 640, 768, 1024, 1536, 2048, 4096)
+TOKEN_US = {0: 0.025, 1: 0.019, 2: 0.019}
+CTA_US, MERGE_US, APART_US, IN_KERNEL_PARTS = 4.0, 2.0, 3.0, 16
+
+
+def _slots(num_sms, group, kind):
+    if kind == 0:
+        return num_sms * (3 if group <= 4 else 1)
+    return num_sms * (4 if group <= 4 else 3)
+
+
+def _makespan(ctx, hkv, part, slots, token_us):
+    nps = [max(0, -(-int(n) // part)) for n in ctx]
+    maxp = max([1] + nps)
+    apart = maxp > IN_KERNEL_PARTS
+    free = [0.0] * slots
+    for z in range(maxp):
+        for n, np_ in zip(ctx, nps):
+            if z >= max(np_, 1):
+                continue
+            tokens = max(0, min(part, int(n) - z * part))
+            d = token_us * tokens + CTA_US + (MERGE_US if (np_ > 1 and not apart) else 0.0)
+            for _ in range(hkv):
+                t = heapq.heappop(free)
+                heapq.heappush(free, t + d)
+    return max(free) + (APART_US if apart else 0.0)
+
+
+def _model_choice(ctx, hq, hkv, d, kind, num_sms):
+    slots = _slots(num_sms, hq // hkv, kind)
+    token_us = TOKEN_US[kind] * d / 128.0
+    if kind != 0 and len(ctx) * hkv < slots and -(-max(ctx) // 512) <= 65535:
+        return 512  # 1-byte caches with fewer units than slots
+    best, best_t = 0, 0.0
+    for part in CANDIDATES:
+        if -(-max(ctx) // part) > 65535:
+            continue
+        t = _makespan(ctx, hkv, part, slots, token_us)
+        if best == 0 or t <= best_t + 1e-9:
+            best, best_t = part, t
+        if part >= max(ctx):
+            break
+    return best
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_choice_equals_the_stated_model(seed):
+    rng = np.random.default_rng(seed)
+    kinds = ["bf16", "int8", "fp8"]
+    for _ in range(4):
+        b = int(rng.integers(1, 300))
+        hkv = int(rng.choice([2, 4, 8]))
+        hq = hkv * int(rng.choice([2, 4, 8]))
+        d = int(rng.choice([64, 128]))
+        kind = int(rng.integers(0, 3))
+        sms = int(rng.choice([132, 148, 152]))
+        shape = rng.choice(["uniform", "exp", "long"])
+        if shape == "uniform":
+            ctx = rng.integers(1, 4097, size=b)
+        elif shape == "exp":
+            ctx = np.clip(np.ceil(rng.exponential(600.0, size=b)), 1, 8192)
+        else:
+            ctx = rng.integers(1, 131073, size=max(1, b // 30))
+        ctx = ctx.astype(np.int32)
+        got = pa.splitk_partition_size(ctx, hq, hkv, d, kinds[kind], num_sms=sms)
+        assert got == _model_choice(ctx.tolist(), hq, hkv, d, kind, sms), (b, hq, hkv, d, kind)
+
+
+def test_choice_properties():
+    # one very long sequence: many partitions are needed to fill the GPU
+    assert pa.splitk_partition_size([131072], 32, 8, 128, num_sms=152) <= 1024
+    # many short sequences: one partition each is best (no split, no merge)
+    ctx = np.full(1024, 200, dtype=np.int32)
+    assert pa.splitk_partition_size(ctx, 32, 8, 128, num_sms=152) >= 200
+    # every answer is a candidate
+    rng = np.random.default_rng(1)
+    for _ in range(20):
+        ctx = rng.integers(1, 20000, size=int(rng.integers(1, 64))).astype(np.int32)
+        assert pa.splitk_partition_size(ctx, 32, 8, 128, num_sms=152) in CANDIDATES
+
+
+def test_invalid_arguments_return_zero():
+    f = pa.lib().pa_splitk_partition_size
+    ctx = np.array([100, 200], dtype=np.int32)
+    p = ctx.ctypes.data_as(ctypes.c_void_p)
+    assert f(None, 2, 32, 8, 128, 0, 152) == 0
+    assert f(p, 0, 32, 8, 128, 0, 152) == 0
+    assert f(p, 2, 30, 8, 128, 0, 152) == 0   # heads not divisible
+    assert f(p, 2, 32, 8, 128, 3, 152) == 0   # unknown cache kind
+    assert f(p, 2, 32, 8, 128, 0, 0) == 0
+    assert f(p, 2, 32, 8, 128, 0, 152) > 0
