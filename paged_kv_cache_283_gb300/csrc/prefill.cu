@@ -71,7 +71,7 @@ constexpr int kBar = kV + 2 * kStages * kHalf;  // mbarriers and the TMEM addres
 constexpr int kRed = kBar + 256;        // row maxima / sums of the two column halves
 constexpr int kSmemBytes = kRed + 2 * kRows * 4 + 1024;  // + alignment slack
 constexpr int kSoftmaxThreads = 256;    // two threads per row, 64 columns each
-constexpr int kThreads = kSoftmaxThreads + 64;  // + an MMA warp and a copy warp
+constexpr int kThreads = kSoftmaxThreads + 96;  // + an MMA warp and two copy warps
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -226,11 +226,12 @@ __device__ __forceinline__ void pair_sync(int warp) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
 }
 
-// grid (query tiles, KV heads, sequences), 320 threads.  Warps 0-7 run the
+// grid (query tiles, KV heads, sequences), 352 threads.  Warps 0-7 run the
 // softmax: thread t < 256 handles row t % 128 (TMEM lane; warps w and w + 4
 // share a lane quarter) and columns [64 h, 64 h + 64) of S and O, h = t / 128.
-// Warp 8 issues the MMAs (lane 0), warp 9 the copies (one block per lane), so
-// that neither chain waits on the other's latencies.
+// Warp 8 issues the MMAs (lane 0), warp 9 the Q and K copies and warp 10 the
+// V copies (one block per lane), so that no chain waits on another's
+// latencies.
 //
 // Tensor memory: S0, S1, S2 = columns [0, 384) in 128-column buffers, O =
 // [384, 512).  P of chunk c replaces S of chunk c in place (hi part in the
@@ -242,8 +243,8 @@ __device__ __forceinline__ void pair_sync(int warp) {
 //
 // MMA warp, per chunk c:  wait PV(c-2) (S[(c+1)%3] holds P(c-2)) and K(c+1):
 //   S[(c+1)%3] = Q K(c+1)^T; wait V(c) and P(c): O += P V(c).
-// Copy warp, per chunk c: wait K slot of c free: copy K(c+3); wait V slot of
-//   c-1 free: copy V(c+2).
+// Copy warps, per chunk c: wait K slot of c free: copy K(c+3) (K warp);
+//   wait V slot of c-1 free: copy V(c+2) (V warp).
 // Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
 //   exponentials; rescale O only if the reference maximum moved (after
 //   PV(c-1)); P into S[c%3]; arrive on p_ready[c%3].
@@ -315,8 +316,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kCopyWarp) {
+  if (warp >= kCopyWarp) {
     // ------------------------------------------------------------ copies
+    // Warp kCopyWarp copies Q and the K ring, warp kCopyWarp + 1 the V ring:
+    // a 32 KiB chunk is 16 tensor-map boxes whose issue takes ~1.6k cycles,
+    // so one warp issuing both rings paced the whole pipeline.
+    const bool vwarp = warp == kCopyWarp + 1;
     const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
     int last_k = -1, last_v = -1;  // last chunk copied into each ring (for the drain)
     bool ok = true;                // lane 0: every wait so far succeeded
@@ -348,41 +353,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (is_v) last_v = c; else last_k = c;
     };
     if (lane == 0) {
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tk)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tv)) : "memory");
-      mbar_arrive_expect_tx(q_full, 2 * kHalf);
-      tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
-      tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(vwarp ? &tv : &tk))
+                   : "memory");
+      if (!vwarp) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tq)) : "memory");
+        mbar_arrive_expect_tx(q_full, 2 * kHalf);
+        tma_3d(sm + kQ, &tq, 0, kvh * G, q0 + i0, q_full);
+        tma_3d(sm + kQ + kHalf, &tq, 64, kvh * G, q0 + i0, q_full);
+      }
     }
     {
       int ids[kStages];
 #pragma unroll
       for (int c = 0; c < kStages; ++c) ids[c] = fetch_id(c);
 #pragma unroll
-      for (int c = 0; c < kStages; ++c) {
-        if (c < nchunks) {
-          load(c, false, ids[c]);
-          load(c, true, ids[c]);
-        }
-      }
+      for (int c = 0; c < kStages; ++c)
+        if (c < nchunks) load(c, vwarp, ids[c]);
     }
-    int id_k = fetch_id(kStages);      // ids of the next K copy (chunk c + 3)
-    int id_v = 0;                      // ids of the next V copy (chunk c + 2)
-    for (int c = 0; c + 2 < nchunks && uniform(ok); ++c) {
-      if (c + 3 < nchunks) {  // QK(c) has read K stage c % 3
-        if (lane == 0) ok = mbar_wait_bounded(&k_free[c % kStages], (c / kStages) & 1, p.err);
-        if (!uniform(ok)) break;
-        load(c + 3, false, id_k);
-      }
-      if (c >= 1) {           // PV(c-1) has read V stage (c-1) % 3 = (c+2) % 3
-        if (lane == 0)
-          ok = mbar_wait_bounded(&v_free[(c - 1) % kStages], ((c - 1) / kStages) & 1, p.err);
-        if (!uniform(ok)) break;
-        load(c + 2, true, id_v);
-      }
-      id_v = id_k;            // chunk c + 3's V is copied next iteration
-      id_k = fetch_id(c + 4);
+    // Block ids run kIdAhead chunks ahead of the copies (idq[i]: the chunk
+    // i copies after the next), so that no copy waits on a table load.
+    constexpr int kIdAhead = 4;
+    int idq[kIdAhead];
+#pragma unroll
+    for (int i = 0; i < kIdAhead; ++i) idq[i] = fetch_id(kStages + i);
+    // K warp, iteration c: QK(c) has read K stage c % 3 -> copy K(c + 3).
+    // V warp, iteration c: PV(c - 1) has read V stage (c + 2) % 3 -> copy V(c + 2).
+    for (int c = vwarp ? 1 : 0; uniform(ok); ++c) {
+      const int next = vwarp ? c + 2 : c + 3;  // the chunk this iteration copies
+      if (next >= nchunks) break;
+      const int freed = vwarp ? c - 1 : c;     // the chunk whose use frees the stage
+      if (lane == 0)
+        ok = mbar_wait_bounded(vwarp ? &v_free[freed % kStages] : &k_free[freed % kStages],
+                               (freed / kStages) & 1, p.err);
+      if (!uniform(ok)) break;
+      load(next, vwarp, idq[0]);
+#pragma unroll
+      for (int i = 0; i + 1 < kIdAhead; ++i) idq[i] = idq[i + 1];
+      idq[kIdAhead - 1] = fetch_id(next + kIdAhead);
     }
     // Copies this warp issued land before the CTA's shared memory is given up
     // (earlier uses of a stage completed before its last copy was issued).
