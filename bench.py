@@ -548,7 +548,9 @@ def run_gpu(args):
     stream = torch.cuda.Stream(device)
     attn = args.attn
     if attn == "auto":
-        attn = "splitk" if args.workload in (2, 3, 5) else "decode"
+        # split-K with the chosen partition size also for the shared-prefix
+        # batch (one partition per sequence there: 98 us vs 110 us whole-sequence)
+        attn = "splitk"
     fused = args.step == "fused"
     partition_choice = "given"
     if args.partition is None:
@@ -1020,7 +1022,9 @@ def main(argv=None):
     ap.add_argument("--op", default="step", choices=["step", "copy_blocks", "prefill"],
                     help="copy_blocks: time pa_copy_blocks on a parallel-sampling step; "
                          "prefill: time pa_prefill on a 16 x 512-token chunked-prefill step")
-    ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"])
+    ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"],
+                    help="auto (default): split-K with the chosen partition size; decode: one "
+                         "CTA per (sequence, KV head)")
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
                     help="fused: one pa_decode_step launch per layer (cache write + attention "
                          "+ split-K merge); separate: the cache write, partition pass and "
