@@ -230,8 +230,8 @@ __device__ __forceinline__ void pair_sync(int warp) {
 // that read it; "pv_done": PV read the P it holds), so that each wait names
 // one use of one slot and no parity wait can match an older phase.
 //
-// MMA warp, per chunk c:  wait PV(c-2) (S[(c+1)%3] holds P(c-2)) and K(c+1):
-//   S[(c+1)%3] = Q K(c+1)^T; wait V(c) and P(c): O += P V(c).
+// MMA warp, per chunk c:  wait PV(c-1) (S[(c+2)%3] holds P(c-1)) and K(c+2):
+//   S[(c+2)%3] = Q K(c+2)^T; wait V(c) and P(c): O += P V(c).
 // Copy warps, per chunk c: wait K slot of c free: copy K(c+3) (K warp);
 //   wait V slot of c-1 free: copy V(c+2) (V warp).
 // Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
@@ -412,15 +412,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       bool ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
       if (ok) qk(0);
+      if (ok && nchunks > 1) {
+        ok = mbar_wait_bounded(&k_full[1], 0, p.err);
+        if (ok) qk(1);
+      }
       for (int c = 0; c < nchunks && ok; ++c) {
         const int sb = c % kSBuf, st = c % kStages;
-        if (c + 1 < nchunks) {
-          // PV(c-2) is done with P(c-2) in S[(c+1)%3]
-          if (c >= 2)
-            ok = mbar_wait_bounded(&pv_done[(c + 1) % kSBuf], ((c - 2) / kSBuf) & 1, p.err);
-          ok = ok && mbar_wait_bounded(&k_full[(c + 1) % kStages], ((c + 1) / kStages) & 1, p.err);
+        if (c + 2 < nchunks) {
+          // scores two chunks ahead: PV(c-1) is done with P(c-1) in S[(c+2)%3]
+          if (c >= 1)
+            ok = mbar_wait_bounded(&pv_done[(c + 2) % kSBuf], ((c - 1) / kSBuf) & 1, p.err);
+          ok = ok && mbar_wait_bounded(&k_full[(c + 2) % kStages], ((c + 2) / kStages) & 1, p.err);
           if (!ok) break;
-          qk(c + 1);
+          qk(c + 2);
         }
         ok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err) &&
              mbar_wait_bounded(&p_ready[sb], (c / kSBuf) & 1, p.err);
