@@ -463,18 +463,18 @@ def _attn_fns(st, attn, partition, fused=True):
     return step, dominant, outs
 
 
-def recorded_traffic(kernel, workload_name, partition):
+def recorded_traffic(kernel, workload_name, partition, sources=("decode.cu", "decode_tile.cuh")):
     """DRAM bytes per launch from the committed ncu summaries, or None when the
-    kernel source or the launch shape changed since the counters were taken.
-    ``profiles/decode_traffic.txt`` holds one ``key=value`` record per kernel,
-    records separated by blank lines."""
+    kernel source (the files ``sources``) or the launch shape changed since the
+    counters were taken.  ``profiles/decode_traffic.txt`` holds one
+    ``key=value`` record per kernel, records separated by blank lines."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
         with open(path) as f:
             blocks = f.read().split("\n\n")
         h = hashlib.sha256()
-        for name in ("decode.cu", "decode_tile.cuh"):
+        for name in sources:
             with open(os.path.join(ROOT, "paged_kv_cache_283_gb300", "csrc", name), "rb") as f:
                 h.update(f.read())
         sha = h.hexdigest()
@@ -994,7 +994,8 @@ def run_prefill(args):
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2),
                      "peak": peak if peak else 1900.0, "unit": "TFLOP/s",
                      "frac": round(tflops / (peak if peak else 1900.0), 4),
-                     "traffic": None, "kernel": "pa_prefill",
+                     "traffic": recorded_traffic("pa_prefill", w.name, 0, ("prefill.cu",)),
+                     "kernel": "pa_prefill",
                      "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
                      if peak else "fallback 1.9 PFLOP/s",
                      "us_per_launch": round(dt * 1e6, 2)},
