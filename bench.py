@@ -407,7 +407,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
     return st
 
 
-def _attn_fns(st, attn, partition, fused=True):
+def _attn_fns(st, attn, partition, fused=True, order=None):
     import torch
 
     from paged_kv_cache_283_gb300 import pa
@@ -430,7 +430,7 @@ def _attn_fns(st, attn, partition, fused=True):
                               w.scale, key=st["key"][layer], value=st["value"][layer],
                               slot_mapping=st["slots"],
                               partition_size=partition if attn == "splitk" else 0,
-                              workspace=ws, counters=counters, **scales)
+                              workspace=ws, counters=counters, order=order, **scales)
 
         def fused_step(r):
             for layer, pool in enumerate(st["replicas"][r]):
@@ -552,6 +552,7 @@ def run_gpu(args):
         # batch (one partition per sequence there: 98 us vs 110 us whole-sequence)
         attn = "splitk"
     fused = args.step == "fused"
+    ordered = fused and attn == "splitk" and args.order == "longest"
     partition_choice = "given"
     if args.partition is None:
         if args.workload == 3:
@@ -560,9 +561,17 @@ def run_gpu(args):
         else:
             args.partition = pa.splitk_partition_size(
                 w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, args.kv,
-                torch.cuda.get_device_properties(device).multi_processor_count)
+                torch.cuda.get_device_properties(device).multi_processor_count, ordered=ordered)
             partition_choice = "pa_splitk_partition_size (makespan model)"
-    step, dominant, outs = _attn_fns(st, attn, args.partition, fused)
+    order = None
+    if ordered:
+        maxp = max(1, -(-int(w.context_lens.max()) // args.partition))
+        if w.num_seqs * maxp <= 65535:
+            order = torch.from_numpy(pa.splitk_order(w.context_lens, args.partition, maxp)).to(
+                device)
+        else:
+            ordered = False
+    step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order)
 
     # eager warmup (sets kernel attributes, checks the error word)
     with torch.cuda.stream(stream):
@@ -602,7 +611,7 @@ def run_gpu(args):
     dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * w.layers)
 
     # end to end through the public API with pinned host buffers
-    e2e = _e2e(st, attn, args, stream)
+    e2e = _e2e(st, attn, args, stream, order)
     assert pa.pa_get_device_error() == 0, "device error word set during the run"
 
     step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
@@ -658,6 +667,8 @@ def run_gpu(args):
             "step": args.step,
             "partition": args.partition if attn == "splitk" else None,
             "partition_choice": partition_choice if attn == "splitk" else None,
+            "work_order": ("longest first (pa_splitk_order)" if ordered else "grid")
+            if attn == "splitk" else None,
             "l2": "pool rotated over %d replicas of %.0f MB (> L2 %.0f MB)"
                   % (len(st["replicas"]), st["pool_bytes"] / 1e6, l2 / 1e6)
             if len(st["replicas"]) > 1 else "32 distinct per-layer pools per step",
@@ -682,7 +693,7 @@ def run_gpu(args):
     return 0
 
 
-def _e2e(st, attn, args, stream):
+def _e2e(st, attn, args, stream, order=None):
     """Same metric through the public API: every step, the step's inputs (q,
     the new tokens' K/V, slots, block tables, context lengths, all layers)
     go from a pinned host buffer to the device in one copy, the library's step
@@ -702,6 +713,8 @@ def _e2e(st, attn, args, stream):
         pieces += [("q", layer, st["q"][layer]), ("key", layer, st["key"][layer]),
                    ("value", layer, st["value"][layer])]
     pieces += [("slots", 0, st["slots"]), ("bt", 0, st["bt"]), ("ctx", 0, st["ctx"])]
+    if order is not None:  # the step's work order is one of its inputs
+        pieces.append(("order", 0, order))
     offs, total = [], 0
     for _, _, t in pieces:
         offs.append(total)
@@ -728,7 +741,8 @@ def _e2e(st, attn, args, stream):
                                 partition_size=args.partition, workspace=ws, stream=stream,
                                 k_scales=pool[2] if len(pool) == 4 else None,
                                 v_scales=pool[3] if len(pool) == 4 else None,
-                                fused=args.step == "fused")
+                                fused=args.step == "fused",
+                                order=views[("order", 0)] if order is not None else None)
                   for l, pool in enumerate(st["replicas"][r])] for r in range(nrep)]
         sets.append({"host": host, "staged": staged, "out": out, "hout": hout, "steps": steps,
                      "in_done": torch.cuda.Event(), "computed": torch.cuda.Event(),
@@ -1026,6 +1040,9 @@ def main(argv=None):
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"],
                     help="auto (default): split-K with the chosen partition size; decode: one "
                          "CTA per (sequence, KV head)")
+    ap.add_argument("--order", default="longest", choices=["longest", "grid"],
+                    help="fused split-K: CTAs handed out longest first (pa_splitk_order) "
+                         "or in grid order")
     ap.add_argument("--step", default="fused", choices=["fused", "separate"],
                     help="fused: one pa_decode_step launch per layer (cache write + attention "
                          "+ split-K merge); separate: the cache write, partition pass and "

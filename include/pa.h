@@ -99,6 +99,7 @@ typedef enum {
 #define PA_DEVERR_CONTEXT_LEN 0x2u  /* context length < 0 or > max_blocks_per_seq*block_size */
 #define PA_DEVERR_SLOT 0x4u         /* slot >= num_blocks * block_size */
 #define PA_DEVERR_WAIT_TIMEOUT 0x8u /* an asynchronous copy did not complete in time */
+#define PA_DEVERR_ORDER 0x10u       /* a work-order entry outside [0, num_seqs * max_partitions) */
 
 /* Static description of a status code; never NULL. */
 const char* pa_status_string(pa_status status);
@@ -356,6 +357,14 @@ pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache
  *     each call leaves them zero again, unless it sets PA_DEVERR_WAIT_TIMEOUT
  *     (then zero them before the next call).  Concurrent calls must not
  *     share counters or workspace.
+ *   order (split-K only, may be NULL): device int32 [num_seqs * max_partitions],
+ *     a permutation of the items item = part * num_seqs + b, the order in
+ *     which the block scheduler receives the (sequence, partition) CTAs
+ *     (pa_splitk_order gives the longest first).  Every item runs whatever the
+ *     order, so an order made for other context lengths only costs speed; an
+ *     entry outside the range sets PA_DEVERR_ORDER and that CTA does nothing
+ *     (its item is then missing: a non-permutation gives wrong results).
+ *     num_seqs * max_partitions <= 65535 (else PA_ERR_UNSUPPORTED_SHAPE).
  * Pools, scales and other arguments as pa_decode / pa_decode_splitk and the
  * _int8 / _fp8 cache writes (the 1-byte variants quantise the new rows by the
  * same rule, bit-identically).
@@ -367,7 +376,7 @@ pa_status pa_decode_step(void* out, const void* q, const void* key, const void* 
                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
                          float scale, int partition_size, float* ws_out, float* ws_m,
                          float* ws_l, unsigned* counters, int max_partitions,
-                         pa_stream_t stream);
+                         const int32_t* order, pa_stream_t stream);
 pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const void* value,
                               const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
                               float* k_scales, float* v_scales, const int32_t* block_tables,
@@ -375,7 +384,7 @@ pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const v
                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                               int num_blocks, float scale, int partition_size, float* ws_out,
                               float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                              pa_stream_t stream);
+                              const int32_t* order, pa_stream_t stream);
 pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const void* value,
                              const int64_t* slot_mapping, uint8_t* k_cache, uint8_t* v_cache,
                              float* k_scales, float* v_scales, const int32_t* block_tables,
@@ -383,7 +392,7 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                              int num_blocks, float scale, int partition_size, float* ws_out,
                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                             pa_stream_t stream);
+                             const int32_t* order, pa_stream_t stream);
 
 /*
  * Paged (chunked) prefill attention ("How LLM Inference Serving Works",
@@ -425,11 +434,25 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
  * kernels) whose batch has fewer (sequence, KV head) units than CTA slots
  * takes 512.  context_lens: host int32
  * [num_seqs]; kv_kind 0 = bf16 cache, 1 = INT8, 2 = FP8; num_sms the device's
- * multiprocessor count.  Returns 0 on invalid arguments.  The result is a
+ * multiprocessor count; ordered != 0 models the launch with the
+ * longest-first order of pa_splitk_order, 0 the plain grid order.  Returns 0
+ * on invalid arguments.  The result is a
  * performance choice only: any partition size gives the same attention.
  */
 int pa_splitk_partition_size(const int32_t* context_lens, int num_seqs, int num_q_heads,
-                             int num_kv_heads, int head_dim, int kv_kind, int num_sms);
+                             int num_kv_heads, int head_dim, int kv_kind, int num_sms,
+                             int ordered);
+
+/*
+ * Longest-first work order for a split-K pa_decode_step (host): fills
+ * order_out[0 .. num_seqs * max_partitions) with the items
+ * item = part * num_seqs + b sorted by the tokens each covers,
+ * min(partition_size, max(0, context_lens[b] - part * partition_size)), most
+ * first, ties in item order.  Returns the item count, or -1 on invalid
+ * arguments (including num_seqs * max_partitions > 65535).
+ */
+int pa_splitk_order(const int32_t* context_lens, int num_seqs, int partition_size,
+                    int max_partitions, int32_t* order_out);
 
 /*
  * Step planning for chunked prefill (host; "How LLM Inference Serving Works",

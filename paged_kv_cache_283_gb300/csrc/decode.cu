@@ -244,8 +244,19 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   griddep_wait();  // the previous kernel (e.g. the cache write) is complete
   griddep_launch_dependents();
   const int kvh = blockIdx.x;
-  const int b = blockIdx.y;
-  const int part = blockIdx.z;
+  // (sequence, partition): the grid's, or the order array's entry for this
+  // CTA (its grid is then (Hkv, B * max_partitions, 1)); an entry out of
+  // range is refused (the item it displaced does not run: the error says so)
+  int b = blockIdx.y, part = blockIdx.z;
+  if (SPLIT && p.order != nullptr) {
+    const int item = __ldg(p.order + blockIdx.y);
+    if (item < 0 || item >= p.num_seqs * p.max_partitions) {
+      if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_ORDER);
+      return;
+    }
+    b = item % p.num_seqs;
+    part = item / p.num_seqs;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int sub = lane % L;
@@ -790,7 +801,9 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, Q>;
   cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
+  const dim3 grid = (SPLIT && p.order != nullptr)
+                        ? dim3(p.num_kv_heads, p.num_seqs * p.max_partitions, 1)
+                        : dim3(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
   return launch_pdl(kernel, grid, dim3(NW * 32), Lay::TOTAL, stream, p);
 }
 

@@ -43,6 +43,9 @@ struct DecodeParams {
   const __nv_bfloat16* new_value;
   const int64_t* slot_mapping;     // [B]: the slot of position context_lens[b] - 1, or < 0
   unsigned* counters;              // split-K: [B, Hkv] arrivals; the last CTA merges
+  // split-K, optional: the order in which the (sequence, partition) items run,
+  // a permutation of [0, B * max_partitions) (item = part * B + b); null: grid order
+  const int32_t* order;
 };
 
 struct ReduceParams {

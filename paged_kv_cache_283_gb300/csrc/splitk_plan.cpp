@@ -14,8 +14,9 @@
 //                       merging the partial results)
 // and a batch whose sequences need more than 16 partitions merges in a second
 // launch (kApartUs).  The constants were fitted to pa_decode_step timings of
-// the Llama-3.1-8B-shaped batch-64 and 32-layer batch-256 steps at partition
-// 384 .. 1536 on a GB300 (bf16 cache).  The 1-byte kernels are issue-bound:
+// the Llama-3.1-8B-shaped batch-64 and 32-layer batch-256 steps on a GB300
+// (bf16 cache), once for each dispatch order: grid order at partition 384 ..
+// 1536, longest first (pa_splitk_order) at 768 .. 2048.  The 1-byte kernels are issue-bound:
 // a CTA that runs with fewer neighbours on its SM does not get much faster,
 // which the model (fixed CTA durations) gets right only once the batch has
 // a CTA for every slot without splitting; with fewer (sequence, KV head)
@@ -32,10 +33,15 @@
 
 namespace {
 
-constexpr double kTokenUsBf16 = 0.025;  // per token and KV head, head_dim 128
-constexpr double kTokenUs1Byte = 0.019;
-constexpr double kCtaUs = 4.0;
-constexpr double kMergeUs = 2.0;
+// Costs (µs) fitted per dispatch order: grid order, and longest first.
+struct Costs {
+  double token_bf16;  // per token and KV head, head_dim 128, bf16 cache
+  double token_1byte;
+  double cta;
+  double merge;
+};
+constexpr Costs kGridCosts = {0.025, 0.019, 4.0, 2.0};
+constexpr Costs kOrderedCosts = {0.022, 0.0167, 8.0, 3.0};
 constexpr double kApartUs = 3.0;
 constexpr int kMergeInKernelParts = 16;  // as pa_decode_step
 constexpr int kCandidates[] = {256, 384, 512, 640, 768, 1024, 1536, 2048, 4096};
@@ -46,25 +52,35 @@ int ctas_per_sm(int group, int kv_kind) {
   return group <= 4 ? 4 : 3;
 }
 
-double makespan(const int32_t* ctx, int num_seqs, int hkv, int part, int slots, double token_us) {
+// Tokens of item (b, z) of a split into `part`-token partitions.
+int item_tokens(int n, int z, int part) { return std::max(0, std::min(part, n - z * part)); }
+
+double makespan(const int32_t* ctx, int num_seqs, int hkv, int part, int slots, double token_us,
+                bool ordered) {
+  const Costs& k = ordered ? kOrderedCosts : kGridCosts;
   int maxp = 1;
   for (int b = 0; b < num_seqs; ++b) maxp = std::max(maxp, (std::max(ctx[b], 0) + part - 1) / part);
   const bool apart = maxp > kMergeInKernelParts;
-  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-  for (int s = 0; s < slots; ++s) free_at.push(0.0);
+  // CTA durations in dispatch order: the grid's (partition slowest), or
+  // longest first (the order pa_splitk_order gives)
+  std::vector<double> items;
   for (int z = 0; z < maxp; ++z) {
     for (int b = 0; b < num_seqs; ++b) {
       const int n = std::max(ctx[b], 0);
       const int np = (n + part - 1) / part;
       if (z >= std::max(np, 1)) continue;
-      const int tokens = std::min(part, n - z * part);
-      const double d = token_us * std::max(tokens, 0) + kCtaUs +
-                       ((np > 1 && !apart) ? kMergeUs : 0.0);
-      for (int h = 0; h < hkv; ++h) {
-        const double t = free_at.top();
-        free_at.pop();
-        free_at.push(t + d);
-      }
+      items.push_back(token_us * item_tokens(n, z, part) + k.cta +
+                      ((np > 1 && !apart) ? k.merge : 0.0));
+    }
+  }
+  if (ordered) std::stable_sort(items.begin(), items.end(), std::greater<double>());
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int s = 0; s < slots; ++s) free_at.push(0.0);
+  for (const double d : items) {
+    for (int h = 0; h < hkv; ++h) {
+      const double t = free_at.top();
+      free_at.pop();
+      free_at.push(t + d);
     }
   }
   double end = 0.0;
@@ -79,14 +95,15 @@ double makespan(const int32_t* ctx, int num_seqs, int hkv, int part, int slots, 
 
 extern "C" int pa_splitk_partition_size(const int32_t* context_lens, int num_seqs,
                                         int num_q_heads, int num_kv_heads, int head_dim,
-                                        int kv_kind, int num_sms) {
+                                        int kv_kind, int num_sms, int ordered) {
   if (!context_lens || num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads != 0 || head_dim <= 0 || kv_kind < 0 || kv_kind > 2 ||
       num_sms <= 0)
     return 0;
   const int group = num_q_heads / num_kv_heads;
   const int slots = num_sms * ctas_per_sm(group, kv_kind);
-  const double token_us = (kv_kind == 0 ? kTokenUsBf16 : kTokenUs1Byte) * head_dim / 128.0;
+  const Costs& k = ordered ? kOrderedCosts : kGridCosts;
+  const double token_us = (kv_kind == 0 ? k.token_bf16 : k.token_1byte) * head_dim / 128.0;
   int max_ctx = 0;
   for (int b = 0; b < num_seqs; ++b) max_ctx = std::max(max_ctx, context_lens[b]);
   if (kv_kind != 0 && static_cast<int64_t>(num_seqs) * num_kv_heads < slots &&
@@ -96,7 +113,8 @@ extern "C" int pa_splitk_partition_size(const int32_t* context_lens, int num_seq
   double best_t = 0.0;
   for (int part : kCandidates) {
     if ((static_cast<int64_t>(max_ctx) + part - 1) / part > 65535) continue;  // grid z
-    const double t = makespan(context_lens, num_seqs, num_kv_heads, part, slots, token_us);
+    const double t =
+        makespan(context_lens, num_seqs, num_kv_heads, part, slots, token_us, ordered != 0);
     // ties go to the larger partition: fewer CTAs, less workspace
     if (best == 0 || t <= best_t + 1e-9) {
       best = part;
@@ -105,4 +123,25 @@ extern "C" int pa_splitk_partition_size(const int32_t* context_lens, int num_seq
     if (part >= max_ctx) break;  // larger sizes give the same single partitions
   }
   return best;
+}
+
+// Longest-first work order for a split-K launch: a permutation of the items
+// [0, num_seqs * max_partitions) (item = part * num_seqs + b) sorted by the
+// tokens each covers, most first, ties in item order; items past a sequence's
+// end (0 tokens) come last.  The block scheduler hands CTAs out in this order,
+// so the long ones start first and the short ones fill the tail.
+extern "C" int pa_splitk_order(const int32_t* context_lens, int num_seqs, int partition_size,
+                               int max_partitions, int32_t* order_out) {
+  if (!context_lens || !order_out || num_seqs <= 0 || partition_size <= 0 ||
+      max_partitions <= 0 || static_cast<int64_t>(num_seqs) * max_partitions > 65535)
+    return -1;
+  const int n_items = num_seqs * max_partitions;
+  std::vector<std::pair<int, int>> key(n_items);  // (-tokens, item)
+  for (int item = 0; item < n_items; ++item) {
+    const int b = item % num_seqs, z = item / num_seqs;
+    key[item] = {-item_tokens(std::max(context_lens[b], 0), z, partition_size), item};
+  }
+  std::sort(key.begin(), key.end());
+  for (int i = 0; i < n_items; ++i) order_out[i] = key[i].second;
+  return n_items;
 }

@@ -25,6 +25,7 @@ PA_DEVERR_BLOCK_ID = 0x1
 PA_DEVERR_CONTEXT_LEN = 0x2
 PA_DEVERR_SLOT = 0x4
 PA_DEVERR_WAIT_TIMEOUT = 0x8
+PA_DEVERR_ORDER = 0x10
 
 # Every function include/pa.h declares: name -> (restype, argtypes).
 _vp, _i, _u, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
@@ -55,13 +56,14 @@ SIGNATURES = {
     "pa_decode_splitk": (_i, [_vp, _vp, _vp, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i,
                               _i, _i, _f, _i, _vp]),
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
-    "pa_splitk_partition_size": (_i, [_vp, _i, _i, _i, _i, _i, _i]),
+    "pa_splitk_partition_size": (_i, [_vp, _i, _i, _i, _i, _i, _i, _i]),
+    "pa_splitk_order": (_i, [_vp, _i, _i, _i, _vp]),
     "pa_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
-                            _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+                            _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
     "pa_decode_step_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
-                                 _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+                                 _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
     "pa_decode_step_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
-                                _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp]),
+                                _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
     "pa_decode_splitk_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _i, _vp]),
     "pa_prefill_supported": (_i, [_i, _i, _i]),
@@ -341,9 +343,10 @@ def splitk_workspace(num_seqs, num_q_heads, head_dim, max_context_len, partition
 
 
 def splitk_partition_size(context_lens, num_q_heads, num_kv_heads, head_dim, kv="bf16",
-                          num_sms=None):
+                          num_sms=None, ordered=False):
     """The split-K partition size pa_splitk_partition_size chooses for a batch
-    (context_lens: host int array).  num_sms defaults to the current CUDA
+    (context_lens: host int array); ordered: for a launch with the
+    longest-first order of splitk_order.  num_sms defaults to the current CUDA
     device's multiprocessor count."""
     import numpy as np
     ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
@@ -352,10 +355,25 @@ def splitk_partition_size(context_lens, num_q_heads, num_kv_heads, head_dim, kv=
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     kind = {"bf16": 0, "int8": 1, "fp8": 2}[kv]
     r = lib().pa_splitk_partition_size(ctx.ctypes.data_as(ctypes.c_void_p), ctx.shape[0],
-                                       num_q_heads, num_kv_heads, head_dim, kind, int(num_sms))
+                                       num_q_heads, num_kv_heads, head_dim, kind, int(num_sms),
+                                       1 if ordered else 0)
     if r <= 0:
         raise ValueError("pa_splitk_partition_size: invalid arguments")
     return int(r)
+
+
+def splitk_order(context_lens, partition_size, max_partitions):
+    """Longest-first work order (host numpy int32 [B * max_partitions]) for a
+    split-K pa_decode_step; copy it to the device and pass it as ``order``."""
+    import numpy as np
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    out = np.empty(ctx.shape[0] * int(max_partitions), dtype=np.int32)
+    r = lib().pa_splitk_order(ctx.ctypes.data_as(ctypes.c_void_p), ctx.shape[0],
+                              int(partition_size), int(max_partitions),
+                              out.ctypes.data_as(ctypes.c_void_p))
+    if r != out.shape[0]:
+        raise ValueError("pa_splitk_order: invalid arguments")
+    return out
 
 
 def step_counters(num_seqs, num_kv_heads, device="cuda"):
@@ -365,7 +383,8 @@ def step_counters(num_seqs, num_kv_heads, device="cuda"):
 
 
 def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
-               slot_mapping, partition_size, workspace, counters, k_scales, v_scales):
+               slot_mapping, partition_size, workspace, counters, k_scales, v_scales,
+               order=None):
     """(C function, argument tuple without the stream) for pa_decode_step*."""
     torch = _torch()
     fp8 = k_cache.dtype == torch.uint8
@@ -404,27 +423,33 @@ def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key,
         wsa = (_dev(ws_o, torch.float32, "ws_out", 4), _dev(ws_m, torch.float32, "ws_m", 3),
                _dev(ws_l, torch.float32, "ws_l", 3), _dev(counters, torch.int32, "counters", 1),
                maxp)
+        if order is not None and order.shape != (B * maxp,):
+            raise ValueError("pa_decode_step: order must be [num_seqs * max_partitions]")
     else:
         wsa = (none, none, none, none, 0)
+        if order is not None:
+            raise ValueError("pa_decode_step: an order needs split-K")
+    ordp = (none,) if order is None else (_dev(order, torch.int32, "order", 1),)
     fn = lib().pa_decode_step_fp8 if fp8 else (lib().pa_decode_step_int8 if one
                                                 else lib().pa_decode_step)
     args = (_dev(out, torch.bfloat16, "out", 3), pq) + kvs + pools + (
-        pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), ps) + wsa
+        pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), ps) + wsa + ordp
     return fn, args
 
 
 def pa_decode_step(out, q, k_cache, v_cache, block_tables, context_lens, scale, key=None,
                    value=None, slot_mapping=None, partition_size=512, workspace=None,
-                   counters=None, k_scales=None, v_scales=None, stream=None):
+                   counters=None, k_scales=None, v_scales=None, stream=None, order=None):
     """Cache write of each sequence's new token (key / value [B, Hkv, D] at
     slot_mapping [B], which must be the slot of position context_lens[b] - 1)
     and the decode, in one launch.  partition_size 0: whole-sequence CTAs;
     > 0: split-K merged in the same launch (workspace = splitk_workspace(...),
     counters = step_counters(...)).  The cache dtype picks bf16 / INT8 (int8)
-    / FP8 (uint8 codes, with k_scales / v_scales)."""
+    / FP8 (uint8 codes, with k_scales / v_scales).  order: optional device
+    int32 work order (splitk_order) for the split-K CTAs."""
     fn, args = _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key,
                           value, slot_mapping, partition_size, workspace, counters, k_scales,
-                          v_scales)
+                          v_scales, order)
     _check(fn(*args, _stream(stream)), "pa_decode_step")
 
 
@@ -552,7 +577,7 @@ class DecodeStep:
     def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                  context_lens, out, scale, split=True, partition_size=512,
                  max_context_len=None, workspace=None, stream=None, k_scales=None,
-                 v_scales=None, fused=True, counters=None):
+                 v_scales=None, fused=True, counters=None, order=None):
         torch = _torch()
         self.fused = bool(fused)
         if self.fused:
@@ -572,9 +597,9 @@ class DecodeStep:
             self._fn, self._args = _step_args(
                 out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
                 slot_mapping, partition_size if self.split else 0, workspace, counters,
-                k_scales, v_scales)
+                k_scales, v_scales, order)
             self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables,
-                          context_lens, out, workspace, counters, k_scales, v_scales]
+                          context_lens, out, workspace, counters, k_scales, v_scales, order]
             return
         T, hkv, d = key.shape
         nb, hkv2, bs, d2 = k_cache.shape

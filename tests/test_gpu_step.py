@@ -231,3 +231,60 @@ def test_fused_step_long_context_matches_separate_kernels():
         assert np.array_equal(kh[si // 16, :, si % 16], w.key[bi])
     assert int(counters.abs().sum().item()) == 0
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("kind", ["longest", "random", "stale"])
+@pytest.mark.parametrize("split", [256, 64])
+def test_fused_step_work_order(kind, split):
+    """A split-K launch in a given work order (pa_splitk_order's longest-first,
+    a random permutation, or the order made for other context lengths) gives
+    the same attention: every item runs whatever the order."""
+    w = I.random_case(6400 + split, len(EDGE), EDGE, 32, 8, 128)
+    c = _Case(w, "bf16")
+    maxp = -(-int(w.context_lens.max()) // split)
+    if kind == "longest":
+        order = pa.splitk_order(w.context_lens, split, maxp)
+    elif kind == "random":
+        order = np.random.default_rng(split).permutation(w.num_seqs * maxp).astype(np.int32)
+    else:
+        other = np.random.default_rng(7).integers(0, 3000, size=w.num_seqs).astype(np.int32)
+        order = pa.splitk_order(other, split, maxp)
+    ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()),
+                             split)
+    counters = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    q = dev_bf16(w.q)
+    out = torch.empty_like(q)
+    pa.pa_clear_device_error()
+    pa.pa_decode_step(out, q, c.dev[0], c.dev[1], _i32(c.bt_p), _i32(w.context_lens), w.scale,
+                      key=dev_bf16(w.key), value=dev_bf16(w.value), slot_mapping=_i64(c.sl_p),
+                      partition_size=split, workspace=ws, counters=counters,
+                      order=_i32(order))
+    torch.cuda.synchronize()
+    c.oracle_write(w.key, w.value, c.sl_m)
+    for got, want in zip(c.device_pools(), c.host):
+        assert np.array_equal(got, want)
+    assert_close(bf16_to_f64(out), c.oracle_decode(w.q), f"order {kind} split={split}")
+    assert int(counters.abs().sum().item()) == 0
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fused_step_order_entry_out_of_range():
+    """An order entry outside [0, B * max_partitions) sets PA_DEVERR_ORDER and
+    its CTA does nothing (no wait, no fault)."""
+    w = I.random_case(6500, 4, [100, 300, 17, 64], 32, 8, 128)
+    c = _Case(w, "bf16")
+    split = 64
+    maxp = -(-int(w.context_lens.max()) // split)
+    order = pa.splitk_order(w.context_lens, split, maxp)
+    order[-1] = w.num_seqs * maxp + 5
+    ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()),
+                             split)
+    counters = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    q = dev_bf16(w.q)
+    out = torch.empty_like(q)
+    pa.pa_clear_device_error()
+    pa.pa_decode_step(out, q, c.dev[0], c.dev[1], _i32(c.bt_p), _i32(w.context_lens), w.scale,
+                      partition_size=split, workspace=ws, counters=counters, order=_i32(order))
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_ORDER
+    pa.pa_clear_device_error()
