@@ -430,9 +430,9 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
  * split-K launch's time -- its CTAs handed in grid order to the first free
  * CTA slot (num_sms x the kernel's CTAs per SM), each costing a time per
  * token, a fixed start-up and, for sequences of several partitions, a merge
- * share -- with ties going to the larger size; a 1-byte cache (issue-bound
- * kernels) whose batch has fewer (sequence, KV head) units than CTA slots
- * takes 512.  context_lens: host int32
+ * share -- with ties going to the larger size; in grid order a 1-byte cache
+ * (issue-bound kernels) whose batch has fewer (sequence, KV head) units than
+ * CTA slots takes 512.  context_lens: host int32
  * [num_seqs]; kv_kind 0 = bf16 cache, 1 = INT8, 2 = FP8; num_sms the device's
  * multiprocessor count; ordered != 0 models the launch with the
  * longest-first order of pa_splitk_order, 0 the plain grid order.  Returns 0

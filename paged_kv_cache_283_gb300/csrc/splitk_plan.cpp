@@ -18,9 +18,11 @@
 // (bf16 cache), once for each dispatch order: grid order at partition 384 ..
 // 1536, longest first (pa_splitk_order) at 768 .. 2048.  The 1-byte kernels are issue-bound:
 // a CTA that runs with fewer neighbours on its SM does not get much faster,
-// which the model (fixed CTA durations) gets right only once the batch has
-// a CTA for every slot without splitting; with fewer (sequence, KV head)
-// units than slots they take 512-token partitions, the measured best there.
+// which the grid-order model (fixed CTA durations) gets right only once the
+// batch has a CTA for every slot without splitting; with fewer (sequence, KV
+// head) units than slots they take 512-token partitions in grid order, the
+// measured best there.  Longest first, the model's choice matched the
+// measured best for them too (batch 64: 1024; 32 layers: 2048).
 
 #include <stdint.h>
 
@@ -106,7 +108,7 @@ extern "C" int pa_splitk_partition_size(const int32_t* context_lens, int num_seq
   const double token_us = (kv_kind == 0 ? k.token_bf16 : k.token_1byte) * head_dim / 128.0;
   int max_ctx = 0;
   for (int b = 0; b < num_seqs; ++b) max_ctx = std::max(max_ctx, context_lens[b]);
-  if (kv_kind != 0 && static_cast<int64_t>(num_seqs) * num_kv_heads < slots &&
+  if (!ordered && kv_kind != 0 && static_cast<int64_t>(num_seqs) * num_kv_heads < slots &&
       (static_cast<int64_t>(max_ctx) + 511) / 512 <= 65535)
     return 512;
   int best = 0;

@@ -49,8 +49,8 @@ def _makespan(ctx, hkv, part, slots, token_us, ordered=False):
 def _model_choice(ctx, hq, hkv, d, kind, num_sms, ordered=False):
     slots = _slots(num_sms, hq // hkv, kind)
     token_us = COSTS[ordered][0 if kind == 0 else 1] * d / 128.0
-    if kind != 0 and len(ctx) * hkv < slots and -(-max(ctx) // 512) <= 65535:
-        return 512  # 1-byte caches with fewer units than slots
+    if not ordered and kind != 0 and len(ctx) * hkv < slots and -(-max(ctx) // 512) <= 65535:
+        return 512  # 1-byte caches in grid order with fewer units than slots
     best, best_t = 0, 0.0
     for part in CANDIDATES:
         if -(-max(ctx) // part) > 65535:
