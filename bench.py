@@ -407,7 +407,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
     return st
 
 
-def _attn_fns(st, attn, partition, fused=True, order=None):
+def _attn_fns(st, attn, partition, fused=True, order=None, early_read=False):
     import torch
 
     from paged_kv_cache_283_gb300 import pa
@@ -430,7 +430,8 @@ def _attn_fns(st, attn, partition, fused=True, order=None):
                               w.scale, key=st["key"][layer], value=st["value"][layer],
                               slot_mapping=st["slots"],
                               partition_size=partition if attn == "splitk" else 0,
-                              workspace=ws, counters=counters, order=order, **scales)
+                              workspace=ws, counters=counters, order=order,
+                              early_read=early_read, **scales)
 
         def fused_step(r):
             for layer, pool in enumerate(st["replicas"][r]):
@@ -574,7 +575,12 @@ def run_gpu(args):
                 device)
         else:
             ordered = False
-    step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order)
+    # Early reads: in this step sequence the kernel before each launch is the
+    # previous layer's or step's, which writes only its own pool (another
+    # replica or layer), so tables, lengths, order and this launch's pool are
+    # not written by it (the contract of PA_STEP_EARLY_READ).
+    early = fused and args.early_read == "on"
+    step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order, early)
 
     # eager warmup (sets kernel attributes, checks the error word)
     with torch.cuda.stream(stream):
@@ -614,7 +620,7 @@ def run_gpu(args):
     dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * w.layers)
 
     # end to end through the public API with pinned host buffers
-    e2e = _e2e(st, attn, args, stream, order)
+    e2e = _e2e(st, attn, args, stream, order, early)
     assert pa.pa_get_device_error() == 0, "device error word set during the run"
 
     step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
@@ -668,6 +674,7 @@ def run_gpu(args):
             "kv_cache": args.kv,
             "graph": "one CUDA graph per step (cache write + attention)",
             "step": args.step,
+            "early_read": early,
             "partition": args.partition if attn == "splitk" else None,
             "partition_choice": partition_choice if attn == "splitk" else None,
             "work_order": ("longest first (pa_splitk_order)" if ordered else "grid")
@@ -696,7 +703,7 @@ def run_gpu(args):
     return 0
 
 
-def _e2e(st, attn, args, stream, order=None):
+def _e2e(st, attn, args, stream, order=None, early=False):
     """Same metric through the public API: every step, the step's inputs (q,
     the new tokens' K/V, slots, block tables, context lengths, all layers)
     go from a pinned host buffer to the device in one copy, the library's step
@@ -745,7 +752,8 @@ def _e2e(st, attn, args, stream, order=None):
                                 k_scales=pool[2] if len(pool) == 4 else None,
                                 v_scales=pool[3] if len(pool) == 4 else None,
                                 fused=args.step == "fused",
-                                order=views[("order", 0)] if order is not None else None)
+                                order=views[("order", 0)] if order is not None else None,
+                                early_read=early)
                   for l, pool in enumerate(st["replicas"][r])] for r in range(nrep)]
         sets.append({"host": host, "staged": staged, "out": out, "hout": hout, "steps": steps,
                      "in_done": torch.cuda.Event(), "computed": torch.cuda.Event(),
@@ -1043,6 +1051,10 @@ def main(argv=None):
     ap.add_argument("--attn", default="auto", choices=["auto", "decode", "splitk"],
                     help="auto (default): split-K with the chosen partition size; decode: one "
                          "CTA per (sequence, KV head)")
+    ap.add_argument("--early-read", default="on", choices=["on", "off"],
+                    help="fused step: read tables, lengths and pools before waiting for "
+                         "the previous kernel (PA_STEP_EARLY_READ; the bench's step sequence "
+                         "keeps its contract)")
     ap.add_argument("--order", default="longest", choices=["longest", "grid"],
                     help="fused split-K: CTAs handed out longest first (pa_splitk_order) "
                          "or in grid order")

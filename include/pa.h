@@ -365,10 +365,20 @@ pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache
  *     entry outside the range sets PA_DEVERR_ORDER and that CTA does nothing
  *     (its item is then missing: a non-permutation gives wrong results).
  *     num_seqs * max_partitions <= 65535 (else PA_ERR_UNSUPPORTED_SHAPE).
+ *   flags: 0, or PA_STEP_EARLY_READ: the caller promises that block_tables,
+ *     context_lens, order and the pools (and scales) are not written by the
+ *     kernel launched just before this one on the stream (in a model, that
+ *     kernel writes q and the new K/V, never these).  The launch then reads
+ *     them -- the first block ids and the first K/V tiles -- before waiting
+ *     for that kernel (programmatic dependent launch), overlapping its start
+ *     with the previous kernel's end; q, key, value and slot_mapping are read,
+ *     and anything is written, only after the wait.  Other bits:
+ *     PA_ERR_INVALID_ARG.
  * Pools, scales and other arguments as pa_decode / pa_decode_splitk and the
  * _int8 / _fp8 cache writes (the 1-byte variants quantise the new rows by the
  * same rule, bit-identically).
  */
+#define PA_STEP_EARLY_READ 0x1
 pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value,
                          const int64_t* slot_mapping, void* k_cache, void* v_cache,
                          const int32_t* block_tables, int max_blocks_per_seq,
@@ -376,7 +386,7 @@ pa_status pa_decode_step(void* out, const void* q, const void* key, const void* 
                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
                          float scale, int partition_size, float* ws_out, float* ws_m,
                          float* ws_l, unsigned* counters, int max_partitions,
-                         const int32_t* order, pa_stream_t stream);
+                         const int32_t* order, int flags, pa_stream_t stream);
 pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const void* value,
                               const int64_t* slot_mapping, int8_t* k_cache, int8_t* v_cache,
                               float* k_scales, float* v_scales, const int32_t* block_tables,
@@ -384,7 +394,7 @@ pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const v
                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                               int num_blocks, float scale, int partition_size, float* ws_out,
                               float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                              const int32_t* order, pa_stream_t stream);
+                              const int32_t* order, int flags, pa_stream_t stream);
 pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const void* value,
                              const int64_t* slot_mapping, uint8_t* k_cache, uint8_t* v_cache,
                              float* k_scales, float* v_scales, const int32_t* block_tables,
@@ -392,7 +402,7 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                              int num_blocks, float scale, int partition_size, float* ws_out,
                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                             const int32_t* order, pa_stream_t stream);
+                             const int32_t* order, int flags, pa_stream_t stream);
 
 /*
  * Paged (chunked) prefill attention ("How LLM Inference Serving Works",

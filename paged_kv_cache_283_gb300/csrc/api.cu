@@ -481,7 +481,7 @@ pa_status decode_step_impl(void* out, const void* q, const void* key, const void
                            int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                            int num_blocks, float scale, int partition_size, float* ws_out,
                            float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                           const int32_t* order, int kv, pa_stream_t stream) {
+                           const int32_t* order, int flags, int kv, pa_stream_t stream) {
   pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, scale);
@@ -499,6 +499,7 @@ pa_status decode_step_impl(void* out, const void* q, const void* key, const void
                 !ok_ptr(counters, 4)))
     return PA_ERR_INVALID_ARG;
   if (kv != 0 && (!ok_ptr(k_scales, 16) || !ok_ptr(v_scales, 16))) return PA_ERR_INVALID_ARG;
+  if ((flags & ~PA_STEP_EARLY_READ) != 0) return PA_ERR_INVALID_ARG;
   if (order != nullptr) {
     if (!split || !ok_ptr(order, 4)) return PA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(num_seqs) * max_partitions > 65535)
@@ -515,6 +516,7 @@ pa_status decode_step_impl(void* out, const void* q, const void* key, const void
     p.fp8 = kv == 2;
   }
   p.out = static_cast<__nv_bfloat16*>(out);
+  p.early_read = (flags & PA_STEP_EARLY_READ) != 0;
   if (write) {
     p.new_key = static_cast<const __nv_bfloat16*>(key);
     p.new_value = static_cast<const __nv_bfloat16*>(value);
@@ -570,11 +572,11 @@ pa_status pa_decode_step(void* out, const void* q, const void* key, const void* 
                          int num_kv_heads, int head_dim, int block_size, int num_blocks,
                          float scale, int partition_size, float* ws_out, float* ws_m,
                          float* ws_l, unsigned* counters, int max_partitions,
-                         const int32_t* order, pa_stream_t stream) {
+                         const int32_t* order, int flags, pa_stream_t stream) {
   return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, nullptr, nullptr,
                           block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                           num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
-                          ws_out, ws_m, ws_l, counters, max_partitions, order, 0, stream);
+                          ws_out, ws_m, ws_l, counters, max_partitions, order, flags, 0, stream);
 }
 
 pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const void* value,
@@ -584,11 +586,11 @@ pa_status pa_decode_step_int8(void* out, const void* q, const void* key, const v
                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                               int num_blocks, float scale, int partition_size, float* ws_out,
                               float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                              const int32_t* order, pa_stream_t stream) {
+                              const int32_t* order, int flags, pa_stream_t stream) {
   return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, k_scales, v_scales,
                           block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                           num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
-                          ws_out, ws_m, ws_l, counters, max_partitions, order, 1, stream);
+                          ws_out, ws_m, ws_l, counters, max_partitions, order, flags, 1, stream);
 }
 
 pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const void* value,
@@ -598,11 +600,11 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                              int num_blocks, float scale, int partition_size, float* ws_out,
                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
-                             const int32_t* order, pa_stream_t stream) {
+                             const int32_t* order, int flags, pa_stream_t stream) {
   return decode_step_impl(out, q, key, value, slot_mapping, k_cache, v_cache, k_scales, v_scales,
                           block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
                           num_kv_heads, head_dim, block_size, num_blocks, scale, partition_size,
-                          ws_out, ws_m, ws_l, counters, max_partitions, order, 2, stream);
+                          ws_out, ws_m, ws_l, counters, max_partitions, order, flags, 2, stream);
 }
 
 }  // extern "C"

@@ -241,7 +241,11 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  griddep_wait();  // the previous kernel (e.g. the cache write) is complete
+  // The previous kernel (e.g. the cache write) is complete after this wait.
+  // With early reads (the caller's promise that tables, lengths, order and
+  // pools are not written by it) the wait comes after the first copies are
+  // out, and before anything else is read or anything is written.
+  if (!p.early_read) griddep_wait();
   griddep_launch_dependents();
   const int kvh = blockIdx.x;
   // (sequence, partition): the grid's, or the order array's entry for this
@@ -285,114 +289,120 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   float qsc[G];       // int8 cache: q scale times scale * log2(e)
   uint32_t qf[D / 16][2];  // fp8 cache: q's MMA fragments (tile_step_f8), f16 pairs
   float2 qfac;             // fp8 cache: per-head factor of heads 2 tig, 2 tig + 1
-  if constexpr (Q == 2) {
-    // Lane (gid, tig) holds head gid's dims [(D/4) tig, +D/4) (zeros for gid >= G),
-    // times 2^k with k per head chosen so that the head's largest |q| lands in
-    // [2^14, 2^15): every bf16 value then converts to f16 exactly unless it is
-    // below 2^-14 (an absolute error under 2^-25 of that maximum), and the
-    // products with codes (|x| <= 448) stay far inside fp32.  qfac carries
-    // 2^-k * scale * log2 e back onto the scores.
-    constexpr int E = D / 4;
-    const int gid = lane >> 2, tig = lane & 3;
-    float f[E];
-    float amax = 0.f;
-    if (gid < G) {
-      const __nv_bfloat16* qh =
-          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + gid) * D +
-          E * tig;
-#pragma unroll
-      for (int u = 0; u < E / 8; ++u) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
-        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
-        const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
-        f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
-        f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
+  // q of the group into this lane's registers (or, for the int8 cache,
+  // quantised through shared memory): the inputs a preceding kernel may
+  // still be writing, so with early reads this runs after the wait.
+  auto load_q = [&]() {
+    if constexpr (Q == 2) {
+      // Lane (gid, tig) holds head gid's dims [(D/4) tig, +D/4) (zeros for gid >= G),
+      // times 2^k with k per head chosen so that the head's largest |q| lands in
+      // [2^14, 2^15): every bf16 value then converts to f16 exactly unless it is
+      // below 2^-14 (an absolute error under 2^-25 of that maximum), and the
+      // products with codes (|x| <= 448) stay far inside fp32.  qfac carries
+      // 2^-k * scale * log2 e back onto the scores.
+      constexpr int E = D / 4;
+      const int gid = lane >> 2, tig = lane & 3;
+      float f[E];
+      float amax = 0.f;
+      if (gid < G) {
+        const __nv_bfloat16* qh =
+            p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + gid) * D +
+            E * tig;
+  #pragma unroll
+        for (int u = 0; u < E / 8; ++u) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+          const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+          const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
+          f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
+          f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
+        }
+      } else {
+  #pragma unroll
+        for (int k = 0; k < E; ++k) f[k] = 0.f;
+      }
+  #pragma unroll
+      for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+      // biased exponent of amax (0 for 0 and subnormals); k = 14 - unbiased
+      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      const int kexp = min(127, max(-126, 141 - ebits));
+      const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
+  #pragma unroll
+      for (int s2 = 0; s2 < D / 16; ++s2) {
+        const __half2 lo = __floats2half2_rn(f[4 * s2] * up, f[4 * s2 + 1] * up);
+        const __half2 hi = __floats2half2_rn(f[4 * s2 + 2] * up, f[4 * s2 + 3] * up);
+        qf[s2][0] = *reinterpret_cast<const uint32_t*>(&lo);
+        qf[s2][1] = *reinterpret_cast<const uint32_t*>(&hi);
+      }
+      const float fac = gid < G ? ldexpf(p.scale_log2, -kexp) : 0.f;
+      qfac = make_float2(__shfl_sync(kFullMask, fac, 8 * tig),
+                         __shfl_sync(kFullMask, fac, 8 * tig + 4));
+    } else if constexpr (Q == 0) {
+      const __nv_bfloat16* qb =
+          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
+      uint4 qw[G];
+  #pragma unroll
+      for (int g = 0; g < G; ++g)
+        qw[g] = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D));
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+  #pragma unroll
+      for (int g = 0; g < G; ++g) {
+        q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
+        q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
+        q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
+        q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
       }
     } else {
-#pragma unroll
-      for (int k = 0; k < E; ++k) f[k] = 0.f;
-    }
-#pragma unroll
-    for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-    // biased exponent of amax (0 for 0 and subnormals); k = 14 - unbiased
-    const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-    const int kexp = min(127, max(-126, 141 - ebits));
-    const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
-#pragma unroll
-    for (int s2 = 0; s2 < D / 16; ++s2) {
-      const __half2 lo = __floats2half2_rn(f[4 * s2] * up, f[4 * s2 + 1] * up);
-      const __half2 hi = __floats2half2_rn(f[4 * s2 + 2] * up, f[4 * s2 + 3] * up);
-      qf[s2][0] = *reinterpret_cast<const uint32_t*>(&lo);
-      qf[s2][1] = *reinterpret_cast<const uint32_t*>(&hi);
-    }
-    const float fac = gid < G ? ldexpf(p.scale_log2, -kexp) : 0.f;
-    qfac = make_float2(__shfl_sync(kFullMask, fac, 8 * tig),
-                       __shfl_sync(kFullMask, fac, 8 * tig + 4));
-  } else if constexpr (Q == 0) {
-    const __nv_bfloat16* qb =
-        p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
-    uint4 qw[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      qw[g] = __ldg(reinterpret_cast<const uint4*>(qb + static_cast<size_t>(g) * D));
-    const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      q2[g][0] = __fmul2_rn(bf16x2_to_float2(qw[g].x), sc2);
-      q2[g][1] = __fmul2_rn(bf16x2_to_float2(qw[g].y), sc2);
-      q2[g][2] = __fmul2_rn(bf16x2_to_float2(qw[g].z), sc2);
-      q2[g][3] = __fmul2_rn(bf16x2_to_float2(qw[g].w), sc2);
-    }
-  } else {
-    // q of each head to int8 codes with one fp32 scale, by the cache's rule
-    // (scale = amax / 127, code = round-half-even(q / scale)), once per CTA:
-    // warp w quantises heads w, w + NW, ... into shared memory, then every
-    // lane loads the codes it needs.  The scores carry scale_q * scale * log2 e.
-    constexpr int E = D / 32;  // values per lane
-    unsigned char* q8 = smem + Lay::QOFF;
-    float* qs = reinterpret_cast<float*>(smem + Lay::QOFF + G * D);
-    for (int g = warp; g < G; g += NW) {
-      const __nv_bfloat16* qh =
-          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + g) * D +
-          lane * E;
-      float f[E];
-      if constexpr (E == 4) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh));
-        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
-        f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
-      } else {
-        const float2 a = bf16x2_to_float2(__ldg(reinterpret_cast<const unsigned int*>(qh)));
-        f[0] = a.x; f[1] = a.y;
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
-#pragma unroll
-      for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
-      const float qscale = __fdiv_rn(amax, 127.0f);
-      uint32_t packed = 0;
-      if (qscale > 0.f) {
-#pragma unroll
-        for (int k = 0; k < E; ++k) {
-          const float c8 = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[k], qscale))));
-          packed |= (static_cast<uint32_t>(static_cast<int>(c8)) & 0xffu) << (8 * k);
+      // q of each head to int8 codes with one fp32 scale, by the cache's rule
+      // (scale = amax / 127, code = round-half-even(q / scale)), once per CTA:
+      // warp w quantises heads w, w + NW, ... into shared memory, then every
+      // lane loads the codes it needs.  The scores carry scale_q * scale * log2 e.
+      constexpr int E = D / 32;  // values per lane
+      unsigned char* q8 = smem + Lay::QOFF;
+      float* qs = reinterpret_cast<float*>(smem + Lay::QOFF + G * D);
+      for (int g = warp; g < G; g += NW) {
+        const __nv_bfloat16* qh =
+            p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + g) * D +
+            lane * E;
+        float f[E];
+        if constexpr (E == 4) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh));
+          const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+          f[0] = a.x; f[1] = a.y; f[2] = c.x; f[3] = c.y;
+        } else {
+          const float2 a = bf16x2_to_float2(__ldg(reinterpret_cast<const unsigned int*>(qh)));
+          f[0] = a.x; f[1] = a.y;
         }
+        float amax = 0.f;
+  #pragma unroll
+        for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
+  #pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, m));
+        const float qscale = __fdiv_rn(amax, 127.0f);
+        uint32_t packed = 0;
+        if (qscale > 0.f) {
+  #pragma unroll
+          for (int k = 0; k < E; ++k) {
+            const float c8 = fminf(127.f, fmaxf(-127.f, rintf(__fdiv_rn(f[k], qscale))));
+            packed |= (static_cast<uint32_t>(static_cast<int>(c8)) & 0xffu) << (8 * k);
+          }
+        }
+        if constexpr (E == 4)
+          *reinterpret_cast<uint32_t*>(q8 + g * D + lane * E) = packed;
+        else
+          *reinterpret_cast<uint16_t*>(q8 + g * D + lane * E) = static_cast<uint16_t>(packed);
+        if (lane == 0) qs[g] = qscale;
       }
-      if constexpr (E == 4)
-        *reinterpret_cast<uint32_t*>(q8 + g * D + lane * E) = packed;
-      else
-        *reinterpret_cast<uint16_t*>(q8 + g * D + lane * E) = static_cast<uint16_t>(packed);
-      if (lane == 0) qs[g] = qscale;
+      __syncthreads();
+  #pragma unroll
+      for (int g = 0; g < G; ++g) {
+        i8_load_row<IG::QB>(q8 + g * D, qsub, qrg, qc[g]);
+        qsc[g] = qs[g] * p.scale_log2;
+      }
     }
-    __syncthreads();
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      i8_load_row<IG::QB>(q8 + g * D, qsub, qrg, qc[g]);
-      qsc[g] = qs[g] * p.scale_log2;
-    }
-  }
+  };
+  if (!p.early_read) load_q();
 
   // Context length lives in device memory: check it here.
   const int ctx_cap = p.max_blocks_per_seq * BS;
@@ -415,6 +425,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
         (nblk + p.partition_blocks - 1) / p.partition_blocks > p.max_partitions)
       raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
     if (part_first >= nblk) {  // past the end of this sequence; CTA-uniform, nothing issued
+      if (p.early_read) griddep_wait();
       if (writer_cta && threadIdx.x == 0 && __ldg(p.slot_mapping + b) >= 0)
         raise_error(p.err, PA_DEVERR_SLOT);  // a new token for an empty sequence
       if (p.counters != nullptr && nblk == 0 && part == 0) {
@@ -514,6 +525,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i);
+  if (p.early_read) {
+    griddep_wait();
+    load_q();
+  }
   // this warp patches its tile of the sequence's last block (the only
   // block with ctx - j * BS <= BS)
   const bool patch_row =

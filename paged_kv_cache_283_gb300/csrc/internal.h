@@ -46,6 +46,9 @@ struct DecodeParams {
   // split-K, optional: the order in which the (sequence, partition) items run,
   // a permutation of [0, B * max_partitions) (item = part * B + b); null: grid order
   const int32_t* order;
+  // Tables, lengths, order and pools are not written by the preceding kernel:
+  // they may be read before waiting for it (programmatic dependent launch).
+  int early_read;
 };
 
 struct ReduceParams {

@@ -26,6 +26,7 @@ PA_DEVERR_CONTEXT_LEN = 0x2
 PA_DEVERR_SLOT = 0x4
 PA_DEVERR_WAIT_TIMEOUT = 0x8
 PA_DEVERR_ORDER = 0x10
+PA_STEP_EARLY_READ = 0x1
 
 # Every function include/pa.h declares: name -> (restype, argtypes).
 _vp, _i, _u, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint, ctypes.c_float, ctypes.c_size_t
@@ -59,11 +60,13 @@ SIGNATURES = {
     "pa_splitk_partition_size": (_i, [_vp, _i, _i, _i, _i, _i, _i, _i]),
     "pa_splitk_order": (_i, [_vp, _i, _i, _i, _vp]),
     "pa_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
-                            _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
+                            _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp]),
     "pa_decode_step_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
-                                 _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
+                                 _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                 _vp]),
     "pa_decode_step_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
-                                _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _vp]),
+                                _i, _i, _i, _i, _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                _vp]),
     "pa_decode_splitk_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i, _i,
                                       _f, _i, _i, _vp]),
     "pa_prefill_supported": (_i, [_i, _i, _i]),
@@ -384,7 +387,7 @@ def step_counters(num_seqs, num_kv_heads, device="cuda"):
 
 def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
                slot_mapping, partition_size, workspace, counters, k_scales, v_scales,
-               order=None):
+               order=None, early_read=False):
     """(C function, argument tuple without the stream) for pa_decode_step*."""
     torch = _torch()
     fp8 = k_cache.dtype == torch.uint8
@@ -433,23 +436,27 @@ def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key,
     fn = lib().pa_decode_step_fp8 if fp8 else (lib().pa_decode_step_int8 if one
                                                 else lib().pa_decode_step)
     args = (_dev(out, torch.bfloat16, "out", 3), pq) + kvs + pools + (
-        pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), ps) + wsa + ordp
+        pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), ps) + wsa + ordp + (
+        PA_STEP_EARLY_READ if early_read else 0,)
     return fn, args
 
 
 def pa_decode_step(out, q, k_cache, v_cache, block_tables, context_lens, scale, key=None,
                    value=None, slot_mapping=None, partition_size=512, workspace=None,
-                   counters=None, k_scales=None, v_scales=None, stream=None, order=None):
+                   counters=None, k_scales=None, v_scales=None, stream=None, order=None,
+                   early_read=False):
     """Cache write of each sequence's new token (key / value [B, Hkv, D] at
     slot_mapping [B], which must be the slot of position context_lens[b] - 1)
     and the decode, in one launch.  partition_size 0: whole-sequence CTAs;
     > 0: split-K merged in the same launch (workspace = splitk_workspace(...),
     counters = step_counters(...)).  The cache dtype picks bf16 / INT8 (int8)
     / FP8 (uint8 codes, with k_scales / v_scales).  order: optional device
-    int32 work order (splitk_order) for the split-K CTAs."""
+    int32 work order (splitk_order) for the split-K CTAs.  early_read: the
+    caller's promise that tables, lengths, order and pools are not written by
+    the kernel launched just before (PA_STEP_EARLY_READ in pa.h)."""
     fn, args = _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key,
                           value, slot_mapping, partition_size, workspace, counters, k_scales,
-                          v_scales, order)
+                          v_scales, order, early_read)
     _check(fn(*args, _stream(stream)), "pa_decode_step")
 
 
@@ -577,7 +584,7 @@ class DecodeStep:
     def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                  context_lens, out, scale, split=True, partition_size=512,
                  max_context_len=None, workspace=None, stream=None, k_scales=None,
-                 v_scales=None, fused=True, counters=None, order=None):
+                 v_scales=None, fused=True, counters=None, order=None, early_read=False):
         torch = _torch()
         self.fused = bool(fused)
         if self.fused:
@@ -597,7 +604,7 @@ class DecodeStep:
             self._fn, self._args = _step_args(
                 out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
                 slot_mapping, partition_size if self.split else 0, workspace, counters,
-                k_scales, v_scales, order)
+                k_scales, v_scales, order, early_read)
             self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                           context_lens, out, workspace, counters, k_scales, v_scales, order]
             return

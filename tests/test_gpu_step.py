@@ -288,3 +288,43 @@ def test_fused_step_order_entry_out_of_range():
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() & pa.PA_DEVERR_ORDER
     pa.pa_clear_device_error()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "int8"])
+def test_fused_step_early_read_chain(kv):
+    """PA_STEP_EARLY_READ: two launches back to back on one stream, the second
+    (layer 2, its own pools) with early reads and with q = the first launch's
+    output, so its q must be read only after waiting for the first kernel.
+    Both against the oracle; the second's q is the first's output as stored."""
+    w = I.random_case(6600, 6, [300, 17, 1, 2049, 512, 96], 32, 8, 128)
+    c1, c2 = _Case(w, kv), _Case(w, kv)
+    split = 256
+    maxp = -(-int(w.context_lens.max()) // split)
+    order = _i32(pa.splitk_order(w.context_lens, split, maxp))
+    ws1 = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()),
+                              split)
+    ws2 = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim, int(w.context_lens.max()),
+                              split)
+    cnt1 = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    cnt2 = pa.step_counters(w.num_seqs, w.num_kv_heads)
+    q1 = dev_bf16(w.q)
+    out1, out2 = torch.empty_like(q1), torch.empty_like(q1)
+    bt, ctx, slots = _i32(c1.bt_p), _i32(w.context_lens), _i64(c1.sl_p)
+    key, val = dev_bf16(w.key), dev_bf16(w.value)
+    kw1 = {"k_scales": c1.dev[2], "v_scales": c1.dev[3]} if kv != "bf16" else {}
+    kw2 = {"k_scales": c2.dev[2], "v_scales": c2.dev[3]} if kv != "bf16" else {}
+    pa.pa_clear_device_error()
+    for _ in range(3):  # a few times, so that the second can start early
+        pa.pa_decode_step(out1, q1, c1.dev[0], c1.dev[1], bt, ctx, w.scale, key=key, value=val,
+                          slot_mapping=slots, partition_size=split, workspace=ws1,
+                          counters=cnt1, order=order, **kw1)
+        pa.pa_decode_step(out2, out1, c2.dev[0], c2.dev[1], bt, ctx, w.scale, key=key,
+                          value=val, slot_mapping=slots, partition_size=split, workspace=ws2,
+                          counters=cnt2, order=order, early_read=True, **kw2)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    c1.oracle_write(w.key, w.value, c1.sl_m)
+    c2.oracle_write(w.key, w.value, c2.sl_m)
+    assert_close(bf16_to_f64(out1), c1.oracle_decode(w.q), f"early-read chain {kv}: first")
+    q2 = host_bits(out1)
+    assert_close(bf16_to_f64(out2), c2.oracle_decode(q2), f"early-read chain {kv}: second")
