@@ -267,9 +267,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   const int rg = lane / L;
 
   // The context length, this warp's first 32 block ids and q are independent
-  // loads, so they go out together: the ids are read speculatively from the
-  // table slots this CTA may use (in bounds whatever the context length is)
-  // and only those below the context length are used, after a range check.
+  // loads, so they go out together (q after the first copies with early
+  // reads): the ids are read speculatively from the table slots this CTA may
+  // use (in bounds whatever the context length is) and only those below the
+  // context length are used, after a range check.
   const int64_t part_first = SPLIT ? static_cast<int64_t>(part) * p.partition_blocks : 0;
   const int tbl_end = SPLIT ? static_cast<int>(min(static_cast<int64_t>(p.max_blocks_per_seq),
                                                    part_first + p.partition_blocks))
