@@ -103,3 +103,29 @@ def test_workspace_bytes(lib):
     assert pa.pa_splitk_workspace_bytes(B, hq, d, 131072, 512) == 4 * B * hq * P * (d + 2)
     assert pa.pa_splitk_workspace_bytes(1, 1, 64, 1, 512) == 4 * 66
     assert pa.pa_splitk_workspace_bytes(1, 1, 64, 10, 0) == 0
+
+
+def test_decode_step_host_checks(lib):
+    # pa_decode_step's own checks (write arguments together, split-K
+    # workspace and counters, work order, flags); every call fails one of them
+    # before any CUDA call, so the fake addresses never reach a kernel.
+    f = ctypes.c_void_p(0x10000)
+
+    def call(out=f, key=f, value=f, slots=f, partition=512, ws=f, counters=f, maxp=4,
+             order=None, flags=0, num_seqs=2):
+        return lib.pa_decode_step(out, f, key, value, slots, f, f, f, 4, f, num_seqs, 32, 8,
+                                  128, 16, 10, 0.1, partition, ws, ws, ws, counters, maxp,
+                                  order, flags, None)
+
+    assert call(out=None) == pa.PA_ERR_INVALID_ARG
+    assert call(value=None) == pa.PA_ERR_INVALID_ARG            # key, value, slots together
+    assert call(slots=ctypes.c_void_p(0x10004)) == pa.PA_ERR_INVALID_ARG  # int64 slots aligned
+    assert call(partition=-16) == pa.PA_ERR_INVALID_ARG
+    assert call(partition=100) == pa.PA_ERR_INVALID_ARG         # not a multiple of 16
+    assert call(maxp=0) == pa.PA_ERR_INVALID_ARG
+    assert call(counters=None) == pa.PA_ERR_INVALID_ARG         # split-K needs counters
+    assert call(ws=None) == pa.PA_ERR_INVALID_ARG               # and a workspace
+    assert call(flags=2) == pa.PA_ERR_INVALID_ARG               # unknown flag bit
+    assert call(order=f, partition=0) == pa.PA_ERR_INVALID_ARG  # an order needs split-K
+    assert call(order=f, num_seqs=300, maxp=300) == pa.PA_ERR_UNSUPPORTED_SHAPE
+    assert call(num_seqs=0, out=None) == pa.PA_OK               # nothing to do
