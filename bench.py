@@ -528,10 +528,10 @@ def run_gpu(args):
     base = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         base = cpu_baseline(args.workload, args.cpu_seconds, args.kv)
-    if world > 1:
-        dist.init_process_group("nccl")
     device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
+    torch.cuda.set_device(device)  # before the process group, so NCCL binds this GPU
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
     from paged_kv_cache_283_gb300 import build as _b
     _b.build()
     pa.lib()
