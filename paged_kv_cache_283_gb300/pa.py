@@ -572,7 +572,10 @@ class DecodeStep:
     the whole-sequence kernel).  fused=True (the default) makes it one
     pa_decode_step launch (each slot must then be its sequence's position
     context_lens[b] - 1); fused=False, the separate cache-write, partition
-    and merge launches.
+    and merge launches.  With partition_size=None and host_context_lens (a
+    host copy of the lengths), the fused step picks its partition size and a
+    longest-first work order for those lengths (splitk_partition_size,
+    splitk_order); any other lengths stay correct, only the speed may differ.
 
     Every argument is checked and marshalled once, here; each call then makes
     two or three bare C calls, which keeps the host ahead of the GPU when a
@@ -584,7 +587,8 @@ class DecodeStep:
     def __init__(self, key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                  context_lens, out, scale, split=True, partition_size=512,
                  max_context_len=None, workspace=None, stream=None, k_scales=None,
-                 v_scales=None, fused=True, counters=None, order=None, early_read=False):
+                 v_scales=None, fused=True, counters=None, order=None, early_read=False,
+                 host_context_lens=None):
         torch = _torch()
         self.fused = bool(fused)
         if self.fused:
@@ -593,6 +597,26 @@ class DecodeStep:
             self.split = bool(split)
             B, hq, d = q.shape
             hkv = k_cache.shape[1]
+            if self.split and host_context_lens is not None and partition_size is None:
+                # chosen for these contexts: the partition size for a
+                # longest-first launch, and that order (host copy of the lengths)
+                import numpy as np
+                hctx = np.ascontiguousarray(host_context_lens, dtype=np.int32)
+                kind = ("fp8" if k_cache.dtype == torch.uint8 else
+                        "int8" if k_cache.dtype == torch.int8 else "bf16")
+                partition_size = splitk_partition_size(
+                    hctx, hq, hkv, d, kind,
+                    torch.cuda.get_device_properties(q.device).multi_processor_count,
+                    ordered=True)
+                if max_context_len is None:
+                    max_context_len = int(hctx.max()) if hctx.size else 1
+                maxp = max(1, -(-int(max_context_len) // partition_size))
+                if order is None and B * maxp <= 65535:
+                    order = torch.from_numpy(splitk_order(hctx, partition_size, maxp)).to(
+                        q.device)
+            elif partition_size is None:
+                partition_size = 512
+            self.partition_size = partition_size
             if self.split:
                 if workspace is None:
                     mc = (int(max_context_len) if max_context_len is not None
@@ -608,6 +632,8 @@ class DecodeStep:
             self._keep = [key, value, k_cache, v_cache, slot_mapping, q, block_tables,
                           context_lens, out, workspace, counters, k_scales, v_scales, order]
             return
+        if partition_size is None:
+            partition_size = 512
         T, hkv, d = key.shape
         nb, hkv2, bs, d2 = k_cache.shape
         if value.shape != key.shape or v_cache.shape != k_cache.shape or (hkv, d) != (hkv2, d2):

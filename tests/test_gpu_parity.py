@@ -394,3 +394,26 @@ def test_decode_step_object_matches_oracle(split, fused):
         ref = OA.decode(nq, kc_o, vc_o, bt_m, w.context_lens, w.scale, 16)
         assert_close(bf16_to_f64(out), ref, f"DecodeStep split={split} fused={fused} call {it}")
     _assert_no_device_error()
+
+
+@pytest.mark.parametrize("kv_len_case", ["mixed", "long"])
+def test_decode_step_object_auto_partition_and_order(kv_len_case):
+    # pa.DecodeStep with partition_size=None and the host lengths: the fused
+    # step picks its partition size and a longest-first order
+    lens = [300, 17, 1, 2049, 512, 96] if kv_len_case == "mixed" else [9000, 40, 4100, 700]
+    w = I.random_case(779 + len(lens), len(lens), lens, 32, 8, 128)
+    bt_m, sl_m, bt_p, sl_p = both_tables(w)
+    kc, vc = dev_bf16(w.k_cache), dev_bf16(w.v_cache)
+    key, val, q = dev_bf16(w.key), dev_bf16(w.value), dev_bf16(w.q)
+    out = torch.empty_like(q)
+    step = pa.DecodeStep(key, val, kc, vc, _dev_i64(sl_p), q, _dev_i32(bt_p),
+                         _dev_i32(w.context_lens), out, w.scale, partition_size=None,
+                         host_context_lens=w.context_lens)
+    assert step.partition_size in (256, 384, 512, 640, 768, 1024, 1536, 2048, 4096)
+    step()
+    torch.cuda.synchronize()
+    kc_o, vc_o = OC.reshape_and_cache(w.key, w.value, w.k_cache.copy(), w.v_cache.copy(), sl_m,
+                                      16, inplace=True)
+    ref = OA.decode(w.q, kc_o, vc_o, bt_m, w.context_lens, w.scale, 16)
+    assert_close(bf16_to_f64(out), ref, f"DecodeStep auto ({kv_len_case})")
+    _assert_no_device_error()
