@@ -16,7 +16,8 @@ steps, replayed as CUDA graphs with inputs resident in HBM and the pool
 rotated over replicas so that no step finds its K/V in L2.  ``roofline``
 reports the dominant kernel alone; ``e2e`` the same metric through the
 public API with host buffers and the copies inside the timed region;
-``cpu_baseline`` the float64 CPU oracle on one host core.
+``cpu_baseline`` the float64 CPU oracle on the host's cores (with a one-core
+run beside it).
 
 ``--impl reference`` times the CPU oracle (the only reference this method
 has) on the same workload and prints the same line with "impl": "reference".
@@ -38,6 +39,7 @@ if ROOT not in sys.path:
 METRIC = "paged decode-attention achieved HBM GB/s (frac of ~8 TB/s) and seq-layers/s"
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context only
+E2E_MIN_SECONDS = 0.25    # shortest end-to-end timed window
 
 
 # ---------------------------------------------------------------------------
@@ -56,6 +58,23 @@ def decode_bytes(ctx, num_seqs, hq, hkv, d, bs, kv_dtype="bf16"):
     kv = int(ctx.sum()) * hkv * per * 2
     qo = 2 * num_seqs * hq * d * 2
     tables = 4 * int((-(-ctx // bs)).sum()) + 4 * num_seqs
+    return kv + qo + tables
+
+
+def unique_decode_bytes(w, kv_dtype="bf16"):
+    """decode_bytes with every cached token counted once however many block
+    tables point at it: differs from decode_bytes only for the shared-prefix
+    workload, whose 1024-token prefix is one set of blocks read by every
+    sequence (logically once per sequence, from DRAM at least once)."""
+    import numpy as np
+    if not w.prefix_len:
+        return decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                            w.head_dim, w.block_size, kv_dtype)
+    per = (w.head_dim + 4) if kv_dtype in ("int8", "fp8") else 2 * w.head_dim
+    tokens = w.prefix_len + int((w.context_lens.astype(np.int64) - w.prefix_len).sum())
+    kv = tokens * w.num_kv_heads * per * 2
+    qo = 2 * w.num_seqs * w.num_q_heads * w.head_dim * 2
+    tables = 4 * int((-(-w.context_lens.astype(np.int64) // w.block_size)).sum()) + 4 * w.num_seqs
     return kv + qo + tables
 
 
@@ -200,7 +219,10 @@ def oracle_step_sample(idx, max_seconds, out_json=True, kv="bf16"):
     nbytes = decode_bytes(w.context_lens[:nseq], nseq, w.num_q_heads, w.num_kv_heads,
                           w.head_dim, w.block_size, kv) + cache_write_bytes(
                               nseq, w.num_kv_heads, w.head_dim, kv)
-    res = {"value": nbytes * reps / total / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+    threads = os.environ.get("OMP_NUM_THREADS", "")
+    cores = int(threads) if threads.isdigit() else os.cpu_count()
+    res = {"value": nbytes * reps / total / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+           "blas_threads": cores, "host_cpus": os.cpu_count(),
            "sample": f"first {nseq} of {w.num_seqs} sequences of the step (cache write + "
                      f"float64 decode, {kv} KV), {reps} repetitions, {total:.1f} s",
            "seconds_per_sample": total / reps, "seqs": nseq, "bytes_per_sample": nbytes}
@@ -209,16 +231,28 @@ def oracle_step_sample(idx, max_seconds, out_json=True, kv="bf16"):
     return res
 
 
-def cpu_baseline(idx, seconds, kv="bf16"):
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+def _oracle_process(idx, seconds, kv, threads):
+    """oracle_step_sample in a fresh process without CUDA, its BLAS (and
+    OpenMP) thread count set to ``threads``."""
+    t = str(threads)
+    env = dict(os.environ, OMP_NUM_THREADS=t, OPENBLAS_NUM_THREADS=t, MKL_NUM_THREADS=t,
                CUDA_VISIBLE_DEVICES="")
     code = ("import bench, sys; bench.oracle_step_sample(%d, %f, kv=%r)" % (idx, seconds, kv))
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True,
                        text=True, timeout=600)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle",
+        return {"value": None, "unit": UNIT, "cores": threads, "kind": "oracle",
                 "sample": "failed: " + r.stderr.strip().splitlines()[-1][:200]}
     return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(idx, seconds, kv="bf16"):
+    """The float64 oracle on the host: once with every host CPU available to
+    its BLAS (the reported baseline) and once on one thread (``one_core``)."""
+    ncpu = os.cpu_count() or 1
+    res = _oracle_process(idx, seconds, kv, ncpu)
+    res["one_core"] = _oracle_process(idx, seconds, kv, 1)
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -319,7 +353,11 @@ def combine_ranks(local_seconds, step_bytes, steps, world, device="cpu"):
 # ---------------------------------------------------------------------------
 # GPU arm
 
-def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
+def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None):
+    """Device inputs of a workload: block tables and slots from the library's
+    allocator, pool replicas (each larger than L2, or one pool per layer),
+    q and the new tokens' K/V.  max_layers (tests) builds only the first
+    layers of the 32-layer workload."""
     import numpy as np
     import torch
 
@@ -349,7 +387,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16"):
             torch.bfloat16)
 
     pool_bytes = 2 * w.k_cache.nbytes
-    layers = w.layers
+    layers = w.layers if max_layers is None else min(w.layers, max_layers)
     if layers > 1:
         # one pool per layer, each a seeded block permutation of the base pool
         base_k, base_v = bf(w.k_cache), bf(w.v_cache)
@@ -464,6 +502,42 @@ def _attn_fns(st, attn, partition, fused=True, order=None, early_read=False):
     return step, dominant, outs
 
 
+def step_launch(workload_idx, w, kv="bf16", step="fused", attn="auto", partition=None,
+                order="longest", early_read="on", num_sms=None):
+    """The launch arguments this benchmark times for a workload: attention
+    kind, fused or separate launches, partition size (and how it was chosen),
+    the host work order (numpy int32, or None for grid order) and whether the
+    fused launches read early.  The GPU parity tests run the same arguments.
+
+    * split-K for every workload (the shared-prefix batch too: one partition
+      per sequence there, 98 us vs 110 us whole-sequence);
+    * the partition size from pa_splitk_partition_size, except the
+      long-context workload, whose configuration fixes 512-token partitions;
+    * longest-first order when the fused step merges inside the launch
+      (plan_decode_step);
+    * early reads for fused launches: in this step sequence the kernel before
+      each launch is the previous layer's or step's, which writes only its own
+      pool (another replica or layer), so tables, lengths, order and this
+      launch's pool are not written by it (PA_STEP_EARLY_READ's contract)."""
+    from paged_kv_cache_283_gb300 import pa
+    attn = "splitk" if attn == "auto" else attn
+    fused = step == "fused"
+    choice = "given"
+    if partition is None and workload_idx == 3:
+        partition, choice = 512, "fixed by the workload"
+    plan = None
+    if attn == "splitk":
+        plan = pa.plan_decode_step(w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, kv,
+                                   num_sms, partition_size=partition,
+                                   order="longest" if fused and order == "longest" else "grid")
+        if plan.chosen:
+            choice = "pa_splitk_partition_size (makespan model)"
+        partition = plan.partition_size
+    return {"attn": attn, "fused": fused, "partition": partition, "partition_choice": choice,
+            "order": plan.order if plan is not None else None, "plan": plan,
+            "early_read": fused and early_read == "on"}
+
+
 def recorded_traffic(kernel, workload_name, partition, sources=("decode.cu", "decode_tile.cuh")):
     """DRAM bytes per launch from the committed ncu summaries, or None when the
     kernel source (the files ``sources``) or the launch shape changed since the
@@ -547,39 +621,13 @@ def run_gpu(args):
     st = _setup(args.workload, device, 4 * l2, args.kv)
     w = st["w"]
     stream = torch.cuda.Stream(device)
-    attn = args.attn
-    if attn == "auto":
-        # split-K with the chosen partition size also for the shared-prefix
-        # batch (one partition per sequence there: 98 us vs 110 us whole-sequence)
-        attn = "splitk"
-    fused = args.step == "fused"
-    ordered = fused and attn == "splitk" and args.order == "longest"
-    partition_choice = "given"
-    if args.partition is None:
-        if args.workload == 3:
-            args.partition = 512  # the long-context configuration fixes 512-token partitions
-            partition_choice = "fixed by the workload"
-        else:
-            args.partition = pa.splitk_partition_size(
-                w.context_lens, w.num_q_heads, w.num_kv_heads, w.head_dim, args.kv,
-                torch.cuda.get_device_properties(device).multi_processor_count, ordered=ordered)
-            partition_choice = "pa_splitk_partition_size (makespan model)"
-    order = None
-    if ordered:
-        maxp = max(1, -(-int(w.context_lens.max()) // args.partition))
-        # past 16 partitions per sequence (merged by a second launch) the items
-        # are nearly all full partitions: nothing to balance, and grid order
-        # measured faster (long context: 328.6 vs 336.0 us)
-        if w.num_seqs * maxp <= 65535 and maxp <= 16:
-            order = torch.from_numpy(pa.splitk_order(w.context_lens, args.partition, maxp)).to(
-                device)
-        else:
-            ordered = False
-    # Early reads: in this step sequence the kernel before each launch is the
-    # previous layer's or step's, which writes only its own pool (another
-    # replica or layer), so tables, lengths, order and this launch's pool are
-    # not written by it (the contract of PA_STEP_EARLY_READ).
-    early = fused and args.early_read == "on"
+    lp = step_launch(args.workload, w, args.kv, step=args.step, attn=args.attn,
+                     partition=args.partition, order=args.order, early_read=args.early_read,
+                     num_sms=torch.cuda.get_device_properties(device).multi_processor_count)
+    attn, fused, early = lp["attn"], lp["fused"], lp["early_read"]
+    args.partition, partition_choice = lp["partition"], lp["partition_choice"]
+    ordered = lp["order"] is not None
+    order = torch.from_numpy(lp["order"]).to(device) if ordered else None
     step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order, early)
 
     # eager warmup (sets kernel attributes, checks the error word)
@@ -594,7 +642,10 @@ def run_gpu(args):
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
-    # soak so that the clock sampler sees the GPU under this load
+    # soak under the same load right before the timed steps, so that the
+    # clock samples (every 200 ms) describe the clocks the steps ran at
+    time.sleep(0.3)
+    t_soak = time.time()
     soak = 0.0
     while soak < args.soak_seconds:
         soak += _time_graphs(graphs, 200, stream)
@@ -608,7 +659,9 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     sampler.stop()
-    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+    clocks = sampler.summary(t_soak, t1 + 0.05)
+    if clocks.get("window") == "timed region":
+        clocks["window"] = "%.2f s of soak under the same load + the timed steps" % soak
 
     # dominant kernel alone: graphs of back-to-back launches over the replicas
     def dom_all(r):
@@ -694,6 +747,18 @@ def run_gpu(args):
         "clocks": clocks,
         "gpu_launches": launches_per_step * args.steps,
     }
+    if w.prefix_len:
+        # shared prefix: the same time over unique bytes (the prefix once)
+        ub = unique_decode_bytes(w, args.kv)
+        if fused:
+            ub += cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim, args.kv)
+        step_unique = w.layers * (unique_decode_bytes(w, args.kv) + cache_write_bytes(
+            w.num_seqs, w.num_kv_heads, w.head_dim, args.kv))
+        res["unique_bytes_per_step"] = step_unique
+        res["value_unique"] = round(world * step_unique * args.steps / dt_max / 1e9, 1)
+        roofline["achieved_unique"] = round(ub / dom_dt / 1e9, 1)
+        roofline["frac_unique"] = round(ub / dom_dt / 1e9 / roofline["peak"], 4)
+        roofline["bytes_per_launch_unique"] = ub
     if base is not None:
         res["cpu_baseline"] = base
     if rank == 0:
@@ -780,7 +845,14 @@ def _e2e(st, attn, args, stream, order=None, early=False):
     for k in range(4):
         one(k)
     torch.cuda.synchronize()
-    n = args.steps
+    # at least E2E_MIN_SECONDS of steps (whatever --steps is), so that a short
+    # run still measures the loop in its steady state
+    t = time.perf_counter()
+    for k in range(20):
+        one(k)
+    torch.cuda.synchronize()
+    per = (time.perf_counter() - t) / 20
+    n = max(args.steps, int(E2E_MIN_SECONDS / max(per, 1e-7)) + 1)
     t = time.perf_counter()
     for k in range(n):
         one(k)
@@ -793,7 +865,7 @@ def _e2e(st, attn, args, stream, order=None, early=False):
     h2d = sum(t.numel() * t.element_size() for _, _, t in pieces)
     return {"value": round(step_bytes * n / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(sets[0]["hout"].numel() * 2),
-            "ms_per_step": dt / n * 1e3,
+            "ms_per_step": dt / n * 1e3, "steps": n, "seconds": round(dt, 3),
             "how": "pa.DecodeStep per layer (pre-marshalled C calls; %s); every step one pinned "
                    % ("one pa_decode_step launch" if args.step == "fused"
                       else "separate cache-write / attention / merge launches") +
@@ -973,7 +1045,9 @@ def run_prefill(args):
     dt = _time_graphs(graphs, steps, stream) / steps
     t1 = time.time()
     sampler.stop()
-    clocks = sampler.summary(t0 - 0.05, t1 + 0.05)
+    clocks = sampler.summary(t_soak, t1 + 0.05)
+    if clocks.get("window") == "timed region":
+        clocks["window"] = "%.2f s of soak under the same load + the timed steps" % soak
 
     # end to end through the public API: q from pinned host memory in, out back
     hq = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)

@@ -355,8 +355,11 @@ pa_status pa_decode_splitk_noalloc(void* out, const void* q, const void* k_cache
  *     more, the merge is a second launch, as pa_splitk_reduce.  counters:
  *     device uint32 [num_seqs * num_kv_heads], all zero before the first call;
  *     each call leaves them zero again, unless it sets PA_DEVERR_WAIT_TIMEOUT
- *     (then zero them before the next call).  Concurrent calls must not
- *     share counters or workspace.
+ *     or PA_DEVERR_ORDER: then a (sequence, KV head) may have missed an
+ *     arrival and its counter stays nonzero, and the next call with those
+ *     counters would merge before all partitions are written -- zero them
+ *     before the next call.  Concurrent calls must not share counters or
+ *     workspace.
  *   order (split-K only, may be NULL): device int32 [num_seqs * max_partitions],
  *     a permutation of the items item = part * num_seqs + b, the order in
  *     which the block scheduler receives the (sequence, partition) CTAs
@@ -419,8 +422,9 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
  *   max_query_len     : host bound on every n_b (sizes the grid; longer
  *                       chunks are cut at it).
  *   k_cache, v_cache, block_tables, context_lens: as pa_decode.
- * Runs on the tensor cores (tcgen05, bf16 in, fp32 accumulate; P is rounded to
- * bf16 before the PV product).  head_dim 128, block_size 16, Hq / Hkv in
+ * Runs on the tensor cores (tcgen05, bf16 in, fp32 accumulate; the softmax
+ * weights P enter the PV product as two bf16 parts, hi = P truncated to bf16
+ * and lo = bf16(P - hi), one MMA each, so they keep about 16 bits).  head_dim 128, block_size 16, Hq / Hkv in
  * {1, 2, 4, 8} (else PA_ERR_UNSUPPORTED_SHAPE); num_seqs <= 65535.  Device-side
  * checks: 0 <= n_b <= ctx_b <= max_blocks_per_seq * 16 and rows within T (else
  * PA_DEVERR_CONTEXT_LEN and the sequence is skipped); bad block ids as

@@ -24,8 +24,11 @@
 //    head; the softmax is online per warp in base-2 units (q is pre-scaled
 //    by scale*log2 e); P is handed to the PV loop through a 256-byte smem
 //    buffer; warps merge (m, l, acc) through shared memory at the end.
-//  * Split-K writes per-partition (m, l, o/l) in fp32; a second small kernel
-//    (splitk_reduce.cu) merges partitions by the log-sum-exp identity.
+//  * Split-K writes per-partition (m, l, o/l) in fp32, merged by the
+//    log-sum-exp identity either by a second small kernel (splitk_reduce.cu,
+//    pa_decode_splitk + pa_splitk_reduce) or, in the fused decode step with
+//    at most 16 partitions per sequence, inside the same launch by the last
+//    CTA of each (sequence, KV head) to finish.
 //  * Every device-resident index is checked: bad block ids read block 0 and
 //    set PA_DEVERR_BLOCK_ID; bad context lengths are clamped; every mbarrier
 //    wait is bounded.  Nothing traps.

@@ -385,6 +385,77 @@ def step_counters(num_seqs, num_kv_heads, device="cuda"):
     return torch.zeros(num_seqs * num_kv_heads, dtype=torch.int32, device=device)
 
 
+# Past this many partitions per sequence a split-K pa_decode_step merges in a
+# second launch, the items are nearly all full partitions and the
+# longest-first order has nothing to balance (long contexts measured slower
+# with it: 336.0 vs 328.3 us), so plan_decode_step keeps grid order there.
+ORDER_MAX_PARTITIONS = 16
+
+
+class StepPlan:
+    """Launch arguments of a split-K pa_decode_step for one batch's contexts:
+    partition_size, max_partitions (the workspace's P) and order (host
+    numpy int32 [B * max_partitions], longest first, or None for grid
+    order)."""
+
+    def __init__(self, partition_size, max_partitions, order, chosen):
+        self.partition_size = int(partition_size)
+        self.max_partitions = int(max_partitions)
+        self.order = order
+        self.chosen = bool(chosen)  # partition size from pa_splitk_partition_size
+
+    def __repr__(self):
+        return "StepPlan(partition_size=%d, max_partitions=%d, order=%s)" % (
+            self.partition_size, self.max_partitions,
+            "grid" if self.order is None else "longest first")
+
+
+def plan_decode_step(context_lens, num_q_heads, num_kv_heads, head_dim, kv="bf16",
+                     num_sms=None, partition_size=None, order="longest",
+                     max_context_len=None):
+    """Partition size, workspace partitions and work order of a split-K
+    pa_decode_step for the host context lengths ``context_lens``.
+
+    partition_size None: pa_splitk_partition_size's choice (for a
+    longest-first launch when ``order`` is "longest").  max_context_len (the
+    longest context the launch must cover; default: the longest of
+    context_lens) sets max_partitions.  order "longest": pa_splitk_order's
+    order for those partitions when a sequence has at most
+    ORDER_MAX_PARTITIONS of them (and the grid fits); otherwise, or with order
+    "grid", None.  Every sequence up to max_context_len tokens stays correct
+    under the plan whatever its length; other lengths change only the speed."""
+    import numpy as np
+    ctx = np.ascontiguousarray(context_lens, dtype=np.int32)
+    longest = order == "longest"
+    if order not in ("longest", "grid"):
+        raise ValueError("plan_decode_step: order is 'longest' or 'grid'")
+    chosen = partition_size is None
+    if chosen:
+        partition_size = splitk_partition_size(ctx, num_q_heads, num_kv_heads, head_dim, kv,
+                                               num_sms, ordered=longest)
+    mc = int(max_context_len) if max_context_len is not None else (
+        int(ctx.max()) if ctx.size else 1)
+    maxp = max(1, -(-mc // int(partition_size)))
+    arr = None
+    if longest and maxp <= ORDER_MAX_PARTITIONS and ctx.shape[0] * maxp <= 65535:
+        arr = splitk_order(ctx, partition_size, maxp)
+    return StepPlan(partition_size, maxp, arr, chosen)
+
+
+def recover_step_counters(counters):
+    """Re-zeroes a split-K pa_decode_step's arrival counters and clears the
+    device error word when it holds PA_DEVERR_ORDER or PA_DEVERR_WAIT_TIMEOUT
+    (a launch that raised either can leave a counter nonzero, and the next
+    launch with those counters would merge too early).  Reads the error word,
+    so it synchronises the device.  Returns the error bits it found."""
+    err = pa_get_device_error()
+    if err & (PA_DEVERR_ORDER | PA_DEVERR_WAIT_TIMEOUT):
+        counters.zero_()
+        _torch().cuda.synchronize()
+        pa_clear_device_error()
+    return err
+
+
 def _step_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, key, value,
                slot_mapping, partition_size, workspace, counters, k_scales, v_scales,
                order=None, early_read=False):
@@ -574,8 +645,12 @@ class DecodeStep:
     context_lens[b] - 1); fused=False, the separate cache-write, partition
     and merge launches.  With partition_size=None and host_context_lens (a
     host copy of the lengths), the fused step picks its partition size and a
-    longest-first work order for those lengths (splitk_partition_size,
-    splitk_order); any other lengths stay correct, only the speed may differ.
+    longest-first work order for those lengths (plan_decode_step), with the
+    workspace and order covering max_context_len tokens (default: the block
+    tables' capacity, max_blocks_per_seq * block_size); any lengths up to that
+    stay correct as they grow from call to call, only the speed may differ.
+    After a launch that raised PA_DEVERR_ORDER or PA_DEVERR_WAIT_TIMEOUT,
+    call recover() before the next one.
 
     Every argument is checked and marshalled once, here; each call then makes
     two or three bare C calls, which keeps the host ahead of the GPU when a
@@ -598,22 +673,22 @@ class DecodeStep:
             B, hq, d = q.shape
             hkv = k_cache.shape[1]
             if self.split and host_context_lens is not None and partition_size is None:
-                # chosen for these contexts: the partition size for a
-                # longest-first launch, and that order (host copy of the lengths)
-                import numpy as np
-                hctx = np.ascontiguousarray(host_context_lens, dtype=np.int32)
+                # chosen for these contexts (plan_decode_step): the partition
+                # size for a longest-first launch, and that order.  The
+                # workspace and the order cover the block tables' capacity
+                # unless max_context_len says less, so the contexts may grow
+                # from call to call up to that capacity.
                 kind = ("fp8" if k_cache.dtype == torch.uint8 else
                         "int8" if k_cache.dtype == torch.int8 else "bf16")
-                partition_size = splitk_partition_size(
-                    hctx, hq, hkv, d, kind,
-                    torch.cuda.get_device_properties(q.device).multi_processor_count,
-                    ordered=True)
                 if max_context_len is None:
-                    max_context_len = int(hctx.max()) if hctx.size else 1
-                maxp = max(1, -(-int(max_context_len) // partition_size))
-                if order is None and B * maxp <= 65535:
-                    order = torch.from_numpy(splitk_order(hctx, partition_size, maxp)).to(
-                        q.device)
+                    max_context_len = block_tables.shape[1] * k_cache.shape[2]
+                plan = plan_decode_step(
+                    host_context_lens, hq, hkv, d, kind,
+                    torch.cuda.get_device_properties(q.device).multi_processor_count,
+                    max_context_len=max_context_len)
+                partition_size = plan.partition_size
+                if order is None and plan.order is not None:
+                    order = torch.from_numpy(plan.order).to(q.device)
             elif partition_size is None:
                 partition_size = 512
             self.partition_size = partition_size
@@ -691,6 +766,14 @@ class DecodeStep:
         else:
             self._f_write, self._f_split, self._f_whole = (
                 L.pa_reshape_and_cache, L.pa_decode_splitk, L.pa_decode)
+
+    def recover(self):
+        """Reads the device error word (synchronises); after PA_DEVERR_ORDER
+        or PA_DEVERR_WAIT_TIMEOUT re-zeroes this step's arrival counters and
+        clears the word.  Returns the error bits found."""
+        if self.fused and self.split and self.counters is not None:
+            return recover_step_counters(self.counters)
+        return pa_get_device_error()
 
     def __call__(self, stream=None):
         s = self._stream if stream is None and self._stream is not None else _stream(stream)

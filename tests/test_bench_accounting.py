@@ -50,3 +50,21 @@ def test_prefill_flops_brute_force():
                 p = c - m + i
                 brute += 2 * (p + 1) * d * 2 * hq  # QK and PV over keys 0 .. p
         assert bench.prefill_flops(ctx, n, hq, d) == brute
+
+
+def test_unique_decode_bytes_shared_prefix():
+    # the shared-prefix batch: 128 sequences whose first 1024 tokens are one
+    # set of 64 blocks; unique K/V bytes count those tokens once, logical
+    # bytes once per sequence; q/out and table terms are the same
+    from paged_kv_cache_283_gb300 import inputs as I
+    w = I.shared_prefix(with_data=False)
+    assert w.prefix_len == 1024 and w.num_seqs == 128
+    suffix = int(w.context_lens.sum()) - 128 * 1024
+    logical = bench.decode_bytes(w.context_lens, 128, 32, 8, 128, 16)
+    unique = bench.unique_decode_bytes(w)
+    assert logical - unique == 127 * 1024 * 4096
+    assert unique == (1024 + suffix) * 4096 + 2 * 128 * 32 * 128 * 2 + \
+        4 * int(sum(-(-int(n) // 16) for n in w.context_lens)) + 4 * 128
+    # every other workload has nothing shared
+    w2 = I.llama8b_batch64(with_data=False)
+    assert bench.unique_decode_bytes(w2) == bench.decode_bytes(w2.context_lens, 64, 32, 8, 128, 16)

@@ -287,7 +287,85 @@ def test_fused_step_order_entry_out_of_range():
                       partition_size=split, workspace=ws, counters=counters, order=_i32(order))
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() & pa.PA_DEVERR_ORDER
+    # the displaced item never arrived, so a counter may be left nonzero:
+    # recovery re-zeroes them, and the next call (valid order, same counters
+    # and workspace) is exact again
+    assert pa.recover_step_counters(counters) & pa.PA_DEVERR_ORDER
+    assert int(counters.abs().sum().item()) == 0 and pa.pa_get_device_error() == 0
+    good = _i32(pa.splitk_order(w.context_lens, split, maxp))
+    pa.pa_decode_step(out, q, c.dev[0], c.dev[1], _i32(c.bt_p), _i32(w.context_lens), w.scale,
+                      partition_size=split, workspace=ws, counters=counters, order=good)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert_close(bf16_to_f64(out), c.oracle_decode(w.q), "call after recovering the counters")
+    assert int(counters.abs().sum().item()) == 0
+
+
+def test_decode_step_object_contexts_grow_past_the_first_plan():
+    """DecodeStep with partition_size=None plans its partition size and order
+    from the first call's contexts (4 sequences of at most 100 tokens: one
+    256-token partition each), but its workspace and order cover the block
+    tables' capacity (1024 tokens), so later calls whose contexts grow to 3
+    and 4 partitions stay exact.  Each call appends one token per sequence
+    (after reserving the positions skipped) and is checked against the
+    oracle."""
+    from oracle.allocator import BlockAllocatorModel
+    nb, hkv, hq, d, cap = 320, 8, 32, 128, 64
+    rng = np.random.default_rng(6700)
+    free = rng.permutation(nb).astype(np.int32)
+    kc_h = I.normal_bf16(rng, (nb, hkv, 16, d))
+    vc_h = I.normal_bf16(rng, (nb, hkv, 16, d))
+    plan_ctx = [[40, 17, 100, 64], [300, 18, 600, 65], [700, 19, 1024, 300]]
+    a = pa.BlockAllocator(nb, 16, free)
+    m = BlockAllocatorModel(nb, 16, free)
+    B = len(plan_ctx[0])
+    for al in (a, m):
+        for b in range(B):
+            al.add_seq(b)
+    kc, vc = dev_bf16(kc_h), dev_bf16(vc_h)
+    q = torch.empty(B, hq, d, dtype=torch.bfloat16, device="cuda")
+    key = torch.empty(B, hkv, d, dtype=torch.bfloat16, device="cuda")
+    val = torch.empty_like(key)
+    out = torch.empty_like(q)
+    bt_d = torch.zeros(B, cap, dtype=torch.int32, device="cuda")
+    ctx_d = torch.zeros(B, dtype=torch.int32, device="cuda")
+    slots_d = torch.zeros(B, dtype=torch.int64, device="cuda")
+    step = None
     pa.pa_clear_device_error()
+    for it, ctx in enumerate(plan_ctx):
+        ctx = np.array(ctx, dtype=np.int32)
+        for b in range(B):
+            grow = int(ctx[b]) - 1 - a.seq_len(b)
+            a.reserve(b, grow)
+            m.reserve(b, grow)
+        slots, _, _ = a.append_slots(list(range(B)))
+        slots_m = np.array([x[0] for x in m.append_slots(range(B))], dtype=np.int64)
+        bt, ctx_a = a.block_tables(list(range(B)), cap)
+        bt_m = np.full_like(bt, -1)
+        for b in range(B):
+            t = m.block_table(b)
+            bt_m[b, :len(t)] = t
+        assert np.array_equal(slots, slots_m) and np.array_equal(bt, bt_m)
+        assert np.array_equal(ctx_a, ctx)
+        nq, nk, nv = (I.normal_bf16(rng, (B, hq, d)), I.normal_bf16(rng, (B, hkv, d)),
+                      I.normal_bf16(rng, (B, hkv, d)))
+        q.copy_(dev_bf16(nq))
+        key.copy_(dev_bf16(nk))
+        val.copy_(dev_bf16(nv))
+        bt_d.copy_(torch.from_numpy(np.maximum(bt, 0)))
+        ctx_d.copy_(torch.from_numpy(ctx))
+        slots_d.copy_(torch.from_numpy(slots))
+        if step is None:
+            step = pa.DecodeStep(key, val, kc, vc, slots_d, q, bt_d, ctx_d, out, 1 / np.sqrt(d),
+                                 partition_size=None, host_context_lens=ctx)
+            assert step.partition_size == 256
+            assert step.workspace[1].shape[2] == cap * 16 // 256
+        step()
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0, f"call {it}"
+        kc_h, vc_h = OC.reshape_and_cache(nk, nv, kc_h, vc_h, slots_m, 16)
+        ref = OA.decode(nq, kc_h, vc_h, bt_m, ctx, 1 / np.sqrt(d), 16)
+        assert_close(bf16_to_f64(out), ref, f"DecodeStep call {it}, contexts {ctx.tolist()}")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "int8"])

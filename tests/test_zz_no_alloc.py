@@ -7,10 +7,13 @@ workspace in a fixed array inside libpa.so.  The test calls it through the C
 ABI twice in a row (different inputs and shapes, so the second call runs on
 top of the first call's leftover partials) and checks each output against the
 regular pa_decode_splitk + pa_splitk_reduce with a caller-allocated
-workspace, under the same tolerance the parity tests use.  It also checks
-that a call needing more than the built-in workspace is refused before any
-launch.  The file sorts last so that a run stopping at the first failure has
-run every other test already.
+workspace and against the float64 oracle, under the same tolerance the
+parity tests use.  It also checks that a call needing more than the built-in
+workspace is refused before any launch, and that a context longer than the
+caller's max_context_len is reported (PA_DEVERR_CONTEXT_LEN) and only its
+first partitions are attended, the rest of the batch unaffected.  The file
+sorts last so that a run stopping at the first failure has run every other
+test already.
 """
 import ctypes
 
@@ -19,6 +22,7 @@ import pytest
 
 torch = pytest.importorskip("torch")
 
+from oracle import attention as OA
 from paged_kv_cache_283_gb300 import inputs as I
 from paged_kv_cache_283_gb300 import pa
 
@@ -54,9 +58,14 @@ def _noalloc_c_abi(q, kc, vc, bt, ctx, scale, max_ctx, partition):
     return out
 
 
-def _case(w):
+def _tables(w):
     bt, _ = model_tables(w, step_append=False)
     bt[bt < 0] = 0
+    return bt
+
+
+def _case(w):
+    bt = _tables(w)
     return (dev_bf16(w.q), dev_bf16(w.k_cache), dev_bf16(w.v_cache), _dev_i32(bt),
             _dev_i32(w.context_lens), w.scale, int(w.context_lens.max()))
 
@@ -71,7 +80,27 @@ def test_noalloc_matches_regular_split_k_twice_in_a_row():
         want = _regular(q, kc, vc, bt, ctx, scale, max_ctx, partition)
         torch.cuda.synchronize()
         assert_close(bf16_to_f64(got), bf16_to_f64(want), f"no-alloc vs regular, {w.name}")
+        ref = OA.decode(w.q, w.k_cache, w.v_cache, _tables(w), w.context_lens, w.scale, 16)
+        assert_close(bf16_to_f64(got), ref, f"no-alloc vs oracle, {w.name}")
     assert pa.pa_get_device_error() == 0
+
+
+def test_noalloc_context_beyond_max_context_len():
+    """max_context_len 512 at partition 256 sizes the built-in workspace for
+    two partitions per sequence; a 700-token context raises
+    PA_DEVERR_CONTEXT_LEN and attends only its first 512 tokens (the excess
+    is dropped); the other sequences are exact."""
+    ctx = np.array([100, 700, 512, 1], dtype=np.int32)
+    w = I.random_case(4444, len(ctx), ctx, 32, 8, 128)
+    q, kc, vc, bt, ctx_d, scale, _ = _case(w)
+    pa.pa_clear_device_error()
+    got = _noalloc_c_abi(q, kc, vc, bt, ctx_d, scale, 512, 256)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_CONTEXT_LEN
+    pa.pa_clear_device_error()
+    seen = np.minimum(ctx, 512)
+    ref = OA.decode(w.q, w.k_cache, w.v_cache, _tables(w), seen, w.scale, 16)
+    assert_close(bf16_to_f64(got), ref, "no-alloc, one context beyond max_context_len")
 
 
 def test_noalloc_refuses_more_than_its_workspace():
