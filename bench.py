@@ -427,7 +427,10 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None):
         def int8_pool():
             nb = w.num_blocks
             shape = (nb, w.num_kv_heads, w.block_size, w.head_dim)
-            return (codes(shape), codes(shape),
+            v = codes(shape)
+            if kv_dtype == "int8":  # V bytes are stored offset binary (code + 128)
+                v = torch.bitwise_xor(v, torch.tensor(-128, dtype=torch.int8, device=device))
+            return (codes(shape), v,
                     torch.rand(shape[:3], generator=gen, device=device) * lo / 2 + lo,
                     torch.rand(shape[:3], generator=gen, device=device) * lo / 2 + lo)
         pool_bytes = 2 * w.num_blocks * w.num_kv_heads * w.block_size * (w.head_dim + 4)

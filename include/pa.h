@@ -182,18 +182,24 @@ pa_status pa_decode(void* out, const void* q, const void* k_cache,
  *   k_cache, v_cache   : [num_blocks, num_kv_heads, block_size, head_dim] int8
  *   k_scales, v_scales : [num_blocks, num_kv_heads, block_size] fp32
  * 2 * (head_dim + 4) bytes per token and KV head instead of 4 * head_dim.
- * v_cache only: inside each (block, head) tile of block_size * head_dim bytes,
- * seen as 128-byte lines of eight 16-byte units, logical unit u of line L is
- * stored at unit u ^ ((2 * L) & 7) (for head_dim 128 a line is one token, so
- * token t's dims [16u, 16u + 16) sit at byte 16 * (u ^ (2t & 7)) of its row).
- * The permutation lets the decode read V for its tensor-core MMAs without
- * shared-memory bank conflicts; whole-block copies (pa_copy_blocks) are
- * unaffected.  k_cache is plain row-major.
+ * k_cache is plain row-major.  v_cache holds each (block, head) tile of
+ * 16 * D bytes (D = head_dim) transposed, for the decode's tensor-core PV:
+ * the code of token t (0..15) and dim d sits at byte
+ *   L * (D / 2) + 16 * ((w / 4) XOR f) + 4 * (w % 4) + y
+ * of the tile, with r = d % 16, L = 4 * (r % 8) + (t % 8) / 2,
+ * w = 2 * (d / 16) + r / 8, y = (t % 2) + 2 * (t / 8), and
+ * f = (L / 2) % 4 for D = 128, (L / 4) % 2 for D = 64; and an INT8 V byte is
+ * the code plus 128 (offset binary: uint8 0..254 for codes -127..127).  Lane L
+ * of a decoding warp then finds, in one 32-bit word per dim it feeds to the
+ * MMA, that dim's codes of the 4 tokens it feeds, with no shared-memory bank
+ * conflicts.  Whole-block copies (pa_copy_blocks) are unaffected.
  * Decode quantises each query head the same way and takes QK as an integer
  * dot product, s_j = scale * scale_q * k_scale_j * sum_d q_code_d * k_code_jd
  * (exact in int32); PV weights w_j = softmax weight j * v_scale_j mix the V
- * codes with fp32 accumulation (each weight carried as a sum of two tf32
- * parts, ~2^-21 relative).  head_dim 64 or 128; otherwise as the bf16 calls.
+ * codes on the tensor cores with fp32 accumulation (each weight, divided by
+ * a power of two bounding the V scales seen so far, carried as an f16 hi part
+ * plus an f16 lo part, ~2^-22 relative).  head_dim 64 or 128; otherwise as
+ * the bf16 calls.
  */
 pa_status pa_reshape_and_cache_int8(const void* key, const void* value,
                                     int8_t* k_cache, int8_t* v_cache,
@@ -226,12 +232,15 @@ pa_status pa_decode_splitk_int8(float* ws_out, float* ws_m, float* ws_l,
  * (token, KV head) row:
  *   scale = max|x| / 448,  code = E4M3(x / scale) round to nearest even,
  *   saturated to +-448 (fp32 arithmetic; scale 0 and codes 0 for an all-zero row).
- * Pools, scales, the V tile's unit permutation and sizes exactly as the INT8
- * cache, with uint8 codes.  Decode keeps q unquantised: scores are
- * scale * q . (decode(k_code) * k_scale) in fp32 (the codes are exact in fp32);
- * PV as the INT8 decode (weights times v_scale, tf32 hi + lo on the tensor
- * cores, exact codes).  A token past the context is masked by position; its
- * codes may be NaN and are never multiplied.  head_dim 64 or 128.
+ * Pools, scales, the transposed V tile and sizes exactly as the INT8 cache,
+ * with uint8 codes (V codes stored as they are, not offset).  Decode keeps q
+ * unquantised: scores are scale * q . (decode(k_code) * k_scale) with fp32
+ * accumulation, taken on the tensor cores in E4M3 with each query head, times
+ * a power of two, split into two E4M3 parts q1 + 2^-5 q2 (exact for bf16 q up
+ * to about 2^-21 of the head's largest |q|); PV as the INT8 decode (weights times
+ * v_scale, f16 hi + lo on the tensor cores, exact codes).  A token past the
+ * context is masked by position; its codes may be NaN and are never
+ * multiplied.  head_dim 64 or 128.
  */
 pa_status pa_reshape_and_cache_fp8(const void* key, const void* value,
                                    uint8_t* k_cache, uint8_t* v_cache,

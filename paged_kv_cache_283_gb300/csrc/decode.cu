@@ -170,18 +170,15 @@ __device__ __forceinline__ bool fused_cache_write(const DecodeParams& p, int b, 
     constexpr int PER = D / 32;
     float ks, vs;
     const uint32_t kc = quantise_row<D, Q == 2>(kw, &ks);
-    const uint32_t vc = quantise_row<D, Q == 2>(vw, &vs);
+    const uint32_t vc = v_stored<Q == 2>(quantise_row<D, Q == 2>(vw, &vs));
     int8_t* k8 = const_cast<int8_t*>(p.k8) + srow * D;
-    int8_t* v8 = const_cast<int8_t*>(p.v8) + srow * D;
-    const int vcol = v_code_col<D>(off, lane * PER);
+    store_v_row_bytes<D>(const_cast<int8_t*>(p.v8) + (srow - off) * D, off, lane, vc);
     if constexpr (PER == 4) {
       *reinterpret_cast<uint32_t*>(k8 + lane * PER) = kc;
-      *reinterpret_cast<uint32_t*>(v8 + vcol) = vc;
       *reinterpret_cast<uint32_t*>(stage + lane * PER) = kc;      // K codes
-      *reinterpret_cast<uint32_t*>(stage + D + lane * PER) = vc;  // V codes, logical order
+      *reinterpret_cast<uint32_t*>(stage + D + lane * PER) = vc;  // V bytes, logical dim order
     } else {
       *reinterpret_cast<uint16_t*>(k8 + lane * PER) = static_cast<uint16_t>(kc);
-      *reinterpret_cast<uint16_t*>(v8 + vcol) = static_cast<uint16_t>(vc);
       *reinterpret_cast<uint16_t*>(stage + lane * PER) = static_cast<uint16_t>(kc);
       *reinterpret_cast<uint16_t*>(stage + D + lane * PER) = static_cast<uint16_t>(vc);
     }
@@ -197,7 +194,8 @@ __device__ __forceinline__ bool fused_cache_write(const DecodeParams& p, int b, 
 
 // Patches the staged new row (fused_cache_write) into row `off` of a landed
 // tile: K tile, V tile, and for the 1-byte caches the two scales.  The stage
-// holds the 1-byte V codes in logical order; the tile, as stored.
+// holds the 1-byte V bytes (as stored) in logical dim order; the tile holds
+// them transposed.
 template <int D, int Q>
 __device__ __forceinline__ void patch_tile(unsigned char* tile, int kt_bytes,
                                            const unsigned char* stage, int off, int lane) {
@@ -208,19 +206,18 @@ __device__ __forceinline__ void patch_tile(unsigned char* tile, int kt_bytes,
           reinterpret_cast<const uint4*>(stage)[lane];
   } else {
     constexpr int PER = D / 32;
-    // the lane's PER codes of the K row, and of the V row at their stored place
-    // (v_code_col may move them into the neighbouring row's bytes at D = 64)
-    const int vcol = v_code_col<D>(off, lane * PER);
+    // the lane's PER codes of the K row, and its V bytes at their places in
+    // the transposed V tile
     if constexpr (PER == 4) {
       *reinterpret_cast<uint32_t*>(tile + off * D + lane * PER) =
           *reinterpret_cast<const uint32_t*>(stage + lane * PER);
-      *reinterpret_cast<uint32_t*>(tile + kt_bytes + off * D + vcol) =
-          *reinterpret_cast<const uint32_t*>(stage + D + lane * PER);
+      store_v_row_bytes<D>(tile + kt_bytes, off, lane,
+                           *reinterpret_cast<const uint32_t*>(stage + D + lane * PER));
     } else {
       *reinterpret_cast<uint16_t*>(tile + off * D + lane * PER) =
           *reinterpret_cast<const uint16_t*>(stage + lane * PER);
-      *reinterpret_cast<uint16_t*>(tile + kt_bytes + off * D + vcol) =
-          *reinterpret_cast<const uint16_t*>(stage + D + lane * PER);
+      store_v_row_bytes<D>(tile + kt_bytes, off, lane,
+                           *reinterpret_cast<const uint16_t*>(stage + D + lane * PER));
     }
     if (lane == 0) {
       float* sc = reinterpret_cast<float*>(tile + 2 * kt_bytes);  // 16 K then 16 V scales
@@ -291,57 +288,78 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   float2 q2[G][4];
   int qc[G][IG::QW];  // int8 cache: this lane's q codes, 4 per word
   float qsc[G];       // int8 cache: q scale times scale * log2(e)
-  uint32_t qf[D / 16][2];  // fp8 cache: q's MMA fragments (tile_step_f8), f16 pairs
-  float2 qfac;             // fp8 cache: per-head factor of heads 2 tig, 2 tig + 1
+  uint32_t qe[QCols<G>::NQ][D / 32][2];  // fp8 cache: q's E4M3 MMA fragments (tile_step_f8)
+  float2 qfac;  // fp8 cache: 2^-k * scale * log2 e of the lane's two score heads
   // q of the group into this lane's registers (or, for the int8 cache,
   // quantised through shared memory): the inputs a preceding kernel may
   // still be writing, so with early reads this runs after the wait.
   auto load_q = [&]() {
     if constexpr (Q == 2) {
-      // Lane (gid, tig) holds head gid's dims [(D/4) tig, +D/4) (zeros for gid >= G),
-      // times 2^k with k per head chosen so that the head's largest |q| lands in
-      // [2^14, 2^15): every bf16 value then converts to f16 exactly unless it is
-      // below 2^-14 (an absolute error under 2^-25 of that maximum), and the
-      // products with codes (|x| <= 448) stay far inside fp32.  qfac carries
-      // 2^-k * scale * log2 e back onto the scores.
+      // Lane (gid, tig) builds MMA column gid's fragments: head hn = head(gid),
+      // dims [(D/4) tig, +D/4).  The head's values times 2^k, k chosen per head
+      // so that its largest |q| lands in [128, 256), are split into two E4M3
+      // parts, x = q1 + 2^-5 q2 with q1 = E4M3(x), q2 = E4M3(32 (x - q1)): a
+      // bf16 value has 8 significant bits and q1 keeps 4 of them, and
+      // |x - q1| <= 8 (half a step of q1 below 256), so 32 (x - q1) <= 256 is
+      // exact in q2 except where it falls below E4M3's normal range: an error
+      // under 2^-14 absolute, about 2^-21 of the head's largest |q|.  G <= 4:
+      // column gid carries part(gid) (parts >= 2 are zeros); G = 8: both parts,
+      // one fragment set each.  Step s's fragment words are dims (D/4) tig + 8s
+      // + 0..3 and + 4..7.
+      using C = QCols<G>;
       constexpr int E = D / 4;
       const int gid = lane >> 2, tig = lane & 3;
+      const int hn = C::head(gid);
       float f[E];
-      float amax = 0.f;
-      if (gid < G) {
-        const __nv_bfloat16* qh =
-            p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + gid) * D +
-            E * tig;
+      const __nv_bfloat16* qh =
+          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + hn) * D +
+          E * tig;
   #pragma unroll
-        for (int u = 0; u < E / 8; ++u) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
-          const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
-          const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
-          f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
-          f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
-        }
-      } else {
-  #pragma unroll
-        for (int k = 0; k < E; ++k) f[k] = 0.f;
+      for (int u = 0; u < E / 8; ++u) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+        const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
+        f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
+        f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
       }
+      float amax = 0.f;
   #pragma unroll
       for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
       amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-      // biased exponent of amax (0 for 0 and subnormals); k = 14 - unbiased
+      // biased exponent of amax (0 for 0 and subnormals); k = 7 - unbiased
       const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-      const int kexp = min(127, max(-126, 141 - ebits));
+      const int kexp = min(127, max(-126, 134 - ebits));
       const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
+      const int pn = C::part(gid);
   #pragma unroll
-      for (int s2 = 0; s2 < D / 16; ++s2) {
-        const __half2 lo = __floats2half2_rn(f[4 * s2] * up, f[4 * s2 + 1] * up);
-        const __half2 hi = __floats2half2_rn(f[4 * s2 + 2] * up, f[4 * s2 + 3] * up);
-        qf[s2][0] = *reinterpret_cast<const uint32_t*>(&lo);
-        qf[s2][1] = *reinterpret_cast<const uint32_t*>(&hi);
+      for (int j = 0; j < E / 4; ++j) {
+        uint32_t w1 = 0, w2 = 0;
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float x0 = f[4 * j + 2 * h] * up, x1 = f[4 * j + 2 * h + 1] * up;
+          const __nv_fp8x2_storage_t c1 =
+              __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw r1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+          __half2 r1h;
+          r1h = *reinterpret_cast<const __half2*>(&r1);
+          const float2 q1 = __half22float2(r1h);
+          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
+              make_float2((x0 - q1.x) * 32.f, (x1 - q1.y) * 32.f), __NV_SATFINITE, __NV_E4M3);
+          w1 |= static_cast<uint32_t>(c1) << (16 * h);
+          w2 |= static_cast<uint32_t>(c2) << (16 * h);
+        }
+        if constexpr (C::PACKED) {
+          qe[0][j / 2][j % 2] = pn == 0 ? w1 : (pn == 1 ? w2 : 0u);
+        } else {
+          qe[0][j / 2][j % 2] = w1;
+          qe[C::NQ - 1][j / 2][j % 2] = w2;
+        }
       }
-      const float fac = gid < G ? ldexpf(p.scale_log2, -kexp) : 0.f;
-      qfac = make_float2(__shfl_sync(kFullMask, fac, 8 * tig),
-                         __shfl_sync(kFullMask, fac, 8 * tig + 4));
+      const float fac = ldexpf(p.scale_log2, -kexp);
+      const int ha = C::head(2 * tig);
+      qfac = make_float2(__shfl_sync(kFullMask, fac, 4 * ha),
+                         __shfl_sync(kFullMask, fac, 4 * (ha + 1)));
     } else if constexpr (Q == 0) {
       const __nv_bfloat16* qb =
           p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
@@ -509,7 +527,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   for (int g = 0; g < G; ++g)
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[g][k] = make_float2(0.f, 0.f);
-  float acc8[D / 16][4];  // int8 cache: MMA accumulators (pv_i8_mma's layout)
+  float acc8[D / 16][4];  // 1-byte caches: PV accumulators (pv_f16's layout)
 #pragma unroll
   for (int c = 0; c < D / 16; ++c)
 #pragma unroll
@@ -518,6 +536,9 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   float l_run = 0.f;        // this lane's share of that head's exp-sum
   float2 m_run2 = make_float2(-INFINITY, -INFINITY);  // fp8 cache: heads 2 tig, 2 tig + 1
   float2 l_run2 = make_float2(0.f, 0.f);
+  // 1-byte caches: the warp's power-of-two bound on the V scales it has
+  // weighted (raise_v_bound) and its reciprocal; acc8 is in units of it
+  float vbound = 0x1p-126f, vinv = 0x1p126f;
   // The lane geometry of the scores and softmax state: the bf16 step's, or
   // the int8 QK geometry.
   constexpr int SL = QI ? IG::QL : L;
@@ -566,17 +587,19 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       if constexpr (QI) {
         if (nvalid == BS)
           tile_step_i8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                   m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
+                                   m_run, l_run, vbound, vinv, nvalid, lane, qsub, qrg, my_head,
+                                   my_i0);
         else
           tile_step_i8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                    m_run, l_run, nvalid, lane, qsub, qrg, my_head, my_i0);
+                                    m_run, l_run, vbound, vinv, nvalid, lane, qsub, qrg, my_head,
+                                    my_i0);
       } else {
         if (nvalid == BS)
-          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, qf, qfac, acc8, m_run2,
-                                   l_run2, nvalid, lane);
+          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, qe, qfac, acc8, m_run2,
+                                   l_run2, vbound, vinv, nvalid, lane);
         else
-          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, qf, qfac, acc8, m_run2,
-                                    l_run2, nvalid, lane);
+          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, qe, qfac, acc8, m_run2,
+                                    l_run2, vbound, vinv, nvalid, lane);
       }
     }
     consumed = i + 1;
@@ -638,17 +661,26 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       }
     }
   } else {
-    // the MMAs already summed over tokens: lane (gid, tig) holds heads 2 tig,
-    // 2 tig + 1 at dims [(D/8) gid, +D/8) (see pv_i8_mma)
-    const int gid = lane >> 2, h0 = 2 * (lane & 3);
+    // acc8: (dims 16c + gid, 16c + gid + 8; columns 2 tig, 2 tig + 1), in
+    // units of the warp's V-scale bound; G <= 4: each head's hi and lo parts
+    // sit in the lanes tig and tig ^ G / 2 and are summed here
+    using C = QCols<G>;
+    if constexpr (C::PACKED) {
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      if (h0 + hh < G) {
-        float4* dst = reinterpret_cast<float4*>(mrg + (h0 + hh) * D + (D / 8) * gid);
+      for (int c = 0; c < D / 16; ++c)
 #pragma unroll
-        for (int k = 0; k < D / 32; ++k)
-          dst[k] = make_float4(acc8[2 * k][hh], acc8[2 * k][2 + hh], acc8[2 * k + 1][hh],
-                               acc8[2 * k + 1][2 + hh]);
+        for (int k = 0; k < 4; ++k) acc8[c][k] += __shfl_xor_sync(kFullMask, acc8[c][k], G / 2);
+    }
+    const int gid = lane >> 2, tig = lane & 3;
+    if (C::part0(tig)) {
+      const int ha = C::head(2 * tig);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        const int d0 = 16 * c + gid;
+        mrg[ha * D + d0] = acc8[c][0] * vbound;
+        mrg[(ha + 1) * D + d0] = acc8[c][1] * vbound;
+        mrg[ha * D + d0 + 8] = acc8[c][2] * vbound;
+        mrg[(ha + 1) * D + d0 + 8] = acc8[c][3] * vbound;
       }
     }
   }

@@ -163,7 +163,9 @@ namespace pa {
 // registers, so a pass covers 32/QL rows and the butterfly that completes the
 // partial dots has only log2(QL) levels (QL = 4: 2 levels; the bf16 step
 // needs 4).  The K and q scales are applied once per score.  PV runs on the
-// tensor cores (pv_q_mma) with the V scale folded into each softmax weight.
+// tensor cores (pv_f16) with the V scale folded into each softmax weight.
+// (INT8 tensor-core MMAs do no more multiply-adds per cycle than dp4a on this
+// GPU, measured, so QK stays on dp4a.)
 template <int D, int G>
 struct I8Geometry {
   static constexpr int BS = kBlockSize;
@@ -207,139 +209,184 @@ __device__ __forceinline__ void i8_load_row(const unsigned char* row, int qsub, 
   }
 }
 
-// One m16n8k8 tf32 tensor-core step, fp32 accumulate: c += a · b.
-__device__ __forceinline__ void mma_tf32(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, "
+// One m16n8k16 f16 tensor-core step, fp32 accumulate: c += a · b.
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
       "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-__device__ __forceinline__ uint32_t to_tf32(float x) {
+// One m16n8k32 E4M3 tensor-core step, fp32 accumulate: c += a · b.
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2 E4M3 codes (16 bits, first code in the low byte) to an f16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t h) {
+  const __half2_raw r =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
+  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+}
+
+// Two offset-binary INT8 V codes (bytes SEL picks: 0x4140 -> bytes 0, 1;
+// 0x4342 -> bytes 2, 3 of w) to an exact f16 pair: the byte permute makes
+// each byte b the mantissa of an f16 with the exponent of 1024 (the value
+// 1024 + b), and subtracting 1152 leaves b - 128, the code.
+template <unsigned SEL>
+__device__ __forceinline__ uint32_t ob8x2_to_f16x2(uint32_t w) {
+  const uint32_t x = __byte_perm(w, 0x64646464u, SEL);
   uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0x64806480u));
   return r;
 }
 
-// 4 int8 codes (one word) to exact floats, bit patterns for the tf32 MMA.
-__device__ __forceinline__ void int8x4_to_tf32(uint32_t w, uint32_t (&f)[4]) {
-  const uint32_t a = w ^ 0x80808080u;
-  const float2 off = make_float2(-8388736.0f, -8388736.0f);
-  float2 lo = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7540)),
-                          __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7541)));
-  float2 hi = make_float2(__uint_as_float(__byte_perm(a, 0x4B000000u, 0x7542)),
-                          __uint_as_float(__byte_perm(a, 0x4B000000u, 0x7543)));
-  lo = __fadd2_rn(lo, off);
-  hi = __fadd2_rn(hi, off);
-  f[0] = __float_as_uint(lo.x);
-  f[1] = __float_as_uint(lo.y);
-  f[2] = __float_as_uint(hi.x);
-  f[3] = __float_as_uint(hi.y);
+// Two floats to an f16 pair (first in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
-// PV of one INT8 or FP8 tile on the tensor cores: out^T[dim][head] += V^T[dim][token]
-// · W[token][head] with m16n8k8 tf32 MMAs (M = 16 dims, N = 8 heads, the
-// group padded with zeros, K = 8 tokens), two K steps per tile.  V codes
-// (small integers, or E4M3 values) are exact in tf32; each weight W (softmax weight times the
-// token's V scale) is split into two tf32 parts, hi + lo, one MMA each, so
-// the products keep ~21 bits.  Lane (gid = lane / 4, tig = lane % 4) owns, in
-// MMA c, dims d0 = (D/8)·gid + 2c (row gid) and d0 + 1 (row gid + 8), and
-// heads 2·tig, 2·tig + 1: acc[c] = {(d0, 2tig), (d0, 2tig+1), (d0+1, 2tig),
-// (d0+1, 2tig+1)}.  It reads the D/8 code bytes at dims [(D/8)·gid, +D/8) of
-// tokens tig, tig + 4, tig + 8, tig + 12; the V tile's 16-byte units are
-// permuted within each 128-byte line (unit u of line L at u ^ (2L & 7)), which
-// puts the 8 lanes of every shared-memory phase on 8 different units.
-template <int D>
-__device__ __forceinline__ const unsigned char* v_i8_row_run(const unsigned char* vt, int t,
-                                                              int gid) {
-  constexpr int RUN = D / 8;                 // bytes per lane and token: 16 or 8
-  const int unit = (t * D + RUN * gid) >> 4;  // logical 16-byte unit in the tile
-  const int line = unit >> 3;
-  return vt + ((line << 3) + ((unit & 7) ^ ((2 * line) & 7))) * 16 + ((RUN * gid) & 15);
-}
-
-// 2 E4M3 codes (16 bits, first code in the low byte) to floats, exact (every
-// E4M3 value is exact in f16 and f32).
-__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t h) {
-  const __half2_raw r =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
+__device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
   __half2 v;
-  v = *reinterpret_cast<const __half2*>(&r);
+  v = *reinterpret_cast<const __half2*>(&h);
   return __half22float2(v);
 }
 
-// 4 E4M3 codes (one word) to float bit patterns for the tf32 MMA (exact: 3
-// mantissa bits fit tf32's 10).
-__device__ __forceinline__ void e4m3x4_to_tf32(uint32_t w, uint32_t (&f)[4]) {
-  const float2 lo = e4m3x2_to_float2(w), hi = e4m3x2_to_float2(w >> 16);
-  f[0] = __float_as_uint(lo.x);
-  f[1] = __float_as_uint(lo.y);
-  f[2] = __float_as_uint(hi.x);
-  f[3] = __float_as_uint(hi.y);
+// A pair of weights as an f16 hi part and an f16 lo part: hi = f16(u),
+// lo = f16(u - hi); their sum keeps ~22 significant bits of u (for u <= 1
+// down to f16's subnormals, far below anything that matters next to 1).
+__device__ __forceinline__ void split_f16x2(float u0, float u1, uint32_t& hi, uint32_t& lo) {
+  hi = f16x2_rn(u0, u1);
+  const float2 h = f16x2_to_float2(hi);
+  lo = f16x2_rn(u0 - h.x, u1 - h.y);
 }
 
-// F8 = false: INT8 codes; true: E4M3 codes.  With E4M3 a code can be NaN, and
-// a token past the context (nvalid) has weight 0 but whatever codes the pool
-// holds there, so its codes are replaced by 0 (0 * NaN would not be 0).
-template <int D, int G, bool F8, bool FULL>
-__device__ __forceinline__ void pv_q_mma(const unsigned char* __restrict__ vt,
-                                         const float* __restrict__ ps, float (&acc)[D / 16][4],
-                                         int lane, int nvalid) {
-  constexpr int NWORD = D / 32;  // code words per lane and token
-  const int gid = lane >> 2, tig = lane & 3;
-  uint32_t whi[4], wlo[4];  // W[token tig + 4j][head gid] = hi + lo
+// The N = 8 columns of the 1-byte decode's MMAs for a group of G heads.  G = 8:
+// one head per column.  G <= 4: column n holds part n / G of head n % G (QK:
+// the two E4M3 parts of q; PV: the hi and lo f16 parts of the weights; parts
+// >= 2 are zero), so one MMA carries both parts and the lanes holding part 1
+// mirror those holding part 0.  Lane tig's accumulator columns 2 tig, 2 tig + 1
+// are heads head(2 tig), head(2 tig) + 1.
+template <int G>
+struct QCols {
+  static constexpr bool PACKED = G < 8;
+  static constexpr int NQ = PACKED ? 1 : 2;  // q fragment sets (G = 8: one per part)
+  static __device__ __forceinline__ int head(int n) { return PACKED ? n % G : n; }
+  static __device__ __forceinline__ int part(int n) { return PACKED ? n / G : 0; }
+  // a lane whose accumulator columns hold part 0 (writes weights and results)
+  static __device__ __forceinline__ bool part0(int tig) { return !PACKED || 2 * tig < G; }
+};
+
+// The lane's D / 8 words of a 1-byte V tile laid out as v_tile_pos (cache_row.cuh)
+// states: word 2c is dim 16c + gid, word 2c + 1 dim 16c + gid + 8, each with the
+// codes of tokens 2 tig, 2 tig + 1, 2 tig + 8, 2 tig + 9 in bytes 0..3.
+template <int D>
+__device__ __forceinline__ void load_v_words(const unsigned char* vt, int lane,
+                                             uint32_t (&w)[D / 8]) {
+  const int f = D == 128 ? ((lane >> 1) & 3) : ((lane >> 2) & 1);
+  const unsigned char* base = vt + lane * (D / 2);
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float w = gid < G ? ps[(tig + 4 * j) * G + gid] : 0.f;
-    whi[j] = to_tf32(w);
-    wlo[j] = to_tf32(w - __uint_as_float(whi[j]));
+  for (int u = 0; u < D / 32; ++u) {
+    const uint4 x = *reinterpret_cast<const uint4*>(base + 16 * (u ^ f));
+    w[4 * u] = x.x;
+    w[4 * u + 1] = x.y;
+    w[4 * u + 2] = x.z;
+    w[4 * u + 3] = x.w;
+  }
+}
+
+// The warp's power-of-two bound on the V scales it has weighted: the PV
+// weights enter the MMA as p * v_scale / bound, at most 1 and so safe in f16
+// whatever the scales are.  For a tile whose largest valid scale (vmax,
+// warp-uniform) is above the bound, raises it to the next power of two and
+// returns old / new (exact), the factor the accumulators take; else 1.
+__device__ __forceinline__ float raise_v_bound(float vmax, float& bound, float& inv) {
+  if (!(vmax > bound)) return 1.f;
+  const float nb = __uint_as_float((__float_as_uint(vmax) + 0x007FFFFFu) & 0x7F800000u);
+  const float r = bound / nb;
+  bound = nb;
+  inv = 1.0f / nb;
+  return r;
+}
+
+// PV of one 1-byte tile on the tensor cores (f16 in, fp32 accumulate):
+// out^T[dim][column] += V^T[dim][token] · W[token][column], m16n8k16 MMAs with
+// M = 16 dims, N = the 8 QCols columns, K = the tile's 16 tokens.  V codes are
+// exact in f16 (INT8 offset-binary through ob8x2_to_f16x2, E4M3 through the
+// conversion instruction); each weight (ps: softmax weight times the token's V
+// scale, [16 tokens][G], 0 past the context) times inv_s enters as an f16 hi
+// and an f16 lo part (G <= 4: the two column halves of one MMA; G = 8: a
+// second MMA).  Lane (gid, tig) feeds dims 16c + gid and 16c + gid + 8 of
+// m-tile c; acc[c] holds (dim 16c + gid; columns 2 tig, 2 tig + 1) and (dim
+// 16c + gid + 8; the same columns).  E4M3 codes of tokens past the context
+// may be NaN and are zeroed (0 * NaN is not 0); INT8 codes are always finite.
+template <int D, int G, bool F8, bool FULL>
+__device__ __forceinline__ void pv_f16(const unsigned char* __restrict__ vt,
+                                       const float* __restrict__ ps, float inv_s,
+                                       float (&acc)[D / 16][4], int lane, int nvalid) {
+  using C = QCols<G>;
+  const int gid = lane >> 2, tig = lane & 3;
+  const float* pc = ps + C::head(gid);
+  uint32_t h0, l0, h1, l1;
+  split_f16x2(pc[(2 * tig) * G] * inv_s, pc[(2 * tig + 1) * G] * inv_s, h0, l0);
+  split_f16x2(pc[(2 * tig + 8) * G] * inv_s, pc[(2 * tig + 9) * G] * inv_s, h1, l1);
+  uint32_t b0 = h0, b1 = h1;  // G = 8: the hi parts here, the lo parts by a second MMA
+  if constexpr (C::PACKED) {
+    const int pn = C::part(gid);
+    b0 = pn == 0 ? h0 : (pn == 1 ? l0 : 0u);
+    b1 = pn == 0 ? h1 : (pn == 1 ? l1 : 0u);
+  }
+  uint32_t w[D / 8];
+  load_v_words<D>(vt, lane, w);
+  if constexpr (F8 && !FULL) {
+    const uint32_t keep = (2 * tig < nvalid ? 0x000000FFu : 0u) |
+                          (2 * tig + 1 < nvalid ? 0x0000FF00u : 0u) |
+                          (2 * tig + 8 < nvalid ? 0x00FF0000u : 0u) |
+                          (2 * tig + 9 < nvalid ? 0xFF000000u : 0u);
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) w[j] &= keep;
   }
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {
-    const int t0 = 8 * ks + tig, t1 = t0 + 4;
-    const unsigned char* r0 = v_i8_row_run<D>(vt, t0, gid);
-    const unsigned char* r1 = v_i8_row_run<D>(vt, t1, gid);
-    uint32_t w0[NWORD], w1[NWORD];
-    if constexpr (NWORD == 4) {
-      const uint4 x = *reinterpret_cast<const uint4*>(r0);
-      const uint4 y = *reinterpret_cast<const uint4*>(r1);
-      w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
-      w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
+  for (int c = 0; c < D / 16; ++c) {
+    uint32_t a0, a1, a2, a3;
+    if constexpr (F8) {
+      a0 = e4m3x2_to_f16x2(w[2 * c]);
+      a2 = e4m3x2_to_f16x2(w[2 * c] >> 16);
+      a1 = e4m3x2_to_f16x2(w[2 * c + 1]);
+      a3 = e4m3x2_to_f16x2(w[2 * c + 1] >> 16);
     } else {
-      const uint2 x = *reinterpret_cast<const uint2*>(r0);
-      const uint2 y = *reinterpret_cast<const uint2*>(r1);
-      w0[0] = x.x; w0[1] = x.y;
-      w1[0] = y.x; w1[1] = y.y;
+      a0 = ob8x2_to_f16x2<0x4140>(w[2 * c]);
+      a2 = ob8x2_to_f16x2<0x4342>(w[2 * c]);
+      a1 = ob8x2_to_f16x2<0x4140>(w[2 * c + 1]);
+      a3 = ob8x2_to_f16x2<0x4342>(w[2 * c + 1]);
     }
-    if constexpr (F8 && !FULL) {
+    mma_f16(acc[c], a0, a1, a2, a3, b0, b1);
+    if constexpr (!C::PACKED) mma_f16(acc[c], a0, a1, a2, a3, l0, l1);
+  }
+}
+
+// Multiplies the PV accumulators of columns 2 tig (fa) and 2 tig + 1 (fb).
+template <int D>
+__device__ __forceinline__ void scale_acc(float (&acc)[D / 16][4], float fa, float fb) {
 #pragma unroll
-      for (int j = 0; j < NWORD; ++j) {
-        if (t0 >= nvalid) w0[j] = 0u;
-        if (t1 >= nvalid) w1[j] = 0u;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NWORD; ++j) {
-      uint32_t f0[4], f1[4];
-      if constexpr (F8) {
-        e4m3x4_to_tf32(w0[j], f0);
-        e4m3x4_to_tf32(w1[j], f1);
-      } else {
-        int8x4_to_tf32(w0[j], f0);
-        int8x4_to_tf32(w1[j], f1);
-      }
-      // word j holds dims 4j .. 4j+3 of the lane's run: MMAs 2j and 2j + 1
-      mma_tf32(acc[2 * j], f0[0], f0[1], f1[0], f1[1], whi[2 * ks], whi[2 * ks + 1]);
-      mma_tf32(acc[2 * j + 1], f0[2], f0[3], f1[2], f1[3], whi[2 * ks], whi[2 * ks + 1]);
-      mma_tf32(acc[2 * j], f0[0], f0[1], f1[0], f1[1], wlo[2 * ks], wlo[2 * ks + 1]);
-      mma_tf32(acc[2 * j + 1], f0[2], f0[3], f1[2], f1[3], wlo[2 * ks], wlo[2 * ks + 1]);
-    }
+  for (int c = 0; c < D / 16; ++c) {
+    acc[c][0] *= fa;
+    acc[c][1] *= fb;
+    acc[c][2] *= fa;
+    acc[c][3] *= fb;
   }
 }
 
 // One INT8 tile.  (qsub, qrg): this lane in the QK geometry; my_head / my_i0:
-// the head and first pass of this lane's scores.
+// the head and first pass of this lane's scores.  vbound / vinv: the warp's
+// V-scale bound (raise_v_bound) and its reciprocal.
 template <int D, int G, bool FULL>
 __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ kt,
                                              const unsigned char* __restrict__ vt,
@@ -348,9 +395,11 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
                                              float* alpha_s,
                                              const int (&qc)[G][I8Geometry<D, G>::QW],
                                              const float (&qsc)[G], float (&acc)[D / 16][4],
-                                             float& m_run, float& l_run, int nvalid, int lane,
-                                             int qsub, int qrg, int my_head, int my_i0) {
+                                             float& m_run, float& l_run, float& vbound,
+                                             float& vinv, int nvalid, int lane, int qsub, int qrg,
+                                             int my_head, int my_i0) {
   using IG = I8Geometry<D, G>;
+  using C = QCols<G>;
   constexpr int QL = IG::QL, QR = IG::ROWS, QP = IG::P, NV = IG::NV, R = IG::R;
 
   // QK: integer partial dots over this lane's QB bytes, value index g * QP + i.
@@ -410,92 +459,97 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
   l_run = l_run * alpha + psum;
   m_run = m_new;
   if (qsub % IG::HEAD_LANES == 0 && qrg == 0) alpha_s[my_head] = alpha;
-  const bool rescale = __any_sync(kFullMask, alpha != 1.0f);
+  // the tile's largest valid V scale, against the warp's bound
+  float vm = (FULL || (lane & 15) < nvalid) ? vsc[lane & 15] : 0.f;
+#pragma unroll
+  for (int m = 1; m < 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+  const float r = raise_v_bound(vm, vbound, vinv);
+  const bool rescale = __any_sync(kFullMask, alpha != 1.0f) || r != 1.0f;
   __syncwarp();
 
   if (rescale) {
-    const int h0 = 2 * (lane & 3);
-    const float a0 = h0 < G ? alpha_s[h0] : 1.f;
-    const float a1 = h0 + 1 < G ? alpha_s[h0 + 1] : 1.f;
-#pragma unroll
-    for (int c = 0; c < D / 16; ++c) {
-      acc[c][0] *= a0;
-      acc[c][1] *= a1;
-      acc[c][2] *= a0;
-      acc[c][3] *= a1;
-    }
+    const int ha = C::head(2 * (lane & 3));
+    scale_acc<D>(acc, alpha_s[ha] * r, alpha_s[ha + 1] * r);
   }
-  pv_q_mma<D, G, false, FULL>(vt, ps, acc, lane, nvalid);
+  pv_f16<D, G, false, FULL>(vt, ps, vinv, acc, lane, nvalid);
 }
 
-// One m16n8k16 f16 tensor-core step, fp32 accumulate: c += a · b.
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
-      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
-// 2 E4M3 codes (16 bits, first code in the low byte) to an f16 pair, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t h) {
-  const __half2_raw r =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
-}
-
-// One FP8 (E4M3) tile.  QK on the tensor cores: S[token][head] = K · qᵀ with
-// m16n8k16 f16 MMAs (M = the tile's 16 tokens, N = 8 heads, the group padded
-// with zeros, K = 16 dims a step).  The codes are exact in f16; q arrives as
-// f16 pairs already multiplied by a power of two per head (exact for bf16 q,
-// see the kernel's prologue) and qfac undoes it together with scale * log2 e.
-// Lane (gid = lane / 4, tig = lane % 4) feeds tokens gid and gid + 8 and reads
-// the D/4 code bytes at dims [(D/4)·tig, +D/4) of each; its step-s fragment
-// columns 2tig, 2tig+1 | 2tig+8, 2tig+9 are dims (D/4)·tig + 4s + 0, 1 | 2, 3,
-// the same dims q's fragment (qf[s], head gid) holds, so the dims reach the
-// MMA in a different order than in memory but every one exactly once.  The
-// accumulator puts scores (token gid | gid + 8, head 2tig | 2tig + 1) in the
-// lane, which are the heads its PV accumulators hold (pv_q_mma), so the
-// online softmax state (m_run, l_run: heads 2tig, 2tig + 1) and the rescale
-// stay in the lane; l_run is this lane's share, summed over gid at the end.
+// One FP8 (E4M3) tile.  QK on the tensor cores in E4M3: S[token][column] =
+// K · q^T with m16n8k32 MMAs (M = the tile's 16 tokens, N = the QCols columns,
+// K = 32 dims a step), q entering as two E4M3 parts whose sum is q times a
+// power of two per head (the kernel's prologue builds qb; the codes need no
+// conversion; the second part is scaled by 2^5 and counts 2^-5).  Lane (gid,
+// tig) feeds tokens gid and gid + 8 with the D / 4
+// code bytes at dims [(D/4) tig, +D/4) of each: a step's k indices 4 tig..+3
+// and 16 + 4 tig..+3 are dims (D/4) tig + 8s + 0..3 and + 4..7, which are the
+// dims of q's fragment for those k, so each dim reaches the MMA exactly once.
+// The accumulator holds (token gid | gid + 8; column 2 tig | 2 tig + 1); the
+// two parts of q are summed across lanes (G <= 4: lane tig ^ G / 2) or
+// accumulators (G = 8).  The online softmax state (m_run, l_run) is that of
+// heads head(2 tig), head(2 tig) + 1, the heads of the lane's PV columns, so
+// the rescale stays in the lane; l_run is this lane's share, summed over gid
+// at the end.  qfac: 2^-k * scale * log2 e of those two heads.
 template <int D, int G, bool FULL>
 __device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ kt,
                                              const unsigned char* __restrict__ vt,
                                              const float* __restrict__ ksc,
                                              const float* __restrict__ vsc, float* ps,
-                                             const uint32_t (&qf)[D / 16][2], float2 qfac,
-                                             float (&acc)[D / 16][4], float2& m_run,
-                                             float2& l_run, int nvalid, int lane) {
-  constexpr int KS = D / 16;  // MMA steps = code words per lane and row
+                                             const uint32_t (&qb)[QCols<G>::NQ][D / 32][2],
+                                             float2 qfac, float (&acc)[D / 16][4],
+                                             float2& m_run, float2& l_run, float& vbound,
+                                             float& vinv, int nvalid, int lane) {
+  using C = QCols<G>;
+  constexpr int KB = D / 4;  // code bytes per lane and row
+  constexpr int KS = D / 32; // MMA steps
   const int gid = lane >> 2, tig = lane & 3;
-  uint32_t w0[KS], w1[KS];  // codes of tokens gid and gid + 8
+  uint32_t k0[KB / 4], k1[KB / 4];  // codes of tokens gid and gid + 8
   {
-    const unsigned char* r0 = kt + gid * D + (D / 4) * tig;
+    const unsigned char* r0 = kt + gid * D + KB * tig;
     const unsigned char* r1 = r0 + 8 * D;
 #pragma unroll
-    for (int u = 0; u < KS / 4; ++u) {
+    for (int u = 0; u < KB / 16; ++u) {
       const uint4 x = *reinterpret_cast<const uint4*>(r0 + 16 * u);
       const uint4 y = *reinterpret_cast<const uint4*>(r1 + 16 * u);
-      w0[4 * u] = x.x; w0[4 * u + 1] = x.y; w0[4 * u + 2] = x.z; w0[4 * u + 3] = x.w;
-      w1[4 * u] = y.x; w1[4 * u + 1] = y.y; w1[4 * u + 2] = y.z; w1[4 * u + 3] = y.w;
+      k0[4 * u] = x.x; k0[4 * u + 1] = x.y; k0[4 * u + 2] = x.z; k0[4 * u + 3] = x.w;
+      k1[4 * u] = y.x; k1[4 * u + 1] = y.y; k1[4 * u + 2] = y.z; k1[4 * u + 3] = y.w;
     }
   }
-  // two independent accumulation chains, summed at the end
   float c[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
-  for (int s = 0; s < KS; ++s)
-    mma_f16(c[s & 1], e4m3x2_to_f16x2(w0[s]), e4m3x2_to_f16x2(w1[s]),
-            e4m3x2_to_f16x2(w0[s] >> 16), e4m3x2_to_f16x2(w1[s] >> 16), qf[s][0], qf[s][1]);
+  for (int st = 0; st < KS; ++st) {
+    if constexpr (C::PACKED) {  // two independent chains, summed below
+      mma_e4m3(c[st & 1], k0[2 * st], k1[2 * st], k0[2 * st + 1], k1[2 * st + 1], qb[0][st][0],
+               qb[0][st][1]);
+    } else {  // one chain per part of q
+      mma_e4m3(c[0], k0[2 * st], k1[2 * st], k0[2 * st + 1], k1[2 * st + 1], qb[0][st][0],
+               qb[0][st][1]);
+      mma_e4m3(c[1], k0[2 * st], k1[2 * st], k0[2 * st + 1], k1[2 * st + 1], qb[1][st][0],
+               qb[1][st][1]);
+    }
+  }
+  // q = q1 + 2^-5 q2: part 1 counts 2^-5
+  float sc[4];
+  if constexpr (C::PACKED) {
+    const float w = C::part(2 * tig) == 1 ? 0.03125f : 1.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      sc[i] = (c[0][i] + c[1][i]) * w;
+      sc[i] += __shfl_xor_sync(kFullMask, sc[i], G / 2);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sc[i] = fmaf(c[1][i], 0.03125f, c[0][i]);
+  }
 
   // scores in base-2 units; a token past the context is masked by position
   // (its codes and scale may be anything, NaN included)
   const bool ok0 = FULL || gid < nvalid, ok1 = FULL || gid + 8 < nvalid;
-  const float k0 = ok0 ? ksc[gid] : 0.f, k1 = ok1 ? ksc[gid + 8] : 0.f;
+  const float ks0 = ok0 ? ksc[gid] : 0.f, ks1 = ok1 ? ksc[gid + 8] : 0.f;
   float s[4];
-  s[0] = ok0 ? (c[0][0] + c[1][0]) * k0 * qfac.x : -INFINITY;
-  s[1] = ok0 ? (c[0][1] + c[1][1]) * k0 * qfac.y : -INFINITY;
-  s[2] = ok1 ? (c[0][2] + c[1][2]) * k1 * qfac.x : -INFINITY;
-  s[3] = ok1 ? (c[0][3] + c[1][3]) * k1 * qfac.y : -INFINITY;
+  s[0] = ok0 ? sc[0] * ks0 * qfac.x : -INFINITY;
+  s[1] = ok0 ? sc[1] * ks0 * qfac.y : -INFINITY;
+  s[2] = ok1 ? sc[2] * ks1 * qfac.x : -INFINITY;
+  s[3] = ok1 ? sc[3] * ks1 * qfac.y : -INFINITY;
   float2 mx = make_float2(fmaxf(s[0], s[2]), fmaxf(s[1], s[3]));
 #pragma unroll
   for (int m = 4; m < 32; m <<= 1) {
@@ -508,29 +562,26 @@ __device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ k
   const float p2 = exp2f(s[2] - m_new.x), p3 = exp2f(s[3] - m_new.y);
   l_run = make_float2(l_run.x * alpha.x + (p0 + p2), l_run.y * alpha.y + (p1 + p3));
   m_run = m_new;
-  // weights with the V scale folded in; 0 past the context
+  // the tile's largest valid V scale, against the warp's bound
   const float v0 = ok0 ? vsc[gid] : 0.f, v1 = ok1 ? vsc[gid + 8] : 0.f;
-  const int h0 = 2 * tig;
-  if (h0 < G) {
-    ps[gid * G + h0] = p0 * v0;
-    ps[(gid + 8) * G + h0] = p2 * v1;
-  }
-  if (h0 + 1 < G) {
-    ps[gid * G + h0 + 1] = p1 * v0;
-    ps[(gid + 8) * G + h0 + 1] = p3 * v1;
-  }
-  const bool rescale = __any_sync(kFullMask, alpha.x != 1.0f || alpha.y != 1.0f);
-  __syncwarp();
-  if (rescale) {
+  float vm = fmaxf(v0, v1);
 #pragma unroll
-    for (int cc = 0; cc < D / 16; ++cc) {
-      acc[cc][0] *= alpha.x;
-      acc[cc][1] *= alpha.y;
-      acc[cc][2] *= alpha.x;
-      acc[cc][3] *= alpha.y;
-    }
+  for (int m = 4; m < 32; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+  const float r = raise_v_bound(vm, vbound, vinv);
+  // weights with the V scale folded in (0 past the context), written once per
+  // (token, head) by the lanes holding part 0
+  if (C::part0(tig)) {
+    const int ha = C::head(2 * tig);
+    ps[gid * G + ha] = p0 * v0;
+    ps[gid * G + ha + 1] = p1 * v0;
+    ps[(gid + 8) * G + ha] = p2 * v1;
+    ps[(gid + 8) * G + ha + 1] = p3 * v1;
   }
-  pv_q_mma<D, G, true, FULL>(vt, ps, acc, lane, nvalid);
+  const float fa = alpha.x * r, fb = alpha.y * r;
+  const bool rescale = __any_sync(kFullMask, fa != 1.0f || fb != 1.0f);
+  __syncwarp();
+  if (rescale) scale_acc<D>(acc, fa, fb);
+  pv_f16<D, G, true, FULL>(vt, ps, vinv, acc, lane, nvalid);
 }
 
 }  // namespace pa

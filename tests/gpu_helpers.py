@@ -91,15 +91,43 @@ def assert_close(got, ref, what=""):
     return amax
 
 
-def swizzle_v_int8(v):
-    """The INT8 V pool's storage order from the logical [NB, Hkv, bs, D] codes
-    (and back: the permutation is its own inverse).  Each (block, head) tile is
-    128-byte lines of eight 16-byte units; unit u of line L is stored at unit
-    u ^ ((2L) & 7), as the library's header states."""
+def v_tile_positions(d):
+    """[16, d] int array: the byte offset, within one (block, head) tile of a
+    1-byte V pool, of token t's code of dim j, as the library's header states:
+    L * (d/2) + 16 * ((w // 4) ^ f) + 4 * (w % 4) + y with r = j % 16,
+    L = 4 * (r % 8) + (t % 8) // 2, w = 2 * (j // 16) + r // 8,
+    y = (t % 2) + 2 * (t // 8), f = (L // 2) % 4 at d = 128, (L // 4) % 2 at 64."""
+    t = np.arange(16)[:, None]
+    j = np.arange(d)[None, :]
+    r = j % 16
+    L = 4 * (r % 8) + (t % 8) // 2
+    w = 2 * (j // 16) + r // 8
+    y = (t % 2) + 2 * (t // 8)
+    f = (L // 2) % 4 if d == 128 else (L // 4) % 2
+    return L * (d // 2) + 16 * ((w // 4) ^ f) + 4 * (w % 4) + y
+
+
+def v_pool_stored(v, fp8):
+    """The 1-byte V pool as the device stores it, from logical codes
+    [NB, Hkv, 16, D] (int8 INT8 codes, or uint8 E4M3 codes): each tile
+    transposed by v_tile_positions, INT8 codes offset by 128."""
     v = np.ascontiguousarray(v)
     nb, hkv, bs, d = v.shape
-    units = v.reshape(nb, hkv, bs * d // 128, 8, 16)
-    line = np.arange(units.shape[2])[:, None]
-    src = np.arange(8)[None, :] ^ ((2 * line) & 7)
-    out = np.take_along_axis(units, src[None, None, :, :, None], axis=3)
-    return out.reshape(v.shape)
+    src = v.reshape(nb, hkv, bs * d).view(np.uint8)
+    if not fp8:
+        src = src ^ np.uint8(0x80)
+    out = np.empty_like(src)
+    out[:, :, v_tile_positions(d).reshape(-1)] = src
+    out = out.reshape(v.shape)
+    return out if fp8 else out.view(np.int8)
+
+
+def v_pool_logical(v, fp8):
+    """Inverse of v_pool_stored: logical codes from the device's V pool bytes."""
+    v = np.ascontiguousarray(v)
+    nb, hkv, bs, d = v.shape
+    out = v.reshape(nb, hkv, bs * d).view(np.uint8)[:, :, v_tile_positions(d).reshape(-1)]
+    if not fp8:
+        out = out ^ np.uint8(0x80)
+    out = out.reshape(v.shape)
+    return out if fp8 else out.view(np.int8)

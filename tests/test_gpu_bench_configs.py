@@ -29,7 +29,7 @@ from paged_kv_cache_283_gb300 import inputs as I  # noqa: E402
 from paged_kv_cache_283_gb300 import pa  # noqa: E402
 
 from gpu_helpers import assert_close, bf16_to_f64, host_bits, model_tables, \
-    swizzle_v_int8  # noqa: E402
+    v_pool_logical  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 
@@ -58,7 +58,7 @@ def _host_pool(pool, kv):
     """A device pool (replica or layer) in the oracle's logical layout."""
     if kv == "bf16":
         return [host_bits(pool[0]), host_bits(pool[1])]
-    return [pool[0].cpu().numpy(), swizzle_v_int8(pool[1].cpu().numpy()),
+    return [pool[0].cpu().numpy(), v_pool_logical(pool[1].cpu().numpy(), kv == "fp8"),
             pool[2].cpu().numpy(), pool[3].cpu().numpy()]
 
 

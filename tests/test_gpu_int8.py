@@ -11,7 +11,7 @@ from paged_kv_cache_283_gb300 import inputs as I
 from paged_kv_cache_283_gb300 import pa
 
 from gpu_helpers import (assert_close, bf16_to_f64, both_tables, dev_bf16, model_tables,
-                         swizzle_v_int8)
+                         v_pool_logical, v_pool_stored)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _pools(w, rng):
 
 def _dev_pools(kq, vq, ks, vs):
     """Device pools from logical codes (V goes to its storage order)."""
-    return (torch.from_numpy(kq).cuda(), torch.from_numpy(swizzle_v_int8(vq)).cuda(),
+    return (torch.from_numpy(kq).cuda(), torch.from_numpy(v_pool_stored(vq, False)).cuda(),
             torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda())
 
 
@@ -55,7 +55,7 @@ def test_int8_cache_write_bit_exact(d):
     pa.pa_clear_device_error()
     pa.pa_reshape_and_cache_int8(dev_bf16(key), dev_bf16(val), dk, dv, dks, dvs, _i64(slots))
     torch.cuda.synchronize()
-    got = (dk.cpu().numpy(), swizzle_v_int8(dv.cpu().numpy()), dks.cpu().numpy(),
+    got = (dk.cpu().numpy(), v_pool_logical(dv.cpu().numpy(), False), dks.cpu().numpy(),
            dvs.cpu().numpy())
     for g, exp in zip(got, want):
         assert np.array_equal(g, exp)

@@ -18,7 +18,7 @@ from paged_kv_cache_283_gb300 import inputs as I
 from paged_kv_cache_283_gb300 import pa
 
 from gpu_helpers import assert_close, bf16_to_f64, both_tables, dev_bf16, host_bits, \
-    swizzle_v_int8
+    v_pool_logical, v_pool_stored
 
 pytestmark = pytest.mark.gpu
 
@@ -45,7 +45,7 @@ class _Case:
             kq, ks = quant(w.k_cache)
             vq, vs = quant(w.v_cache)
             self.host = [kq, vq, ks, vs]
-            self.dev = [torch.from_numpy(kq).cuda(), torch.from_numpy(swizzle_v_int8(vq)).cuda(),
+            self.dev = [torch.from_numpy(kq).cuda(), torch.from_numpy(v_pool_stored(vq, kv == "fp8")).cuda(),
                         torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()]
 
     def oracle_write(self, key, val, slots):
@@ -70,7 +70,7 @@ class _Case:
         """Device pools in the oracle's (logical) layout, for bit comparison."""
         if self.kv == "bf16":
             return [host_bits(self.dev[0]), host_bits(self.dev[1])]
-        return [self.dev[0].cpu().numpy(), swizzle_v_int8(self.dev[1].cpu().numpy()),
+        return [self.dev[0].cpu().numpy(), v_pool_logical(self.dev[1].cpu().numpy(), self.kv == "fp8"),
                 self.dev[2].cpu().numpy(), self.dev[3].cpu().numpy()]
 
     def run(self, q, key, val, slots, split, ctx=None, counters=None, workspace=None):
