@@ -104,9 +104,13 @@ struct SmemLayout {
   static constexpr int BARS = S * 8;
   static constexpr int MERGE = (G * D + 2 * G) * 4;  // aliases TILES after the loop
   static constexpr int WARP = ((TILES + PS + ALPHA + BARS + 127) / 128) * 128;
-  // int8 cache: the CTA's quantised q, codes [G][D] then scales [G]
+  // 1-byte caches: the CTA's prepared q (int8 cache: codes [G][D] then scales
+  // [G]; fp8 cache: see QF8)
   static constexpr int QOFF = NW * WARP;
-  static constexpr int QREG = I8 ? ((G * D + G * 4 + 127) / 128) * 128 : 0;
+  // (the fp8 cache: q's MMA fragment words and per-head factors, [word][lane])
+  static constexpr int QI8 = ((G * D + G * 4 + 127) / 128) * 128;
+  static constexpr int QF8 = 32 * ((G < 8 ? 1 : 2) * D / 16 + 2) * 4;
+  static constexpr int QREG = I8 ? (QI8 > QF8 ? QI8 : QF8) : 0;
   // fused decode step: the new row staged for the patch (bf16: K and V rows;
   // 1-byte: K codes, V codes, the two scales)
   static constexpr int PATCHOFF = NW * WARP + QREG;
@@ -305,61 +309,85 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       // under 2^-14 absolute, about 2^-21 of the head's largest |q|.  G <= 4:
       // column gid carries part(gid) (parts >= 2 are zeros); G = 8: both parts,
       // one fragment set each.  Step s's fragment words are dims (D/4) tig + 8s
-      // + 0..3 and + 4..7.
+      // + 0..3 and + 4..7.  Every warp needs the same fragments: warp 0 builds
+      // them into shared memory ([word][lane]) and the others load them.
       using C = QCols<G>;
-      constexpr int E = D / 4;
-      const int gid = lane >> 2, tig = lane & 3;
-      const int hn = C::head(gid);
-      float f[E];
-      const __nv_bfloat16* qh =
-          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + hn) * D +
-          E * tig;
-  #pragma unroll
-      for (int u = 0; u < E / 8; ++u) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
-        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
-        const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
-        f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
-        f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
-      }
-      float amax = 0.f;
-  #pragma unroll
-      for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
-      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-      // biased exponent of amax (0 for 0 and subnormals); k = 7 - unbiased
-      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-      const int kexp = min(127, max(-126, 134 - ebits));
-      const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
-      const int pn = C::part(gid);
-  #pragma unroll
-      for (int j = 0; j < E / 4; ++j) {
-        uint32_t w1 = 0, w2 = 0;
-  #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float x0 = f[4 * j + 2 * h] * up, x1 = f[4 * j + 2 * h + 1] * up;
-          const __nv_fp8x2_storage_t c1 =
-              __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-          const __half2_raw r1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
-          __half2 r1h;
-          r1h = *reinterpret_cast<const __half2*>(&r1);
-          const float2 q1 = __half22float2(r1h);
-          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
-              make_float2((x0 - q1.x) * 32.f, (x1 - q1.y) * 32.f), __NV_SATFINITE, __NV_E4M3);
-          w1 |= static_cast<uint32_t>(c1) << (16 * h);
-          w2 |= static_cast<uint32_t>(c2) << (16 * h);
+      constexpr int NWORD = C::NQ * D / 16;
+      uint32_t* qsm = reinterpret_cast<uint32_t*>(smem + Lay::QOFF);
+      if (warp == 0) {
+        constexpr int E = D / 4;
+        const int gid = lane >> 2, tig = lane & 3;
+        const int hn = C::head(gid);
+        float f[E];
+        const __nv_bfloat16* qh =
+            p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + hn) * D +
+            E * tig;
+    #pragma unroll
+        for (int u = 0; u < E / 8; ++u) {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+          const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+          const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
+          f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
+          f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
         }
-        if constexpr (C::PACKED) {
-          qe[0][j / 2][j % 2] = pn == 0 ? w1 : (pn == 1 ? w2 : 0u);
-        } else {
-          qe[0][j / 2][j % 2] = w1;
-          qe[C::NQ - 1][j / 2][j % 2] = w2;
+        float amax = 0.f;
+    #pragma unroll
+        for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+        // biased exponent of amax (0 for 0 and subnormals); k = 7 - unbiased
+        const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+        const int kexp = min(127, max(-126, 134 - ebits));
+        const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
+        const int pn = C::part(gid);
+    #pragma unroll
+        for (int j = 0; j < E / 4; ++j) {
+          uint32_t w1 = 0, w2 = 0;
+    #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float x0 = f[4 * j + 2 * h] * up, x1 = f[4 * j + 2 * h + 1] * up;
+            const __nv_fp8x2_storage_t c1 =
+                __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+            const __half2_raw r1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+            __half2 r1h;
+            r1h = *reinterpret_cast<const __half2*>(&r1);
+            const float2 q1 = __half22float2(r1h);
+            const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
+                make_float2((x0 - q1.x) * 32.f, (x1 - q1.y) * 32.f), __NV_SATFINITE, __NV_E4M3);
+            w1 |= static_cast<uint32_t>(c1) << (16 * h);
+            w2 |= static_cast<uint32_t>(c2) << (16 * h);
+          }
+          if constexpr (C::PACKED) {
+            qe[0][j / 2][j % 2] = pn == 0 ? w1 : (pn == 1 ? w2 : 0u);
+          } else {
+            qe[0][j / 2][j % 2] = w1;
+            qe[C::NQ - 1][j / 2][j % 2] = w2;
+          }
         }
+        const float fac = ldexpf(p.scale_log2, -kexp);
+        const int ha = C::head(2 * tig);
+        qfac = make_float2(__shfl_sync(kFullMask, fac, 4 * ha),
+                           __shfl_sync(kFullMask, fac, 4 * (ha + 1)));
+    #pragma unroll
+        for (int n = 0; n < C::NQ; ++n)
+    #pragma unroll
+          for (int s2 = 0; s2 < D / 32; ++s2)
+    #pragma unroll
+            for (int h = 0; h < 2; ++h) qsm[((n * (D / 32) + s2) * 2 + h) * 32 + lane] = qe[n][s2][h];
+        qsm[NWORD * 32 + lane] = __float_as_uint(qfac.x);
+        qsm[(NWORD + 1) * 32 + lane] = __float_as_uint(qfac.y);
       }
-      const float fac = ldexpf(p.scale_log2, -kexp);
-      const int ha = C::head(2 * tig);
-      qfac = make_float2(__shfl_sync(kFullMask, fac, 4 * ha),
-                         __shfl_sync(kFullMask, fac, 4 * (ha + 1)));
+      __syncthreads();
+      if (warp != 0) {
+  #pragma unroll
+        for (int n = 0; n < C::NQ; ++n)
+  #pragma unroll
+          for (int s2 = 0; s2 < D / 32; ++s2)
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) qe[n][s2][h] = qsm[((n * (D / 32) + s2) * 2 + h) * 32 + lane];
+        qfac = make_float2(__uint_as_float(qsm[NWORD * 32 + lane]),
+                           __uint_as_float(qsm[(NWORD + 1) * 32 + lane]));
+      }
     } else if constexpr (Q == 0) {
       const __nv_bfloat16* qb =
           p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;

@@ -227,11 +227,14 @@ __device__ __forceinline__ void mma_e4m3(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// 2 E4M3 codes (16 bits, first code in the low byte) to an f16 pair, exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t h) {
-  const __half2_raw r =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(h & 0xFFFFu), __NV_E4M3);
-  return static_cast<uint32_t>(r.x) | (static_cast<uint32_t>(r.y) << 16);
+// 4 E4M3 codes (one word, first code in the low byte) to two exact f16 pairs:
+// codes 0, 1 -> lo, codes 2, 3 -> hi (the conversion reads each 16-bit half
+// of the word directly).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
 }
 
 // Two offset-binary INT8 V codes (bytes SEL picks: 0x4140 -> bytes 0, 1;
@@ -260,7 +263,7 @@ __device__ __forceinline__ float2 f16x2_to_float2(uint32_t h) {
 }
 
 // A pair of weights as an f16 hi part and an f16 lo part: hi = f16(u),
-// lo = f16(u - hi); their sum keeps ~22 significant bits of u (for u <= 1
+// lo = f16(u - hi); their sum keeps ~22 significant bits of u (for u <= 2^8
 // down to f16's subnormals, far below anything that matters next to 1).
 __device__ __forceinline__ void split_f16x2(float u0, float u1, uint32_t& hi, uint32_t& lo) {
   hi = f16x2_rn(u0, u1);
@@ -302,9 +305,18 @@ __device__ __forceinline__ void load_v_words(const unsigned char* vt, int lane,
   }
 }
 
+// The 1-byte decode's softmax reference: it moves to the tile's maximum only
+// when that exceeds it by more than 2^8 (base-2 units), so most tiles keep
+// the reference and skip rescaling their accumulators.  Weights exp2(s - m)
+// are then at most 2^8 (times V scale / bound: still far inside f16), and the
+// (m, l) pairs a partition emits hold for any reference.  Starts from -inf.
+__device__ __forceinline__ float lazy_max(float m_ref, float tile_max) {
+  return tile_max > m_ref + 8.f ? tile_max : m_ref;
+}
+
 // The warp's power-of-two bound on the V scales it has weighted: the PV
-// weights enter the MMA as p * v_scale / bound, at most 1 and so safe in f16
-// whatever the scales are.  For a tile whose largest valid scale (vmax,
+// weights enter the MMA as p * v_scale / bound, at most 2^8 (lazy_max) and
+// so safe in f16 whatever the scales are.  For a tile whose largest valid scale (vmax,
 // warp-uniform) is above the bound, raises it to the next power of two and
 // returns old / new (exact), the factor the accumulators take; else 1.
 __device__ __forceinline__ float raise_v_bound(float vmax, float& bound, float& inv) {
@@ -357,10 +369,8 @@ __device__ __forceinline__ void pv_f16(const unsigned char* __restrict__ vt,
   for (int c = 0; c < D / 16; ++c) {
     uint32_t a0, a1, a2, a3;
     if constexpr (F8) {
-      a0 = e4m3x2_to_f16x2(w[2 * c]);
-      a2 = e4m3x2_to_f16x2(w[2 * c] >> 16);
-      a1 = e4m3x2_to_f16x2(w[2 * c + 1]);
-      a3 = e4m3x2_to_f16x2(w[2 * c + 1] >> 16);
+      e4m3x4_to_f16x2x2(w[2 * c], a0, a2);
+      e4m3x4_to_f16x2x2(w[2 * c + 1], a1, a3);
     } else {
       a0 = ob8x2_to_f16x2<0x4140>(w[2 * c]);
       a2 = ob8x2_to_f16x2<0x4342>(w[2 * c]);
@@ -444,7 +454,7 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
   for (int m = 1; m < IG::HEAD_LANES; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
 #pragma unroll
   for (int m = QL; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
-  const float m_new = fmaxf(m_run, mx);
+  const float m_new = lazy_max(m_run, mx);
   const float alpha = exp2f(m_run - m_new);
   float psum = 0.f;
 #pragma unroll
@@ -556,7 +566,7 @@ __device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ k
     mx.x = fmaxf(mx.x, __shfl_xor_sync(kFullMask, mx.x, m));
     mx.y = fmaxf(mx.y, __shfl_xor_sync(kFullMask, mx.y, m));
   }
-  const float2 m_new = make_float2(fmaxf(m_run.x, mx.x), fmaxf(m_run.y, mx.y));
+  const float2 m_new = make_float2(lazy_max(m_run.x, mx.x), lazy_max(m_run.y, mx.y));
   const float2 alpha = make_float2(exp2f(m_run.x - m_new.x), exp2f(m_run.y - m_new.y));
   const float p0 = exp2f(s[0] - m_new.x), p1 = exp2f(s[1] - m_new.y);
   const float p2 = exp2f(s[2] - m_new.x), p3 = exp2f(s[3] - m_new.y);
