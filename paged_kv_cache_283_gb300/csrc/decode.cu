@@ -71,24 +71,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 #endif
 // MINB is the number of CTAs meant to share an SM, handed to the register
 // allocator through __launch_bounds__.
-template <int D, bool SPLIT, bool I8>
+template <int D, bool SPLIT, int Q>
 struct Pipe {  // head_dim 64: 2 KiB tiles, deeper rings
   static constexpr int NW = 4;
-  static constexpr int S = I8 ? 6 : 4;
+  static constexpr int S = Q != 0 ? 6 : 4;
 };
-template <bool SPLIT, bool I8>
-struct Pipe<128, SPLIT, I8> {
+template <bool SPLIT, int Q>
+struct Pipe<128, SPLIT, Q> {
   static constexpr int NW = SPLIT ? PA_SPLIT_WARPS_D128 : PA_WHOLE_WARPS_D128;
-  static constexpr int S = I8 ? 3 : (SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128);
+  static constexpr int S = Q == 1 ? 3 : Q == 2 ? 2 : (SPLIT ? PA_SPLIT_STAGES_D128 : PA_WHOLE_STAGES_D128);
 };
 // Small bf16 CTAs share an SM three at a time (<= 168 registers); groups of 8
-// heads need more registers than that and get one CTA's worth.  The INT8
-// kernel needs fewer registers and more warps to hide its latencies: four
-// 4-warp CTAs (two 8-warp ones) per SM, <= 128 registers, each warp with 3
-// stages of 4.2 KiB in flight (head_dim 128).
+// heads need more registers than that and get one CTA's worth.  The 1-byte
+// kernels need fewer registers and more warps to hide their latencies: four
+// 4-warp INT8 CTAs per SM (<= 128 registers, 3 stages of 4.2 KiB per warp at
+// head_dim 128), five FP8 ones (<= 102 registers, 2 stages: measured faster
+// than 4 x 3 on the batch-64 and 32-layer steps; INT8 spills at that budget);
+// 8-warp CTAs two per SM.
 template <int NW, int G, int Q>
 constexpr int min_blocks() {
-  if constexpr (Q != 0) return NW <= 4 ? (G <= 4 ? 4 : 3) : 2;
+  if constexpr (Q != 0) return NW <= 4 ? (G <= 4 ? (Q == 2 ? 5 : 4) : 3) : 2;
   else return (NW <= 4 && G <= 4) ? 3 : 1;  // bf16
 }
 
@@ -518,34 +520,45 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   const size_t block_stride = static_cast<size_t>(p.num_kv_heads) * BS * D;
   const size_t head_off = static_cast<size_t>(kvh) * BS * D;
   int issued = 0;
-  // Called by the whole warp, in tile order.
-  auto issue = [&](int i) {
+  // Called by the whole warp, in tile order, with the tile's ring stage: lane
+  // 0 arms the stage's mbarrier with its bytes, and lanes 0 .. NCOPY - 1 each
+  // issue one of its bulk copies (K tile, V tile, and for the 1-byte caches the
+  // K and V scale runs).  A copy landing before the arming is fine: the
+  // stage's phase cannot complete while lane 0's arrival is pending.
+  auto issue = [&](int i, int st) {
     if ((i >> 5) != ids_win) {
       ids_cur = ids_next;
       ++ids_win;
       ids_next = (ids_win + 1) * 32 < nw ? load_ids(ids_win + 1) : 0;
     }
     int id = __shfl_sync(kFullMask, ids_cur, i & 31);
-    if (lane == 0) {
+    constexpr int NCOPY = I8 ? 4 : 2;
+    if (lane < NCOPY) {
       if (id < 0 || id >= p.num_blocks) {  // never dereferenced: read block 0 instead
-        raise_error(p.err, PA_DEVERR_BLOCK_ID);
+        if (lane == 0) raise_error(p.err, PA_DEVERR_BLOCK_ID);
         id = 0;
       }
-      const int st = i % S;
       uint64_t* bar = &bars[st];
       unsigned char* dst = tiles + st * Lay::STAGE;
       const size_t off = static_cast<size_t>(id) * block_stride + head_off;  // elements
-      mbar_arrive_expect_tx(bar, Lay::STAGE);
+      if (lane == 0) mbar_arrive_expect_tx(bar, Lay::STAGE);
+      const void* src;
+      unsigned bytes = Lay::KT;
       if constexpr (!I8) {
-        bulk_copy_g2s(dst, p.k_cache + off, Lay::KT, bar, policy);
-        bulk_copy_g2s(dst + Lay::KT, p.v_cache + off, Lay::KT, bar, policy);
+        src = lane == 0 ? static_cast<const void*>(p.k_cache + off)
+                        : static_cast<const void*>(p.v_cache + off);
+        dst += lane * Lay::KT;
+      } else if (lane < 2) {
+        src = lane == 0 ? static_cast<const void*>(p.k8 + off) : static_cast<const void*>(p.v8 + off);
+        dst += lane * Lay::KT;
       } else {
         const size_t soff = off / D;  // scales: one per token
-        bulk_copy_g2s(dst, p.k8 + off, Lay::KT, bar, policy);
-        bulk_copy_g2s(dst + Lay::KT, p.v8 + off, Lay::KT, bar, policy);
-        bulk_copy_g2s(dst + 2 * Lay::KT, p.k_scales + soff, BS * 4, bar, policy);
-        bulk_copy_g2s(dst + 2 * Lay::KT + BS * 4, p.v_scales + soff, BS * 4, bar, policy);
+        src = lane == 2 ? static_cast<const void*>(p.k_scales + soff)
+                        : static_cast<const void*>(p.v_scales + soff);
+        bytes = BS * 4;
+        dst += 2 * Lay::KT + (lane - 2) * BS * 4;
       }
+      bulk_copy_g2s(dst, src, bytes, bar, policy);
     }
     issued = i + 1;
   };
@@ -577,7 +590,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   const int my_i0 = QI ? (qsub * IG::R) % IG::P : (sub * R) % P;
 
   const int npro = nw < S ? nw : S;
-  for (int i = 0; i < npro; ++i) issue(i);
+  for (int i = 0; i < npro; ++i) issue(i, i);
   if (p.early_read) {
     griddep_wait();
     load_q();
@@ -589,9 +602,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       fused_cache_write<D, Q>(p, b, kvh, ctx, tbl, lane, smem + Lay::PATCHOFF);
 
   int consumed = 0;
+  int st = 0;        // ring stage of tile i
+  unsigned ph = 0;   // its mbarrier phase parity
   for (int i = 0; i < nw; ++i) {
-    const int st = i % S;
-    const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&bars[st], (i / S) & 1, p.err));
+    const bool ready = __all_sync(kFullMask, mbar_wait_bounded(&bars[st], ph, p.err));
     if (!ready) break;
     const int j = jb + warp + i * NW;
     const int nvalid = min(BS, ctx - j * BS);
@@ -632,7 +646,11 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     }
     consumed = i + 1;
     __syncwarp();  // every lane is done with this stage and with ps / alpha_s
-    if (i + S < nw) issue(i + S);
+    if (i + S < nw) issue(i + S, st);
+    if (++st == S) {
+      st = 0;
+      ph ^= 1u;
+    }
   }
   // Only after a timed-out wait: let copies still in flight land (bounded)
   // before this CTA's shared memory can be reused.
@@ -874,7 +892,7 @@ cudaError_t allow_smem(K kernel, int bytes, std::atomic<uint64_t>& done_mask) {
 template <int D, int G, bool SPLIT, int Q>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   constexpr bool I8 = Q != 0;
-  constexpr int NW = Pipe<D, SPLIT, I8>::NW, S = Pipe<D, SPLIT, I8>::S;
+  constexpr int NW = Pipe<D, SPLIT, Q>::NW, S = Pipe<D, SPLIT, Q>::S;
   using Lay = SmemLayout<D, G, NW, S, I8>;
   static std::atomic<uint64_t> smem_set{0};
   auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, Q>;

@@ -305,6 +305,16 @@ __device__ __forceinline__ void load_v_words(const unsigned char* vt, int lane,
   }
 }
 
+// 2^x by the hardware's approximate exponential (relative error below
+// 2^-22; results below 2^-126 flush to zero, and exp2(-inf) is 0).  The
+// 1-byte decode's weights are relative to a reference at most 2^8 below the
+// largest score, so nothing that matters is that small.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // The 1-byte decode's softmax reference: it moves to the tile's maximum only
 // when that exceeds it by more than 2^8 (base-2 units), so most tiles keep
 // the reference and skip rescaling their accumulators.  Weights exp2(s - m)
@@ -455,12 +465,12 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
 #pragma unroll
   for (int m = QL; m < 32; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, m));
   const float m_new = lazy_max(m_run, mx);
-  const float alpha = exp2f(m_run - m_new);
+  const float alpha = ex2_fast(m_run - m_new);
   float psum = 0.f;
 #pragma unroll
   for (int r = 0; r < R; ++r) {
     const int t = (my_i0 + r) * QR + qrg;
-    const float pr = exp2f(s[r] - m_new);
+    const float pr = ex2_fast(s[r] - m_new);
     psum += pr;
     // V scale folded in; a token past the context gets weight 0 (its codes
     // are finite whatever the pool holds, its scale may not be)
@@ -469,11 +479,15 @@ __device__ __forceinline__ void tile_step_i8(const unsigned char* __restrict__ k
   l_run = l_run * alpha + psum;
   m_run = m_new;
   if (qsub % IG::HEAD_LANES == 0 && qrg == 0) alpha_s[my_head] = alpha;
-  // the tile's largest valid V scale, against the warp's bound
+  // the tile's largest valid V scale, against the warp's bound (reduced only
+  // when some lane sees a scale above it)
   float vm = (FULL || (lane & 15) < nvalid) ? vsc[lane & 15] : 0.f;
+  float r = 1.f;
+  if (__any_sync(kFullMask, vm > vbound)) {
 #pragma unroll
-  for (int m = 1; m < 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
-  const float r = raise_v_bound(vm, vbound, vinv);
+    for (int m = 1; m < 16; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+    r = raise_v_bound(vm, vbound, vinv);
+  }
   const bool rescale = __any_sync(kFullMask, alpha != 1.0f) || r != 1.0f;
   __syncwarp();
 
@@ -567,17 +581,21 @@ __device__ __forceinline__ void tile_step_f8(const unsigned char* __restrict__ k
     mx.y = fmaxf(mx.y, __shfl_xor_sync(kFullMask, mx.y, m));
   }
   const float2 m_new = make_float2(lazy_max(m_run.x, mx.x), lazy_max(m_run.y, mx.y));
-  const float2 alpha = make_float2(exp2f(m_run.x - m_new.x), exp2f(m_run.y - m_new.y));
-  const float p0 = exp2f(s[0] - m_new.x), p1 = exp2f(s[1] - m_new.y);
-  const float p2 = exp2f(s[2] - m_new.x), p3 = exp2f(s[3] - m_new.y);
+  const float2 alpha = make_float2(ex2_fast(m_run.x - m_new.x), ex2_fast(m_run.y - m_new.y));
+  const float p0 = ex2_fast(s[0] - m_new.x), p1 = ex2_fast(s[1] - m_new.y);
+  const float p2 = ex2_fast(s[2] - m_new.x), p3 = ex2_fast(s[3] - m_new.y);
   l_run = make_float2(l_run.x * alpha.x + (p0 + p2), l_run.y * alpha.y + (p1 + p3));
   m_run = m_new;
-  // the tile's largest valid V scale, against the warp's bound
+  // the tile's largest valid V scale, against the warp's bound (reduced only
+  // when some lane sees a scale above it)
   const float v0 = ok0 ? vsc[gid] : 0.f, v1 = ok1 ? vsc[gid + 8] : 0.f;
   float vm = fmaxf(v0, v1);
+  float r = 1.f;
+  if (__any_sync(kFullMask, vm > vbound)) {
 #pragma unroll
-  for (int m = 4; m < 32; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
-  const float r = raise_v_bound(vm, vbound, vinv);
+    for (int m = 4; m < 32; m <<= 1) vm = fmaxf(vm, __shfl_xor_sync(kFullMask, vm, m));
+    r = raise_v_bound(vm, vbound, vinv);
+  }
   // weights with the V scale folded in (0 past the context), written once per
   // (token, head) by the lanes holding part 0
   if (C::part0(tig)) {
