@@ -353,11 +353,13 @@ def combine_ranks(local_seconds, step_bytes, steps, world, device="cpu"):
 # ---------------------------------------------------------------------------
 # GPU arm
 
-def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None):
+def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None, n_replicas=None):
     """Device inputs of a workload: block tables and slots from the library's
     allocator, pool replicas (each larger than L2, or one pool per layer),
-    q and the new tokens' K/V.  max_layers (tests) builds only the first
-    layers of the 32-layer workload."""
+    q and the new tokens' K/V.  max_layers (tests, profiling) builds only the
+    first layers of the 32-layer workload (each layer's launch is the same);
+    n_replicas (profiling) sets the number of pool replicas of a one-layer
+    workload (default: enough to exceed replicas_min_bytes, at least 2)."""
     import numpy as np
     import torch
 
@@ -402,7 +404,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None):
         vals = [bf(x[2]) for x in per_layer]
         replicas = [pools]
     else:
-        nrep = max(2, -(-replicas_min_bytes // pool_bytes))
+        nrep = n_replicas or max(2, -(-replicas_min_bytes // pool_bytes))
         k0, v0 = bf(w.k_cache), bf(w.v_cache)
         replicas = [[(k0, v0)]] + [[(k0.clone(), v0.clone())] for _ in range(nrep - 1)]
         qs, keys, vals = [bf(w.q)], [bf(w.key)], [bf(w.value)]
@@ -437,7 +439,7 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None):
         if layers > 1:
             replicas = [[int8_pool() for _ in range(layers)]]
         else:
-            nrep = max(2, -(-replicas_min_bytes // pool_bytes))
+            nrep = n_replicas or max(2, -(-replicas_min_bytes // pool_bytes))
             replicas = [[int8_pool()] for _ in range(nrep)]
     st = {
         "w": w, "bt": torch.from_numpy(bt).to(device), "ctx": torch.from_numpy(ctx).to(device),
@@ -621,8 +623,10 @@ def run_gpu(args):
         pass
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
-    st = _setup(args.workload, device, 4 * l2, args.kv)
+    st = _setup(args.workload, device, 4 * l2, args.kv, max_layers=args.max_layers,
+                n_replicas=args.replicas)
     w = st["w"]
+    nl = len(st["replicas"][0])  # layers built (all, unless --max-layers)
     stream = torch.cuda.Stream(device)
     lp = step_launch(args.workload, w, args.kv, step=args.step, attn=args.attn,
                      partition=args.partition, order=args.order, early_read=args.early_read,
@@ -641,7 +645,7 @@ def run_gpu(args):
     assert pa.pa_get_device_error() == 0, "device error word set during warmup"
 
     graphs = [_capture(lambda r=r: step(r), stream) for r in range(len(st["replicas"]))]
-    launches_per_step = w.layers * (1 if fused else (2 if attn == "decode" else 3))
+    launches_per_step = nl * (1 if fused else (2 if attn == "decode" else 3))
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -673,13 +677,13 @@ def run_gpu(args):
     dom_graphs = [_capture(lambda r=r: dom_all(r), stream) for r in range(len(st["replicas"]))]
     _time_graphs(dom_graphs, 20, stream)
     n_dom = max(args.steps, 50)
-    dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * w.layers)
+    dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * nl)
 
     # end to end through the public API with pinned host buffers
-    e2e = _e2e(st, attn, args, stream, order, early)
+    e2e = _e2e(st, attn, args, stream, order, early) if not args.no_e2e else None
     assert pa.pa_get_device_error() == 0, "device error word set during the run"
 
-    step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
+    step_bytes = nl * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
                                           w.num_kv_heads, w.head_dim, w.block_size, args.kv)
                              + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
                                                  args.kv))
@@ -722,7 +726,7 @@ def run_gpu(args):
         "ms_per_step": dt_max / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": args.kv, "data": "synthetic",
         "config": {
-            "workload": w.name, "batch": w.num_seqs, "layers": w.layers,
+            "workload": w.name, "batch": w.num_seqs, "layers": nl,
             "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "num_blocks": w.num_blocks,
             "mean_context": float(np.mean(w.context_lens)), "new_tokens_per_step": w.num_seqs,
@@ -740,7 +744,7 @@ def run_gpu(args):
             if len(st["replicas"]) > 1 else "32 distinct per-layer pools per step",
             "parallelism": "dp%d (independent sequences per GPU)" % world,
         },
-        "seq_layers_per_s": round(world * w.num_seqs * w.layers * args.steps / dt_max, 1),
+        "seq_layers_per_s": round(world * w.num_seqs * nl * args.steps / dt_max, 1),
         "tokens_per_s": round(world * w.num_seqs * args.steps / dt_max, 1),
         "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(value / world / hbm_peak, 4) if hbm_peak else None,
@@ -755,7 +759,7 @@ def run_gpu(args):
         ub = unique_decode_bytes(w, args.kv)
         if fused:
             ub += cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim, args.kv)
-        step_unique = w.layers * (unique_decode_bytes(w, args.kv) + cache_write_bytes(
+        step_unique = nl * (unique_decode_bytes(w, args.kv) + cache_write_bytes(
             w.num_seqs, w.num_kv_heads, w.head_dim, args.kv))
         res["unique_bytes_per_step"] = step_unique
         res["value_unique"] = round(world * step_unique * args.steps / dt_max / 1e9, 1)
@@ -785,7 +789,7 @@ def _e2e(st, attn, args, stream, order=None, early=False):
 
     w = st["w"]
     dev = st["bt"].device
-    layers = w.layers
+    layers = len(st["replicas"][0])
     pieces = []
     for layer in range(layers):
         pieces += [("q", layer, st["q"][layer]), ("key", layer, st["key"][layer]),
@@ -861,7 +865,7 @@ def _e2e(st, attn, args, stream, order=None, early=False):
         one(k)
     torch.cuda.synchronize()
     dt = time.perf_counter() - t
-    step_bytes = w.layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
+    step_bytes = layers * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
                                           w.num_kv_heads, w.head_dim, w.block_size, st["kv"])
                              + cache_write_bytes(w.num_seqs, w.num_kv_heads, w.head_dim,
                                                  st["kv"]))
@@ -1143,6 +1147,14 @@ def main(argv=None):
                     help="split-K partition size in tokens (default: 512 for the long-context "
                          "workload, else chosen by pa_splitk_partition_size)")
     ap.add_argument("--soak-seconds", type=float, default=0.5)
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="profiling: skip the end-to-end leg (its thousands of launches)")
+    ap.add_argument("--max-layers", type=int, default=None,
+                    help="profiling: build only the first layers of the 32-layer workload "
+                         "(each layer's launch is unchanged; the line then reports those layers)")
+    ap.add_argument("--replicas", type=int, default=None,
+                    help="profiling: pool replicas of a one-layer workload (default: enough to "
+                         "exceed 4x L2, at least 2)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
