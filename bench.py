@@ -1047,7 +1047,13 @@ def run_prefill(args):
     steps = max(args.steps // 10, 20)
     sampler = ClockSampler(0)
     sampler.start()
-    _time_graphs(graphs, 3, stream)
+    time.sleep(0.3)
+    # soak under the same load right before the timed steps, so that the
+    # clock samples (every 20 ms) describe the clocks the steps ran at
+    t_soak = time.time()
+    soak = 0.0
+    while soak < args.soak_seconds:
+        soak += _time_graphs(graphs, 20, stream)
     t0 = time.time()
     dt = _time_graphs(graphs, steps, stream) / steps
     t1 = time.time()

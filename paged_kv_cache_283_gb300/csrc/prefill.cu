@@ -51,27 +51,38 @@
 namespace pa {
 namespace {
 
+// Keys per chunk (the N of S = Q K^T): 128, one CTA per SM holding 3 S
+// buffers and 3-stage K and V rings; or 64, two CTAs per SM (so four softmax
+// warps per scheduler instead of two), each with 2 S buffers and 2-stage rings.
+#ifndef PA_PREFILL_KEYS
+#define PA_PREFILL_KEYS 64
+#endif
 constexpr int kD = 128;                 // head_dim
 constexpr int kRows = 128;              // query rows per CTA = MMA M
-constexpr int kKeys = 128;              // keys per chunk = MMA N of S = Q K^T
+constexpr int kKeys = PA_PREFILL_KEYS;  // keys per chunk = MMA N of S = Q K^T
+constexpr int kCtasPerSm = kKeys == 128 ? 1 : 2;
 constexpr int kBS = 16;                 // tokens per cache block
 constexpr int kChunkBlocks = kKeys / kBS;
-constexpr int kHalf = 128 * 128;        // one 64-column half of a 128-row bf16 tile
+constexpr int kHalf = kRows * 128;      // one 64-column half of Q (128 rows x 128 bytes)
+constexpr int kKVHalf = kKeys * 128;    // one 64-column half of a K or V chunk
 constexpr int kBox = kBS * 128;         // one TMA box of K or V: 16 rows x 128 bytes
-constexpr uint32_t kTmemCols = 512;     // S0..S2: [0, 384) in 128-column buffers, O: [384, 512)
-constexpr int kSBuf = 3;                // S (then P) buffers in tensor memory
-constexpr uint32_t kTO = 384;           // O's first column
+constexpr int kSBuf = kKeys == 128 ? 3 : 2;  // S (then P) buffers in tensor memory
+constexpr int kAhead = kSBuf - 1;       // chunks of scores issued ahead of PV
+constexpr uint32_t kTO = kSBuf * kKeys;  // O's first column (after the S buffers)
+constexpr uint32_t kTmemCols = kKeys == 128 ? 512 : 256;  // S buffers + O (128 columns)
+static_assert(kTO + 128 <= kTmemCols, "tensor memory");
 
 // Shared memory, from a 1024-byte aligned base (the swizzle atom).
 constexpr int kQ = 0;                   // Q: 2 halves
-constexpr int kStages = 3;              // K and V ring depth (chunks)
-constexpr int kK = kQ + 2 * kHalf;      // K: 3 stages x 2 halves
-constexpr int kV = kK + 2 * kStages * kHalf;  // V: 3 stages x 2 halves
-constexpr int kBar = kV + 2 * kStages * kHalf;  // mbarriers and the TMEM address slot
+constexpr int kStages = kKeys == 128 ? 3 : 2;  // K and V ring depth (chunks)
+constexpr int kK = kQ + 2 * kHalf;      // K: kStages stages x 2 halves
+constexpr int kV = kK + 2 * kStages * kKVHalf;  // V: kStages stages x 2 halves
+constexpr int kBar = kV + 2 * kStages * kKVHalf;  // mbarriers and the TMEM address slot
 constexpr int kRed = kBar + 256;        // row maxima / sums of the two column halves
 constexpr int kSmemBytes = kRed + 2 * kRows * 4 + 1024;  // + alignment slack
-constexpr int kSoftmaxThreads = 256;    // two threads per row, 64 columns each
+constexpr int kSoftmaxThreads = 256;    // two threads per row, kKeys / 2 columns each
 constexpr int kThreads = kSoftmaxThreads + 96;  // + an MMA warp and two copy warps
+static_assert(kCtasPerSm * kSmemBytes <= 232448, "shared memory per SM");
 
 struct PrefillParams {
   __nv_bfloat16* out;
@@ -217,30 +228,32 @@ __device__ __forceinline__ void pair_sync(int warp) {
 
 // grid (query tiles, KV heads, sequences), 352 threads.  Warps 0-7 run the
 // softmax: thread t < 256 handles row t % 128 (TMEM lane; warps w and w + 4
-// share a lane quarter) and columns [64 h, 64 h + 64) of S and O, h = t / 128.
+// share a lane quarter), columns [h kKeys / 2, (h + 1) kKeys / 2) of S and
+// [64 h, 64 h + 64) of O, h = t / 128.
 // Warp 8 issues the MMAs (lane 0), warp 9 the Q and K copies and warp 10 the
 // V copies (one block per lane), so that no chain waits on another's
 // latencies.
 //
-// Tensor memory: S0, S1, S2 = columns [0, 384) in 128-column buffers, O =
-// [384, 512).  P of chunk c replaces S of chunk c in place (hi part in the
-// buffer's first 64 columns, lo part in the next 64, bf16 pairs packed per
-// column); buffer c % 3.  K and V run in 3-chunk rings.  Every ring slot has
+// Tensor memory: kSBuf S buffers of kKeys columns, then O (128 columns).  P of
+// chunk c replaces S of chunk c in place (hi part in the buffer's first
+// kKeys / 2 columns, lo part in the next, bf16 pairs packed per column); buffer
+// c % kSBuf.  K and V run in kStages-chunk rings.  Every ring slot has
 // its own barriers ("full": copies landed; "free": committed after the MMA
 // that read it; "pv_done": PV read the P it holds), so that each wait names
 // one use of one slot and no parity wait can match an older phase.
 //
-// MMA warp, per chunk c:  wait PV(c-1) (S[(c+2)%3] holds P(c-1)) and K(c+2):
-//   S[(c+2)%3] = Q K(c+2)^T; wait V(c) and P(c): O += P V(c).
-// Copy warps, per chunk c: wait K slot of c free: copy K(c+3) (K warp);
-//   wait V slot of c-1 free: copy V(c+2) (V warp).
+// MMA warp, per chunk c (A = kAhead = kSBuf - 1): wait PV(c-1) (its buffer
+//   S[(c+A)%kSBuf] held P(c-1)) and K(c+A): S[(c+A)%kSBuf] = Q K(c+A)^T; wait
+//   V(c) and P(c): O += P V(c).
+// Copy warps, per chunk c: wait K slot of c free: copy K(c+kStages) (K warp);
+//   wait V slot of c-1 free: copy V(c+kStages-1) (V warp).
 // Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
 //   exponentials; rescale O only if the reference maximum moved (after
 //   PV(c-1)); P into S[c%3]; arrive on p_ready[c%3].
 // No softmax thread leaves the loop early (the pair barriers must stay
 // matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -282,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pv_done = k_full + 15;
   uint64_t* q_full = k_full + 18;
   // [3] per S buffer, 8 warp arrivals per chunk.  One barrier per buffer: a
-  // softmax warp can be up to two chunks ahead of another (the scores of c + 2
-  // need only PV(c - 1)), and its arrivals must not count for an earlier chunk.
+  // softmax warp can be up to kAhead chunks ahead of another (the scores of
+  // c + kAhead need only PV(c - 1)), and its arrivals must not count for an
+  // earlier chunk.
   uint64_t* p_ready = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
   float* red = reinterpret_cast<float*>(sm + kRed);            // [2][128]
@@ -326,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = c % kStages;
       const int nb = min(kChunkBlocks, nblk_all - c * kChunkBlocks);
       uint64_t* bar = is_v ? &v_full[st] : &k_full[st];
-      unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kHalf + lane * kBox;
+      unsigned char* dst = sm + (is_v ? kV : kK) + 2 * st * kKVHalf + lane * kBox;
       if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nb * 2 * kBox));
       __syncwarp();
       if (lane < nb) {
@@ -336,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int row = (id * p.num_kv_heads + kvh) * kBS;
         tma_2d(dst, is_v ? &tv : &tk, 0, row, bar);
-        tma_2d(dst + kHalf, is_v ? &tv : &tk, 64, row, bar);
+        tma_2d(dst + kKVHalf, is_v ? &tv : &tk, 64, row, bar);
       }
       __syncwarp();
       if (is_v) last_v = c; else last_k = c;
@@ -365,10 +379,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int idq[kIdAhead];
 #pragma unroll
     for (int i = 0; i < kIdAhead; ++i) idq[i] = fetch_id(kStages + i);
-    // K warp, iteration c: QK(c) has read K stage c % 3 -> copy K(c + 3).
-    // V warp, iteration c: PV(c - 1) has read V stage (c + 2) % 3 -> copy V(c + 2).
+    // K warp, iteration c: QK(c) has read K stage c % kStages -> copy
+    // K(c + kStages).  V warp, iteration c: PV(c - 1) has read V stage
+    // (c - 1) % kStages -> copy V(c - 1 + kStages).
     for (int c = vwarp ? 1 : 0; uniform(ok); ++c) {
-      const int next = vwarp ? c + 2 : c + 3;  // the chunk this iteration copies
+      const int next = vwarp ? c - 1 + kStages : c + kStages;  // the chunk this iteration copies
       if (next >= nchunks) break;
       const int freed = vwarp ? c - 1 : c;     // the chunk whose use frees the stage
       if (lane == 0)
@@ -399,44 +414,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qdesc = sw128_desc(sQ, 16, 1024);
       auto qk = [&](int c) {
         const int sb = c % kSBuf, st = c % kStages;
-        const uint64_t kdesc = sw128_desc(sK + 2 * st * kHalf, 16, 1024);
+        const uint64_t kdesc = sw128_desc(sK + 2 * st * kKVHalf, 16, 1024);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;  // descriptor units
-          umma_bf16(tmem + sb * 128, qdesc + off, kdesc + off, kIdescQK, kk > 0);
+          // descriptor units (16 bytes): kk's 32-byte column step within a
+          // 64-column half, and the half's offset
+          const uint32_t qoff = ((kk >> 2) * kHalf + (kk & 3) * 32) >> 4;
+          const uint32_t koff = ((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4;
+          umma_bf16(tmem + sb * kKeys, qdesc + qoff, kdesc + koff, kIdescQK, kk > 0);
         }
         umma_commit(&s_done[sb]);
         umma_commit(&k_free[st]);
         ++s_iss;
       };
-      bool ok = mbar_wait_bounded(q_full, 0, p.err) && mbar_wait_bounded(&k_full[0], 0, p.err);
-      if (ok) qk(0);
-      if (ok && nchunks > 1) {
-        ok = mbar_wait_bounded(&k_full[1], 0, p.err);
-        if (ok) qk(1);
+      bool ok = mbar_wait_bounded(q_full, 0, p.err);
+      for (int c = 0; c < kAhead && c < nchunks && ok; ++c) {
+        ok = mbar_wait_bounded(&k_full[c % kStages], (c / kStages) & 1, p.err);
+        if (ok) qk(c);
       }
       for (int c = 0; c < nchunks && ok; ++c) {
         const int sb = c % kSBuf, st = c % kStages;
-        if (c + 2 < nchunks) {
-          // scores two chunks ahead: PV(c-1) is done with P(c-1) in S[(c+2)%3]
+        if (c + kAhead < nchunks) {
+          // scores kAhead chunks ahead: PV(c-1) is done with P(c-1) in
+          // S[(c + kAhead) % kSBuf]
           if (c >= 1)
-            ok = mbar_wait_bounded(&pv_done[(c + 2) % kSBuf], ((c - 1) / kSBuf) & 1, p.err);
-          ok = ok && mbar_wait_bounded(&k_full[(c + 2) % kStages], ((c + 2) / kStages) & 1, p.err);
+            ok = mbar_wait_bounded(&pv_done[(c + kAhead) % kSBuf], ((c - 1) / kSBuf) & 1,
+                                   p.err);
+          ok = ok && mbar_wait_bounded(&k_full[(c + kAhead) % kStages],
+                                       ((c + kAhead) / kStages) & 1, p.err);
           if (!ok) break;
-          qk(c + 2);
+          qk(c + kAhead);
         }
         ok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err) &&
              mbar_wait_bounded(&p_ready[sb], (c / kSBuf) & 1, p.err);
         if (!ok) break;
         tc_fence_after();
-        const uint64_t vdesc = sw128_desc(sV + 2 * st * kHalf, kHalf, 1024);
+        const uint64_t vdesc = sw128_desc(sV + 2 * st * kKVHalf, kKVHalf, 1024);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          umma_bf16_ts(tmem + kTO, tmem + sb * 128 + 8 * kk, vdesc + kk * (2048 >> 4), kIdescPV,
-                       (c > 0 || kk > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + kTO, tmem + sb * 128 + 64 + 8 * kk, vdesc + kk * (2048 >> 4),
-                       kIdescPV, 1u);
+          umma_bf16_ts(tmem + kTO, tmem + sb * kKeys + 8 * kk, vdesc + kk * (2048 >> 4),
+                       kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kTO, tmem + sb * kKeys + kKeys / 2 + 8 * kk,
+                       vdesc + kk * (2048 >> 4), kIdescPV, 1u);
         }
         umma_commit(&pv_done[sb]);
         umma_commit(&v_free[st]);
@@ -475,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q4 = 0; q4 < HK / 32; ++q4) {
           uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
-          tmem_ld32(tmem + lane_base + sb * 128 + HK * hcol + 32 * q4, chunk);
+          tmem_ld32(tmem + lane_base + sb * kKeys + HK * hcol + 32 * q4, chunk);
         }
         tmem_wait_ld();
       }
@@ -557,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // bf16 (its upper 16 bits), lo = bf16(p - hi) (p - hi is exact and
         // below 2^-7 p, so hi + lo keeps p to ~2^-16)
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
+        for (int q2 = 0; q2 < HK / 32; ++q2) {
           uint32_t wh[16], wl[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
@@ -569,8 +589,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const __nv_bfloat162 lo = __floats2bfloat162_rn(r2.x, r2.y);
             wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          tmem_st16(tmem + lane_base + sb * 128 + 32 * hcol + 16 * q2, wh);
-          tmem_st16(tmem + lane_base + sb * 128 + 64 + 32 * hcol + 16 * q2, wl);
+          // hi pairs in the buffer's first kKeys / 2 columns, lo pairs in the next
+          tmem_st16(tmem + lane_base + sb * kKeys + (HK / 2) * hcol + 16 * q2, wh);
+          tmem_st16(tmem + lane_base + sb * kKeys + kKeys / 2 + (HK / 2) * hcol + 16 * q2, wl);
         }
         tmem_wait_st();
       }
@@ -581,9 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lok && vk < kKeys) {
         const int st = c % kStages;
         lok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err);
-        if (lok && r >= vk) {
+        if (lok && r >= vk && r < kKeys) {
           const uint4 z = make_uint4(0, 0, 0, 0);
-          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hcol) * kHalf + prow);
+          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hcol) * kKVHalf + prow);
 #pragma unroll
           for (int k = 0; k < 8; ++k) row[k] = z;
         }
