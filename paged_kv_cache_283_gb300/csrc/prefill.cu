@@ -9,21 +9,25 @@
 // keys 0 .. p through the block table ("PagedAttention: Virtual Memory for
 // the KV Cache").  n = 1 is a decode step.
 //
-// Design (one CTA per 128 query rows: 8 softmax warps, an MMA warp, two copy warps):
+// Design (one CTA per 128 query rows: 8 softmax warps, an MMA warp, two copy
+// warps; two CTAs per SM):
 //  * Rows are (token, head) pairs of one GQA group: 128 / G tokens x G heads,
 //    so each K/V tile loaded serves the whole group.  Q arrives by one 3-D TMA
 //    per 64-column half; K and V arrive per 16-token block by 2-D TMA (the
-//    block table is a gather of 16-row boxes), 8 blocks = 128 keys per chunk,
-//    three chunk stages each.  TMA writes the 128-byte-swizzled layout the tensor
-//    cores read.
-//  * S = Q K^T (M = 128 rows, N = 128 keys, K = 128 dims) and O += P V
-//    (M = 128, N = 128 dims, K = 128 keys) are tcgen05.mma kind::f16 (bf16 in,
+//    block table is a gather of 16-row boxes), kKeys = 64 keys (4 blocks) per
+//    chunk by default (PA_PREFILL_KEYS: 64 or 128), in rings of kStages chunk
+//    stages each.  TMA writes the 128-byte-swizzled layout the tensor cores
+//    read.
+//  * S = Q K^T (M = 128 rows, N = kKeys, K = 128 dims) and O += P V
+//    (M = 128, N = 128 dims, K = kKeys) are tcgen05.mma kind::f16 (bf16 in,
 //    fp32 accumulate) issued by one thread of the MMA warp, with S and O in
-//    tensor memory (three S buffers + O: all 512 columns).  V is the MN-major operand.
-//    Shared memory: Q 32 KiB, K and V 3 x 32 KiB each (224 KiB, one CTA per
-//    SM, which also holds all 512 tensor-memory columns).
+//    tensor memory (kSBuf S buffers + O).  V is the MN-major operand.  At 64
+//    keys: Q 32 KiB, K and V 2 x 16 KiB each, 2 S buffers, 256 tensor-memory
+//    columns, so two CTAs share an SM and one's MMAs overlap the other's
+//    softmax; at 128 keys: 3 stages of 32 KiB, 3 S buffers, all 512 columns,
+//    one CTA per SM.
 //  * The online softmax reads its row of S from tensor memory (two threads per
-//    row = TMEM lane, 64 columns each, maxima and sums combined through shared
+//    row = TMEM lane, kKeys / 2 columns each, maxima and sums combined through shared
 //    memory), masks causally, keeps a running maximum that is only raised
 //    when it grows by more than 2^8 (then O's row is rescaled in tensor
 //    memory), and writes P back into tensor memory, over its own S, as two
