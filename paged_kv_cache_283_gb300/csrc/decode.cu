@@ -101,21 +101,21 @@ struct SmemLayout {
   static constexpr int KT = I8 ? Geo::BS * D : Geo::TILE;      // bytes of one K (or V) tile
   static constexpr int STAGE = I8 ? 2 * KT + 2 * Geo::BS * 4 : 2 * KT;
   static constexpr int TILES = S * STAGE;
-  static constexpr int PS = Geo::BS * G * 4;       // softmax weights of one tile
-  static constexpr int ALPHA = ((G * 4 + 15) / 16) * 16;
+  // bf16: softmax weights of one tile and the heads' rescale factors (the
+  // 1-byte caches keep both in registers)
+  static constexpr int PS = I8 ? 0 : Geo::BS * G * 4;
+  static constexpr int ALPHA = I8 ? 0 : ((G * 4 + 15) / 16) * 16;
   static constexpr int BARS = S * 8;
   static constexpr int MERGE = (G * D + 2 * G) * 4;  // aliases TILES after the loop
   static constexpr int WARP = ((TILES + PS + ALPHA + BARS + 127) / 128) * 128;
-  // 1-byte caches: the CTA's prepared q (int8 cache: codes [G][D] then scales
-  // [G]; fp8 cache: see QF8)
+  // 1-byte caches: the int8 cache's quantised q, codes [G][D] then scales
+  // [G] (the fp8 cache's warps each build their own q words)
   static constexpr int QOFF = NW * WARP;
-  // (the fp8 cache: q's MMA fragment words and per-head factors, [word][lane])
   static constexpr int QI8 = ((G * D + G * 4 + 127) / 128) * 128;
-  static constexpr int QF8 = 32 * ((G < 8 ? 1 : 2) * D / 16 + 2) * 4;
-  static constexpr int QREG = I8 ? (QI8 > QF8 ? QI8 : QF8) : 0;
+  static constexpr int QREG = I8 ? QI8 : 0;
   // fused decode step: the new row staged for the patch (bf16: K and V rows;
   // 1-byte: K codes, V codes, the two scales)
-  static constexpr int PATCHOFF = NW * WARP + QREG;
+  static constexpr int PATCHOFF = QOFF + QREG;
   static constexpr int PATCH = 4 * D + 32;
   static constexpr int TOTAL = PATCHOFF + PATCH;
   static_assert(MERGE <= TILES, "merge area must fit in the tile ring");
@@ -235,13 +235,13 @@ __device__ __forceinline__ void patch_tile(unsigned char* tile, int kt_bytes,
 
 // Q: the cache's element type: 0 = bf16, 1 = INT8, 2 = FP8 (E4M3).  INT8 and
 // FP8 share the 1-byte-code tile layout (codes + per-token scales) and the
-// tensor-core PV; INT8 quantises q and takes QK in integers, FP8 takes QK on
-// the tensor cores as well (f16 MMAs on the exactly converted codes).
+// tile step (tile_step_1b: QK and PV on the tensor cores, weights in
+// registers); INT8 quantises q and its QK is exact in integers (f16 MMAs on
+// the codes), FP8 takes QK in E4M3 on two exact parts of q.
 template <int D, int G, int NW, int S, bool SPLIT, int Q>
 __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     paged_decode_kernel(const DecodeParams p) {
   constexpr bool I8 = Q != 0;   // 1-byte codes + scales
-  constexpr bool QI = Q == 1;   // INT8 QK
   using Geo = Geometry<D, G>;
   using Lay = SmemLayout<D, G, NW, S, I8>;
   constexpr int BS = Geo::BS, L = Geo::L, P = Geo::P, R = Geo::R;
@@ -288,108 +288,72 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   };
   int ctx = __ldg(p.context_lens + b);
   int ids_cur = load_ids(0);
-  using IG = I8Geometry<D, G>;
-  const int qsub = lane % IG::QL;  // int8 cache: this lane in the QK geometry
-  const int qrg = lane / IG::QL;
   float2 q2[G][4];
-  int qc[G][IG::QW];  // int8 cache: this lane's q codes, 4 per word
-  float qsc[G];       // int8 cache: q scale times scale * log2(e)
-  uint32_t qe[QCols<G>::NQ][D / 32][2];  // fp8 cache: q's E4M3 MMA fragments (tile_step_f8)
-  float2 qfac;  // fp8 cache: 2^-k * scale * log2 e of the lane's two score heads
+  // 1-byte caches: the lane's q words for the QK MMAs and its head's score
+  // factor (tile_step_1b)
+  uint32_t qa[D / 8];
+  float qf = 0.f;
+  float qoff = 0.f;  // int8 cache: 128 * the sum of head(gid)'s q codes (tile_step_1b)
   // q of the group into this lane's registers (or, for the int8 cache,
   // quantised through shared memory): the inputs a preceding kernel may
   // still be writing, so with early reads this runs after the wait.
   auto load_q = [&]() {
     if constexpr (Q == 2) {
-      // Lane (gid, tig) builds MMA column gid's fragments: head hn = head(gid),
-      // dims [(D/4) tig, +D/4).  The head's values times 2^k, k chosen per head
-      // so that its largest |q| lands in [128, 256), are split into two E4M3
-      // parts, x = q1 + 2^-5 q2 with q1 = E4M3(x), q2 = E4M3(32 (x - q1)): a
-      // bf16 value has 8 significant bits and q1 keeps 4 of them, and
-      // |x - q1| <= 8 (half a step of q1 below 256), so 32 (x - q1) <= 256 is
-      // exact in q2 except where it falls below E4M3's normal range: an error
-      // under 2^-14 absolute, about 2^-21 of the head's largest |q|.  G <= 4:
-      // column gid carries part(gid) (parts >= 2 are zeros); G = 8: both parts,
-      // one fragment set each.  Step s's fragment words are dims (D/4) tig + 8s
-      // + 0..3 and + 4..7.  Every warp needs the same fragments: warp 0 builds
-      // them into shared memory ([word][lane]) and the others load them.
+      // Every warp builds its own words (no barrier): lane (gid, tig) takes
+      // head hn = head(gid), dims [(D/4) tig, +D/4).  The head's values times
+      // 2^k, k chosen per head so that its largest |q| lands in [128, 256),
+      // are split into two E4M3 parts, x = q1 + 2^-5 q2 with q1 = E4M3(x),
+      // q2 = E4M3(32 (x - q1)): a bf16 value has 8 significant bits and q1
+      // keeps 4 of them, and |x - q1| <= 8 (half a step of q1 below 256), so
+      // 32 (x - q1) <= 256 is exact in q2 except where it falls below E4M3's
+      // normal range: an error under 2^-14 absolute, about 2^-21 of the
+      // head's largest |q|.
       using C = QCols<G>;
-      constexpr int NWORD = C::NQ * D / 16;
-      uint32_t* qsm = reinterpret_cast<uint32_t*>(smem + Lay::QOFF);
-      if (warp == 0) {
-        constexpr int E = D / 4;
-        const int gid = lane >> 2, tig = lane & 3;
-        const int hn = C::head(gid);
-        float f[E];
-        const __nv_bfloat16* qh =
-            p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + hn) * D +
-            E * tig;
-    #pragma unroll
-        for (int u = 0; u < E / 8; ++u) {
-          const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
-          const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
-          const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
-          f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
-          f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
-        }
-        float amax = 0.f;
-    #pragma unroll
-        for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-        // biased exponent of amax (0 for 0 and subnormals); k = 7 - unbiased
-        const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
-        const int kexp = min(127, max(-126, 134 - ebits));
-        const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
-        const int pn = C::part(gid);
-    #pragma unroll
-        for (int j = 0; j < E / 4; ++j) {
-          uint32_t w1 = 0, w2 = 0;
-    #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float x0 = f[4 * j + 2 * h] * up, x1 = f[4 * j + 2 * h + 1] * up;
-            const __nv_fp8x2_storage_t c1 =
-                __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
-            const __half2_raw r1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
-            __half2 r1h;
-            r1h = *reinterpret_cast<const __half2*>(&r1);
-            const float2 q1 = __half22float2(r1h);
-            const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
-                make_float2((x0 - q1.x) * 32.f, (x1 - q1.y) * 32.f), __NV_SATFINITE, __NV_E4M3);
-            w1 |= static_cast<uint32_t>(c1) << (16 * h);
-            w2 |= static_cast<uint32_t>(c2) << (16 * h);
-          }
-          if constexpr (C::PACKED) {
-            qe[0][j / 2][j % 2] = pn == 0 ? w1 : (pn == 1 ? w2 : 0u);
-          } else {
-            qe[0][j / 2][j % 2] = w1;
-            qe[C::NQ - 1][j / 2][j % 2] = w2;
-          }
-        }
-        const float fac = ldexpf(p.scale_log2, -kexp);
-        const int ha = C::head(2 * tig);
-        qfac = make_float2(__shfl_sync(kFullMask, fac, 4 * ha),
-                           __shfl_sync(kFullMask, fac, 4 * (ha + 1)));
-    #pragma unroll
-        for (int n = 0; n < C::NQ; ++n)
-    #pragma unroll
-          for (int s2 = 0; s2 < D / 32; ++s2)
-    #pragma unroll
-            for (int h = 0; h < 2; ++h) qsm[((n * (D / 32) + s2) * 2 + h) * 32 + lane] = qe[n][s2][h];
-        qsm[NWORD * 32 + lane] = __float_as_uint(qfac.x);
-        qsm[(NWORD + 1) * 32 + lane] = __float_as_uint(qfac.y);
+      constexpr int E = D / 4;
+      const int gid = lane >> 2, tig = lane & 3;
+      const int hn = C::head(gid);
+      float f[E];
+      const __nv_bfloat16* qh =
+          p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G + hn) * D +
+          E * tig;
+  #pragma unroll
+      for (int u = 0; u < E / 8; ++u) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(qh) + u);
+        const float2 a = bf16x2_to_float2(w.x), c = bf16x2_to_float2(w.y);
+        const float2 d = bf16x2_to_float2(w.z), e = bf16x2_to_float2(w.w);
+        f[8 * u] = a.x; f[8 * u + 1] = a.y; f[8 * u + 2] = c.x; f[8 * u + 3] = c.y;
+        f[8 * u + 4] = d.x; f[8 * u + 5] = d.y; f[8 * u + 6] = e.x; f[8 * u + 7] = e.y;
       }
-      __syncthreads();
-      if (warp != 0) {
+      float amax = 0.f;
   #pragma unroll
-        for (int n = 0; n < C::NQ; ++n)
+      for (int k = 0; k < E; ++k) amax = fmaxf(amax, fabsf(f[k]));
+      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+      // biased exponent of amax (0 for 0 and subnormals); k = 7 - unbiased
+      const int ebits = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+      const int kexp = min(127, max(-126, 134 - ebits));
+      const float up = __uint_as_float(static_cast<uint32_t>(kexp + 127) << 23);
   #pragma unroll
-          for (int s2 = 0; s2 < D / 32; ++s2)
+      for (int j = 0; j < E / 4; ++j) {  // word j: dims (D/4) tig + 4j + 0..3
+        uint32_t w1 = 0, w2 = 0;
   #pragma unroll
-            for (int h = 0; h < 2; ++h) qe[n][s2][h] = qsm[((n * (D / 32) + s2) * 2 + h) * 32 + lane];
-        qfac = make_float2(__uint_as_float(qsm[NWORD * 32 + lane]),
-                           __uint_as_float(qsm[(NWORD + 1) * 32 + lane]));
+        for (int h = 0; h < 2; ++h) {
+          const float x0 = f[4 * j + 2 * h] * up, x1 = f[4 * j + 2 * h + 1] * up;
+          const __nv_fp8x2_storage_t c1 =
+              __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
+          const __half2_raw r1 = __nv_cvt_fp8x2_to_halfraw2(c1, __NV_E4M3);
+          __half2 r1h;
+          r1h = *reinterpret_cast<const __half2*>(&r1);
+          const float2 q1 = __half22float2(r1h);
+          const __nv_fp8x2_storage_t c2 = __nv_cvt_float2_to_fp8x2(
+              make_float2((x0 - q1.x) * 32.f, (x1 - q1.y) * 32.f), __NV_SATFINITE, __NV_E4M3);
+          w1 |= static_cast<uint32_t>(c1) << (16 * h);
+          w2 |= static_cast<uint32_t>(c2) << (16 * h);
+        }
+        qa[4 * (j / 2) + 2 * (j % 2)] = w1;      // row gid: q1
+        qa[4 * (j / 2) + 2 * (j % 2) + 1] = w2;  // row gid + 8: q2
       }
+      qf = ldexpf(p.scale_log2, -kexp);
     } else if constexpr (Q == 0) {
       const __nv_bfloat16* qb =
           p.q + (static_cast<size_t>(b) * p.num_q_heads + static_cast<size_t>(kvh) * G) * D + sub * 8;
@@ -447,11 +411,28 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
         if (lane == 0) qs[g] = qscale;
       }
       __syncthreads();
+      // the lane's words: head(gid)'s codes at dims [(D/4) tig, +D/4) as
+      // exact f16 pairs
+      const int gid = lane >> 2, tig = lane & 3;
+      const int hn = QCols<G>::head(gid);
+      const unsigned char* row = q8 + hn * D + (D / 4) * tig;
+      int qsum = 0;
   #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        i8_load_row<IG::QB>(q8 + g * D, qsub, qrg, qc[g]);
-        qsc[g] = qs[g] * p.scale_log2;
+      for (int u = 0; u < D / 64; ++u) {
+        const uint4 x = *reinterpret_cast<const uint4*>(row + 16 * u);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t ob = xw[k] ^ 0x80808080u;
+          qa[2 * (4 * u + k)] = ob8x2_to_f16x2<0x4140>(ob);
+          qa[2 * (4 * u + k) + 1] = ob8x2_to_f16x2<0x4342>(ob);
+          qsum = __dp4a(static_cast<int>(xw[k]), 0x01010101, qsum);
+        }
       }
+      qsum += __shfl_xor_sync(kFullMask, qsum, 1);
+      qsum += __shfl_xor_sync(kFullMask, qsum, 2);
+      qoff = 128.f * static_cast<float>(qsum);
+      qf = qs[hn] * p.scale_log2;
     }
   };
   if (!p.early_read) load_q();
@@ -575,19 +556,12 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     for (int k = 0; k < 4; ++k) acc8[c][k] = 0.f;
   float m_run = -INFINITY;  // running max of this lane's head, base-2 units
   float l_run = 0.f;        // this lane's share of that head's exp-sum
-  float2 m_run2 = make_float2(-INFINITY, -INFINITY);  // fp8 cache: heads 2 tig, 2 tig + 1
-  float2 l_run2 = make_float2(0.f, 0.f);
+  float wsum = 0.f;         // int8 cache: this lane's share of its PV column's weights
   // 1-byte caches: the warp's power-of-two bound on the V scales it has
   // weighted (raise_v_bound) and its reciprocal; acc8 is in units of it
   float vbound = 0x1p-126f, vinv = 0x1p126f;
-  // The lane geometry of the scores and softmax state: the bf16 step's, or
-  // the int8 QK geometry.
-  constexpr int SL = QI ? IG::QL : L;
-  constexpr int SHL = QI ? IG::HEAD_LANES : Geo::HEAD_LANES;
-  const int ssub = QI ? qsub : sub;
-  const int srg = QI ? qrg : rg;
-  const int my_head = QI ? (qsub * IG::R) / IG::P : (sub * R) / P;
-  const int my_i0 = QI ? (qsub * IG::R) % IG::P : (sub * R) % P;
+  const int my_head = (sub * R) / P;  // bf16 cache: the lane's score head and first pass
+  const int my_i0 = (sub * R) % P;
 
   const int npro = nw < S ? nw : S;
   for (int i = 0; i < npro; ++i) issue(i, i);
@@ -626,26 +600,15 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     } else {
       const float* ksc = reinterpret_cast<const float*>(stage + 2 * Lay::KT);
       const float* vsc = ksc + BS;
-      if constexpr (QI) {
-        if (nvalid == BS)
-          tile_step_i8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                   m_run, l_run, vbound, vinv, nvalid, lane, qsub, qrg, my_head,
-                                   my_i0);
-        else
-          tile_step_i8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, alpha_s, qc, qsc, acc8,
-                                    m_run, l_run, vbound, vinv, nvalid, lane, qsub, qrg, my_head,
-                                    my_i0);
-      } else {
-        if (nvalid == BS)
-          tile_step_f8<D, G, true>(stage, stage + Lay::KT, ksc, vsc, ps, qe, qfac, acc8, m_run2,
-                                   l_run2, vbound, vinv, nvalid, lane);
-        else
-          tile_step_f8<D, G, false>(stage, stage + Lay::KT, ksc, vsc, ps, qe, qfac, acc8, m_run2,
-                                    l_run2, vbound, vinv, nvalid, lane);
-      }
+      if (nvalid == BS)
+        tile_step_1b<D, G, Q == 2, true>(stage, stage + Lay::KT, ksc, vsc, qa, qf, qoff, acc8,
+                                         m_run, l_run, wsum, vbound, vinv, nvalid, lane);
+      else
+        tile_step_1b<D, G, Q == 2, false>(stage, stage + Lay::KT, ksc, vsc, qa, qf, qoff, acc8,
+                                          m_run, l_run, wsum, vbound, vinv, nvalid, lane);
     }
     consumed = i + 1;
-    __syncwarp();  // every lane is done with this stage and with ps / alpha_s
+    __syncwarp();  // every lane is done with this stage (and, bf16, with ps / alpha_s)
     if (i + S < nw) issue(i + S, st);
     if (++st == S) {
       st = 0;
@@ -673,17 +636,14 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
                  : "memory");
 
   // Per-warp totals: l over the lanes of each head, acc over row groups.
-  if constexpr (Q == 2) {
-#pragma unroll
-    for (int m = 4; m < 32; m <<= 1) {
-      l_run2.x += __shfl_xor_sync(kFullMask, l_run2.x, m);
-      l_run2.y += __shfl_xor_sync(kFullMask, l_run2.y, m);
-    }
+  if constexpr (I8) {  // the 4 lanes of each row of the QK MMA
+    l_run += __shfl_xor_sync(kFullMask, l_run, 1);
+    l_run += __shfl_xor_sync(kFullMask, l_run, 2);
   } else {
 #pragma unroll
-    for (int m = 1; m < SHL; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+    for (int m = 1; m < Geo::HEAD_LANES; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
 #pragma unroll
-    for (int m = SL; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
+    for (int m = L; m < 32; m <<= 1) l_run += __shfl_xor_sync(kFullMask, l_run, m);
   }
   // Merge warps through shared memory (each warp writes into its own, now
   // idle, tile ring): [G][D] acc, then m[G], l[G].
@@ -718,6 +678,22 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
         for (int k = 0; k < 4; ++k) acc8[c][k] += __shfl_xor_sync(kFullMask, acc8[c][k], G / 2);
     }
     const int gid = lane >> 2, tig = lane & 3;
+    if constexpr (Q == 1) {
+      // int8: the sums held 2^-24 (w . v + 128 sum w); the weights of
+      // columns 2 tig, 2 tig + 1 (heads 2 tig, 2 tig + 1 on the part-0
+      // lanes) come from rows 2 tig and 2 tig + 1
+      wsum += __shfl_xor_sync(kFullMask, wsum, 1);
+      wsum += __shfl_xor_sync(kFullMask, wsum, 2);
+      const float wa = 128.f * __shfl_sync(kFullMask, wsum, 8 * tig);
+      const float wb = 128.f * __shfl_sync(kFullMask, wsum, 8 * tig + 4);
+#pragma unroll
+      for (int c = 0; c < D / 16; ++c) {
+        acc8[c][0] = fmaf(acc8[c][0], 0x1p24f, -wa);
+        acc8[c][1] = fmaf(acc8[c][1], 0x1p24f, -wb);
+        acc8[c][2] = fmaf(acc8[c][2], 0x1p24f, -wa);
+        acc8[c][3] = fmaf(acc8[c][3], 0x1p24f, -wb);
+      }
+    }
     if (C::part0(tig)) {
       const int ha = C::head(2 * tig);
 #pragma unroll
@@ -730,17 +706,12 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       }
     }
   }
-  if constexpr (Q == 2) {
-    const int h0 = 2 * lane;  // lanes 0-3 (gid 0): heads 2 tig, 2 tig + 1
-    if (lane < 4 && h0 < G) {
-      mrg[G * D + h0] = m_run2.x;
-      mrg[G * D + G + h0] = l_run2.x;
+  if constexpr (I8) {  // head gid's state, from its part-0 row
+    if (lane % 4 == 0 && lane / 4 < G) {
+      mrg[G * D + lane / 4] = m_run;
+      mrg[G * D + G + lane / 4] = l_run;
     }
-    if (lane < 4 && h0 + 1 < G) {
-      mrg[G * D + h0 + 1] = m_run2.y;
-      mrg[G * D + G + h0 + 1] = l_run2.y;
-    }
-  } else if (srg == 0 && ssub % SHL == 0) {
+  } else if (rg == 0 && sub % Geo::HEAD_LANES == 0) {
     mrg[G * D + my_head] = m_run;
     mrg[G * D + G + my_head] = l_run;
   }
