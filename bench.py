@@ -40,6 +40,10 @@ METRIC = "paged decode-attention achieved HBM GB/s (frac of ~8 TB/s) and seq-lay
 UNIT = "GB/s"
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e nominal, context only
 E2E_MIN_SECONDS = 0.25    # shortest end-to-end timed window
+# --step shared-prefix: the prefix's tensor-core partitions (tokens) and the
+# split-K partition size of the rest of each context
+SHARED_PREFIX_SPLIT = 256
+SHARED_PREFIX_PARTITION = 512
 
 
 # ---------------------------------------------------------------------------
@@ -450,7 +454,8 @@ def _setup(idx, device, replicas_min_bytes, kv_dtype="bf16", max_layers=None, n_
     return st
 
 
-def _attn_fns(st, attn, partition, fused=True, order=None, early_read=False):
+def _attn_fns(st, attn, partition, fused=True, order=None, early_read=False,
+              shared_prefix=False):
     import torch
 
     from paged_kv_cache_283_gb300 import pa
@@ -461,6 +466,33 @@ def _attn_fns(st, attn, partition, fused=True, order=None, early_read=False):
     if attn == "splitk":
         ws = pa.splitk_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
                                  int(w.context_lens.max()), partition, st["q"][0].device)
+
+    if shared_prefix:
+        # the shared-prefix step: the prefix's partitions for the whole batch
+        # on the tensor cores, the rest by split-K with the cache write and
+        # the merge (two launches per layer)
+        dev = st["q"][0].device
+        sp_ws = pa.shared_prefix_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
+                                           int(w.context_lens.max()), w.prefix_len,
+                                           SHARED_PREFIX_SPLIT, partition, dev)
+        sp_cnt = pa.step_counters(w.num_seqs, w.num_kv_heads, dev)
+        if order is None:
+            order = torch.from_numpy(pa.shared_prefix_order(
+                w.context_lens, w.prefix_len, partition, sp_ws[1].shape[2],
+                SHARED_PREFIX_SPLIT)).to(dev)
+
+        def prefix_layer(layer, *pool):
+            pa.pa_decode_step_shared_prefix(outs[layer], st["q"][layer], pool[0], pool[1],
+                                            st["bt"], st["ctx"], w.scale, w.prefix_len,
+                                            SHARED_PREFIX_SPLIT, partition, sp_ws, sp_cnt,
+                                            key=st["key"][layer], value=st["value"][layer],
+                                            slot_mapping=st["slots"], order=order)
+
+        def prefix_step(r):
+            for layer, pool in enumerate(st["replicas"][r]):
+                prefix_layer(layer, *pool)
+
+        return prefix_step, prefix_layer, outs
 
     if fused:
         # one pa_decode_step launch per layer: cache write + attention (+ merge)
@@ -526,6 +558,19 @@ def step_launch(workload_idx, w, kv="bf16", step="fused", attn="auto", partition
       launch's pool are not written by it (PA_STEP_EARLY_READ's contract)."""
     from paged_kv_cache_283_gb300 import pa
     attn = "splitk" if attn == "auto" else attn
+    if step == "shared-prefix":
+        if not w.prefix_len or kv != "bf16":
+            raise ValueError("--step shared-prefix: the shared-prefix workload, bf16 cache")
+        part = partition or SHARED_PREFIX_PARTITION
+        maxp = pa.shared_prefix_partitions(int(w.context_lens.max()), w.prefix_len,
+                                           SHARED_PREFIX_SPLIT, part)
+        return {"attn": "splitk", "fused": False, "shared_prefix": True, "partition": part,
+                "partition_choice": "given" if partition else
+                "%d after the prefix (the prefix: %d tensor-core partitions of %d)"
+                % (part, w.prefix_len // SHARED_PREFIX_SPLIT, SHARED_PREFIX_SPLIT),
+                "order": pa.shared_prefix_order(w.context_lens, w.prefix_len, part, maxp,
+                                                SHARED_PREFIX_SPLIT),
+                "plan": None, "early_read": False}
     fused = step == "fused"
     choice = "given"
     if partition is None and workload_idx == 3:
@@ -538,9 +583,9 @@ def step_launch(workload_idx, w, kv="bf16", step="fused", attn="auto", partition
         if plan.chosen:
             choice = "pa_splitk_partition_size (makespan model)"
         partition = plan.partition_size
-    return {"attn": attn, "fused": fused, "partition": partition, "partition_choice": choice,
-            "order": plan.order if plan is not None else None, "plan": plan,
-            "early_read": fused and early_read == "on"}
+    return {"attn": attn, "fused": fused, "shared_prefix": False, "partition": partition,
+            "partition_choice": choice, "order": plan.order if plan is not None else None,
+            "plan": plan, "early_read": fused and early_read == "on"}
 
 
 def recorded_traffic(kernel, workload_name, partition, sources=("decode.cu", "decode_tile.cuh")):
@@ -635,7 +680,8 @@ def run_gpu(args):
     args.partition, partition_choice = lp["partition"], lp["partition_choice"]
     ordered = lp["order"] is not None
     order = torch.from_numpy(lp["order"]).to(device) if ordered else None
-    step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order, early)
+    step, dominant, outs = _attn_fns(st, attn, args.partition, fused, order, early,
+                                     lp["shared_prefix"])
 
     # eager warmup (sets kernel attributes, checks the error word)
     with torch.cuda.stream(stream):
@@ -645,7 +691,8 @@ def run_gpu(args):
     assert pa.pa_get_device_error() == 0, "device error word set during warmup"
 
     graphs = [_capture(lambda r=r: step(r), stream) for r in range(len(st["replicas"]))]
-    launches_per_step = nl * (1 if fused else (2 if attn == "decode" else 3))
+    launches_per_step = nl * (2 if lp["shared_prefix"] else
+                              1 if fused else (2 if attn == "decode" else 3))
 
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     sampler.start()
@@ -680,7 +727,8 @@ def run_gpu(args):
     dom_dt = _time_graphs(dom_graphs, n_dom, stream) / (n_dom * nl)
 
     # end to end through the public API with pinned host buffers
-    e2e = _e2e(st, attn, args, stream, order, early) if not args.no_e2e else None
+    e2e = (_e2e(st, attn, args, stream, order, early, lp["shared_prefix"]) if not args.no_e2e
+           else None)
     assert pa.pa_get_device_error() == 0, "device error word set during the run"
 
     step_bytes = nl * (decode_bytes(w.context_lens, w.num_seqs, w.num_q_heads,
@@ -694,7 +742,9 @@ def run_gpu(args):
     dt_max, value = combine_ranks(dt, step_bytes, args.steps, world, device)
     hbm_peak = peaks.get("hbm_gbs")
     achieved = dom_bytes / dom_dt / 1e9
-    if fused:
+    if lp["shared_prefix"]:
+        kname = kkey = "pa_decode_step_shared_prefix (prefix partials; split-K rest + merge)"
+    elif fused:
         kname = ("pa_decode_step" + KV_SUFFIX[args.kv]
                  + (" (split-K %d, merged in-kernel)" % args.partition if attn == "splitk"
                     else " (whole sequence)"))
@@ -712,7 +762,12 @@ def run_gpu(args):
                 else "fallback 6.8 TB/s",
                 "bytes_per_launch": dom_bytes, "us_per_launch": round(dom_dt * 1e6, 2)}
     sfx = KV_SUFFIX[args.kv]
-    if fused:
+    if lp["shared_prefix"]:
+        attention = ("pa_decode_step_shared_prefix: the %d-token prefix as %d tensor-core "
+                     "partitions for the whole batch, the rest by split-K (partition %d) with "
+                     "the cache write and the merge (two launches)"
+                     % (w.prefix_len, w.prefix_len // SHARED_PREFIX_SPLIT, args.partition))
+    elif fused:
         attention = ("pa_decode_step%s: cache write + split-K (partition %d) + merge in one launch"
                      % (sfx, args.partition) if attn == "splitk" else
                      "pa_decode_step%s: cache write + whole-sequence decode in one launch" % sfx)
@@ -775,7 +830,7 @@ def run_gpu(args):
     return 0
 
 
-def _e2e(st, attn, args, stream, order=None, early=False):
+def _e2e(st, attn, args, stream, order=None, early=False, shared_prefix=False):
     """Same metric through the public API: every step, the step's inputs (q,
     the new tokens' K/V, slots, block tables, context lengths, all layers)
     go from a pinned host buffer to the device in one copy, the library's step
@@ -817,6 +872,23 @@ def _e2e(st, attn, args, stream, order=None, early=False):
             views[(name, layer)] = staged[off:off + n].view(t.dtype).view(t.shape)
         out = torch.empty((layers,) + tuple(st["q"][0].shape), dtype=torch.bfloat16, device=dev)
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        def sp_step(l, pool, views=views, out=out):
+            sp_ws = pa.shared_prefix_workspace(w.num_seqs, w.num_q_heads, w.head_dim,
+                                               int(w.context_lens.max()), w.prefix_len,
+                                               SHARED_PREFIX_SPLIT, args.partition, dev)
+            sp_cnt = pa.step_counters(w.num_seqs, w.num_kv_heads, dev)
+            return pa.SharedPrefixStep(
+                out[l], views[("q", l)], pool[0], pool[1], views[("bt", 0)], views[("ctx", 0)],
+                w.scale, w.prefix_len, SHARED_PREFIX_SPLIT, args.partition, sp_ws, sp_cnt,
+                key=views[("key", l)], value=views[("value", l)], slot_mapping=views[("slots", 0)],
+                order=views[("order", 0)] if order is not None else None, stream=stream)
+        if shared_prefix:
+            sets.append({"host": host, "staged": staged, "out": out, "hout": hout,
+                         "steps": [[sp_step(l, pool) for l, pool in enumerate(st["replicas"][r])]
+                                   for r in range(nrep)],
+                         "in_done": torch.cuda.Event(), "computed": torch.cuda.Event(),
+                         "out_done": torch.cuda.Event()})
+            continue
         steps = [[pa.DecodeStep(views[("key", l)], views[("value", l)], pool[0], pool[1],
                                 views[("slots", 0)], views[("q", l)], views[("bt", 0)],
                                 views[("ctx", 0)], out[l], w.scale, split=attn == "splitk",
@@ -873,9 +945,11 @@ def _e2e(st, attn, args, stream, order=None, early=False):
     return {"value": round(step_bytes * n / dt / 1e9, 1), "unit": UNIT,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(sets[0]["hout"].numel() * 2),
             "ms_per_step": dt / n * 1e3, "steps": n, "seconds": round(dt, 3),
-            "how": "pa.DecodeStep per layer (pre-marshalled C calls; %s); every step one pinned "
-                   % ("one pa_decode_step launch" if args.step == "fused"
-                      else "separate cache-write / attention / merge launches") +
+            "how": ("pa.SharedPrefixStep per layer (pre-marshalled C calls; two launches); "
+                    "every step one pinned " if shared_prefix else
+                    "pa.DecodeStep per layer (pre-marshalled C calls; %s); every step one pinned "
+                    % ("one pa_decode_step launch" if args.step == "fused"
+                       else "separate cache-write / attention / merge launches")) +
                    "host->device copy of all inputs and one device->host copy of the output, "
                    "double-buffered on two copy streams; wall clock around all steps"}
 
@@ -1145,10 +1219,12 @@ def main(argv=None):
     ap.add_argument("--order", default="longest", choices=["longest", "grid"],
                     help="fused split-K: CTAs handed out longest first (pa_splitk_order) "
                          "or in grid order")
-    ap.add_argument("--step", default="fused", choices=["fused", "separate"],
+    ap.add_argument("--step", default="fused", choices=["fused", "separate", "shared-prefix"],
                     help="fused: one pa_decode_step launch per layer (cache write + attention "
                          "+ split-K merge); separate: the cache write, partition pass and "
-                         "merge as three launches")
+                         "merge as three launches; shared-prefix (the shared-prefix workload): "
+                         "pa_decode_step_shared_prefix, the prefix on the tensor cores once "
+                         "for the whole batch")
     ap.add_argument("--partition", type=int, default=None,
                     help="split-K partition size in tokens (default: 512 for the long-context "
                          "workload, else chosen by pa_splitk_partition_size)")

@@ -100,6 +100,7 @@ typedef enum {
 #define PA_DEVERR_SLOT 0x4u         /* slot >= num_blocks * block_size */
 #define PA_DEVERR_WAIT_TIMEOUT 0x8u /* an asynchronous copy did not complete in time */
 #define PA_DEVERR_ORDER 0x10u       /* a work-order entry outside [0, num_seqs * max_partitions) */
+#define PA_DEVERR_PREFIX 0x20u      /* a sequence does not hold the shared prefix it was given */
 
 /* Static description of a status code; never NULL. */
 const char* pa_status_string(pa_status status);
@@ -415,6 +416,52 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
                              int num_blocks, float scale, int partition_size, float* ws_out,
                              float* ws_m, float* ws_l, unsigned* counters, int max_partitions,
                              const int32_t* order, int flags, pa_stream_t stream);
+
+/*
+ * Fused decode step of a batch sharing a prefix [SH], [WALK] Step 8: every
+ * sequence's first prefix_len tokens are the same blocks (block_tables[b][j]
+ * == block_tables[0][j] for j < prefix_len / block_size, e.g. forks of one
+ * prompt) and its context goes past them (context_lens[b] > prefix_len).
+ * Computes what pa_decode_step computes (the new tokens' cache write, then
+ * attention) but reads the prefix's K/V once per KV head for the whole batch
+ * instead of once per sequence.  Two launches: (1) the prefix in partitions
+ * of prefix_split tokens, each one tensor-core pass in which the queries of
+ * all sequences and heads of a KV group attend to that partition's keys
+ * together (the chunked-prefill kernel without a causal mask), writing
+ * split-K partials to workspace partitions 0 .. prefix_len / prefix_split -
+ * 1; (2) the split-K decode with the cache write over the rest of each
+ * context, in partitions of partition_size tokens from the prefix's end
+ * (workspace partitions from prefix_len / prefix_split on), overlapping (1)
+ * and merging all of a sequence's partitions in its last CTA (counters as
+ * pa_decode_step's).  A sequence whose table does not hold the prefix, or
+ * whose context does not go past it, sets PA_DEVERR_PREFIX (its output is
+ * then wrong).
+ *   prefix_split: a multiple of block_size dividing prefix_len;
+ *   partition_size: a multiple of block_size; workspace as pa_decode_splitk's
+ *   with max_partitions > prefix_len / prefix_split and at least
+ *   prefix_len / prefix_split + ceil((context_lens[b] - prefix_len) /
+ *   partition_size) for every b (else PA_DEVERR_CONTEXT_LEN).
+ *   order (may be NULL): the work order of launch (2)'s CTAs, device int32
+ *     [num_seqs * (max_partitions - prefix_len / prefix_split)], a
+ *     permutation of its items item = part * num_seqs + b over the
+ *     partitions past the prefix (pa_splitk_order of the lengths past the
+ *     prefix gives the longest first); as pa_decode_step's order otherwise.
+ *   bf16 cache, head_dim and group supported by both pa_decode_supported
+ *     and pa_prefill_supported (else PA_ERR_UNSUPPORTED_SHAPE); other
+ *     arguments as pa_decode_step (key / value / slot_mapping all NULL:
+ *     attention only).
+ * Asynchronous on `stream`.
+ */
+pa_status pa_decode_step_shared_prefix(void* out, const void* q, const void* key,
+                                       const void* value, const int64_t* slot_mapping,
+                                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks, float scale,
+                                       int prefix_len, int prefix_split, int partition_size,
+                                       float* ws_out, float* ws_m, float* ws_l,
+                                       unsigned* counters, int max_partitions,
+                                       const int32_t* order, pa_stream_t stream);
 
 /*
  * Paged (chunked) prefill attention ("How LLM Inference Serving Works",

@@ -565,6 +565,76 @@ pa_status decode_step_impl(void* out, const void* q, const void* key, const void
 
 extern "C" {
 
+// Shared-prefix decode step: the prefix's partitions by the tensor-core
+// prefill kernel (all queries of the batch against the shared keys), the
+// rest by the fused split-K decode (with the cache write), which overlaps the
+// first and merges every sequence's partitions in its last CTA.
+pa_status pa_decode_step_shared_prefix(void* out, const void* q, const void* key,
+                                       const void* value, const int64_t* slot_mapping,
+                                       void* k_cache, void* v_cache, const int32_t* block_tables,
+                                       int max_blocks_per_seq, const int32_t* context_lens,
+                                       int num_seqs, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks, float scale,
+                                       int prefix_len, int prefix_split, int partition_size,
+                                       float* ws_out, float* ws_m, float* ws_l,
+                                       unsigned* counters, int max_partitions,
+                                       const int32_t* order, pa_stream_t stream) {
+  pa_status s = check_decode_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                  block_size, num_blocks, scale);
+  if (s != PA_OK) return s;
+  if (prefix_split <= 0 || prefix_split % block_size != 0 || prefix_len <= 0 ||
+      prefix_len % prefix_split != 0 || prefix_len / block_size > max_blocks_per_seq ||
+      partition_size <= 0 || partition_size % block_size != 0 ||
+      max_partitions <= prefix_len / prefix_split || max_partitions > 65535)
+    return PA_ERR_INVALID_ARG;
+  if (!pa_prefill_supported(head_dim, num_q_heads / num_kv_heads, block_size) ||
+      num_seqs > 65535)
+    return PA_ERR_UNSUPPORTED_SHAPE;
+  if (num_seqs == 0) return PA_OK;
+  const bool write = key != nullptr || value != nullptr || slot_mapping != nullptr;
+  if (!ok_ptr(out, 16) || !ok_ptr(ws_out, 16) || !ok_ptr(ws_m, 4) || !ok_ptr(ws_l, 4) ||
+      !ok_ptr(counters, 4))
+    return PA_ERR_INVALID_ARG;
+  if (write && (!ok_ptr(key, 16) || !ok_ptr(value, 16) || !ok_ptr(slot_mapping, 8)))
+    return PA_ERR_INVALID_ARG;
+  const int splits = prefix_len / prefix_split;
+  if (order != nullptr) {
+    if (!ok_ptr(order, 4)) return PA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(num_seqs) * (max_partitions - splits) > 65535)
+      return PA_ERR_UNSUPPORTED_SHAPE;
+  }
+  unsigned* err = device_error_word();
+  if (!err) return cuda_fail(cudaGetLastError());
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_prefix_partials(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                         context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                         num_blocks, scale, prefix_split / block_size, splits,
+                                         ws_out, ws_m, ws_l, max_partitions, err, st);
+  if (e != cudaSuccess) return cuda_fail(e);
+  DecodeParams p = make_decode_params(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                      context_lens, num_seqs, num_q_heads, num_kv_heads,
+                                      num_blocks, scale);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  if (write) {
+    p.new_key = static_cast<const __nv_bfloat16*>(key);
+    p.new_value = static_cast<const __nv_bfloat16*>(value);
+    p.slot_mapping = slot_mapping;
+  }
+  p.ws_o = ws_out;
+  p.ws_m = ws_m;
+  p.ws_l = ws_l;
+  p.counters = counters;
+  p.max_partitions = max_partitions;
+  p.partition_blocks = partition_size / block_size;
+  p.first_partition = splits;
+  p.prefix_blocks = prefix_len / block_size;
+  p.order = order;
+  p.err = err;
+  e = launch_decode(p, head_dim, num_q_heads / num_kv_heads, true, st);
+  return e == cudaSuccess ? PA_OK : cuda_fail(e);
+}
+
 pa_status pa_decode_step(void* out, const void* q, const void* key, const void* value,
                          const int64_t* slot_mapping, void* k_cache, void* v_cache,
                          const int32_t* block_tables, int max_blocks_per_seq,

@@ -251,21 +251,27 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   // With early reads (the caller's promise that tables, lengths, order and
   // pools are not written by it) the wait comes after the first copies are
   // out, and before anything else is read or anything is written.
-  if (!p.early_read) griddep_wait();
+  // After a shared prefix (first_partition > 0) the preceding kernel computes
+  // the prefix's partitions and reads nothing this one writes, and its own
+  // predecessor is complete once it runs: wait for it only before reading its
+  // partitions (the merge) and before exiting.
+  const bool after_prefix = SPLIT && p.first_partition > 0;
+  if (!p.early_read && !after_prefix) griddep_wait();
   griddep_launch_dependents();
   const int kvh = blockIdx.x;
   // (sequence, partition): the grid's, or the order array's entry for this
   // CTA (its grid is then (Hkv, B * max_partitions, 1)); an entry out of
   // range is refused (the item it displaced does not run: the error says so)
-  int b = blockIdx.y, part = blockIdx.z;
-  if (SPLIT && p.order != nullptr) {
+  int b = blockIdx.y, part = blockIdx.z + (SPLIT ? p.first_partition : 0);
+  if (SPLIT && p.order != nullptr) {  // (items over the partitions from first_partition)
     const int item = __ldg(p.order + blockIdx.y);
-    if (item < 0 || item >= p.num_seqs * p.max_partitions) {
+    if (item < 0 || item >= p.num_seqs * (p.max_partitions - p.first_partition)) {
       if (threadIdx.x == 0) raise_error(p.err, PA_DEVERR_ORDER);
+      if (after_prefix) griddep_wait();
       return;
     }
     b = item % p.num_seqs;
-    part = item / p.num_seqs;
+    part = item / p.num_seqs + p.first_partition;
   }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -277,7 +283,21 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   // reads): the ids are read speculatively from the table slots this CTA may
   // use (in bounds whatever the context length is) and only those below the
   // context length are used, after a range check.
-  const int64_t part_first = SPLIT ? static_cast<int64_t>(part) * p.partition_blocks : 0;
+  // Split-K partitions: partition_blocks each from block 0, or after a shared
+  // prefix, first_partition prefix partitions (another kernel's) and then
+  // partition_blocks each from block prefix_blocks.
+  auto part_start = [&](int pt) -> int64_t {
+    return after_prefix ? p.prefix_blocks + static_cast<int64_t>(pt - p.first_partition) *
+                                                p.partition_blocks
+                        : static_cast<int64_t>(pt) * p.partition_blocks;
+  };
+  auto parts_of = [&](int n) -> int {  // partitions of a sequence of n blocks
+    return after_prefix
+               ? p.first_partition + max(0, (n - p.prefix_blocks + p.partition_blocks - 1) /
+                                                p.partition_blocks)
+               : (n + p.partition_blocks - 1) / p.partition_blocks;
+  };
+  const int64_t part_first = SPLIT ? part_start(part) : 0;
   const int tbl_end = SPLIT ? static_cast<int>(min(static_cast<int64_t>(p.max_blocks_per_seq),
                                                    part_first + p.partition_blocks))
                             : p.max_blocks_per_seq;
@@ -450,15 +470,19 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   // owner of the sequence's last block, in the CTA whose range holds it),
   // once its first copies are out; it patches its tile with the new row at
   // iteration patch_it.
-  const bool writer_cta = p.slot_mapping != nullptr &&
-                          (!SPLIT || part == (nblk > 0 ? (nblk - 1) / p.partition_blocks : 0));
+  // (after a shared prefix only a block past the prefix is ever written)
+  const bool writer_cta =
+      p.slot_mapping != nullptr &&
+      (!SPLIT || (nblk > 0 ? (!after_prefix || nblk - 1 >= p.prefix_blocks) &&
+                                 part == parts_of(nblk) - 1
+                           : part == 0));
   const int last_blk = nblk > 0 ? nblk - 1 - (SPLIT ? static_cast<int>(part_first) : 0) : 0;
   if constexpr (SPLIT) {
-    if (part == 0 && threadIdx.x == 0 &&
-        (nblk + p.partition_blocks - 1) / p.partition_blocks > p.max_partitions)
+    if (part == (after_prefix ? p.first_partition : 0) && threadIdx.x == 0 &&
+        parts_of(nblk) > p.max_partitions)
       raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
     if (part_first >= nblk) {  // past the end of this sequence; CTA-uniform, nothing issued
-      if (p.early_read) griddep_wait();
+      if (p.early_read || after_prefix) griddep_wait();
       if (writer_cta && threadIdx.x == 0 && __ldg(p.slot_mapping + b) >= 0)
         raise_error(p.err, PA_DEVERR_SLOT);  // a new token for an empty sequence
       if (p.counters != nullptr && nblk == 0 && part == 0) {
@@ -620,9 +644,9 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   for (int i = consumed; i < issued; ++i) mbar_wait_bounded(&bars[i % S], (i / S) & 1, p.err);
 
   // partitions of this sequence that have a CTA (split-K)
-  const int nparts = SPLIT ? min((nblk + p.partition_blocks - 1) / p.partition_blocks,
-                                 p.max_partitions)
-                           : 1;
+  const int nparts = SPLIT ? min(parts_of(nblk), p.max_partitions) : 1;
+  // of which this launch computes (the rest: a shared prefix's)
+  const int nparts_here = nparts - (after_prefix ? p.first_partition : 0);
   // In-kernel split-K merge: count this CTA in now (the count's round trip
   // overlaps the merge of the warps below).  Counter word: arrivals in the
   // low 16 bits, partitions published in the high 16 bits.
@@ -773,7 +797,10 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
   }
 
   if constexpr (SPLIT) {
-    if (!merging) return;
+    if (!merging) {
+      if (after_prefix) griddep_wait();
+      return;
+    }
     // Every CTA but the last to arrive publishes its rows (a release on the
     // counter) and leaves; the last waits until all the others have
     // published -- they arrived before it, so they are running and finish
@@ -783,7 +810,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
     __shared__ unsigned s_last;
     __syncthreads();  // every thread's workspace rows are written
     if (threadIdx.x == 0) {
-      if ((arrival & 0xFFFFu) + 1u != static_cast<unsigned>(nparts)) {
+      if ((arrival & 0xFFFFu) + 1u != static_cast<unsigned>(nparts_here)) {
         asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(cnt), "r"(0x10000u)
                      : "memory");
         s_last = 0u;
@@ -793,7 +820,7 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
         for (;;) {
           unsigned v;
           asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-          if ((v >> 16) + 1u >= static_cast<unsigned>(nparts)) break;
+          if ((v >> 16) + 1u >= static_cast<unsigned>(nparts_here)) break;
           if (global_timer_ns() - t0 > 2000000000ull) {
             raise_error(p.err, PA_DEVERR_WAIT_TIMEOUT);
             ok = false;
@@ -805,33 +832,48 @@ __global__ void __launch_bounds__(NW * 32, (min_blocks<NW, G, Q>()))
       }
     }
     __syncthreads();
+    if (after_prefix) griddep_wait();  // the prefix's partitions are written
     if (!s_last) return;
     for (int idx = threadIdx.x; idx < G * (D / 4); idx += NW * 32) {
       const int hq = kvh * G + idx / (D / 4);
       const int d0 = (idx % (D / 4)) * 4;
       const size_t row0 = (static_cast<size_t>(b) * p.num_q_heads + hq) * p.max_partitions;
-      // one pass, rescaling to the running maximum (natural-log units)
+      // one pass, rescaling to the running maximum (natural-log units); the
+      // rows of up to MU partitions are loaded together (one round trip)
+      constexpr int MU = 8;
       float M = -INFINITY, Ls = 0.f;
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int i = 0; i < nparts; ++i) {
-        const float m = __ldcg(p.ws_m + row0 + i);
-        const float l = __ldcg(p.ws_l + row0 + i);
-        const float4 o = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (row0 + i) * D + d0));
-        if (m > M) {
-          const float c = expf(M - m);  // 0 on the first partition
-          Ls *= c;
-          a.x *= c;
-          a.y *= c;
-          a.z *= c;
-          a.w *= c;
-          M = m;
+      for (int i0 = 0; i0 < nparts; i0 += MU) {
+        float mv[MU], lv[MU];
+        float4 ov[MU];
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+          if (i0 + u < nparts) {
+            mv[u] = __ldcg(p.ws_m + row0 + i0 + u);
+            lv[u] = __ldcg(p.ws_l + row0 + i0 + u);
+            ov[u] = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (row0 + i0 + u) * D + d0));
+          }
         }
-        const float w = l * expf(m - M);
-        Ls += w;
-        a.x += w * o.x;
-        a.y += w * o.y;
-        a.z += w * o.z;
-        a.w += w * o.w;
+#pragma unroll
+        for (int u = 0; u < MU; ++u) {
+          if (i0 + u >= nparts) break;
+          const float m = mv[u];
+          if (m > M) {
+            const float c = expf(M - m);  // 0 on the first partition
+            Ls *= c;
+            a.x *= c;
+            a.y *= c;
+            a.z *= c;
+            a.w *= c;
+            M = m;
+          }
+          const float w = lv[u] * expf(m - M);
+          Ls += w;
+          a.x += w * ov[u].x;
+          a.y += w * ov[u].y;
+          a.z += w * ov[u].z;
+          a.w += w * ov[u].w;
+        }
       }
       const float inv = 1.0f / Ls;  // every partition has a token: Ls >= 1
       const __nv_bfloat162 h0 = __float22bfloat162_rn(make_float2(a.x * inv, a.y * inv));
@@ -869,9 +911,11 @@ cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   auto kernel = paged_decode_kernel<D, G, NW, S, SPLIT, Q>;
   cudaError_t e = allow_smem(kernel, Lay::TOTAL, smem_set);
   if (e != cudaSuccess) return e;
-  const dim3 grid = (SPLIT && p.order != nullptr)
-                        ? dim3(p.num_kv_heads, p.num_seqs * p.max_partitions, 1)
-                        : dim3(p.num_kv_heads, p.num_seqs, SPLIT ? p.max_partitions : 1);
+  const dim3 grid =
+      (SPLIT && p.order != nullptr)
+          ? dim3(p.num_kv_heads, p.num_seqs * (p.max_partitions - p.first_partition), 1)
+                        : dim3(p.num_kv_heads, p.num_seqs,
+                               SPLIT ? p.max_partitions - p.first_partition : 1);
   return launch_pdl(kernel, grid, dim3(NW * 32), Lay::TOTAL, stream, p);
 }
 

@@ -49,6 +49,12 @@ struct DecodeParams {
   // Tables, lengths, order and pools are not written by the preceding kernel:
   // they may be read before waiting for it (programmatic dependent launch).
   int early_read;
+  // split-K: partitions below first_partition are not computed here (a
+  // shared prefix's prefix_blocks blocks, computed by launch_prefix_partials,
+  // which also checks that every sequence holds them); the others hold
+  // partition_blocks blocks each from block prefix_blocks on.
+  int first_partition;
+  int prefix_blocks;
 };
 
 struct ReduceParams {
@@ -101,6 +107,17 @@ bool decode_shape_supported(int head_dim, int group, int block_size);
 cudaError_t launch_decode(const DecodeParams& p, int head_dim, int group, bool split,
                           cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams& p, int head_dim, cudaStream_t stream);
+// prefill.cu: the split-K partials of a decode batch's queries over a shared
+// prefix, partitions [0, splits) of split_blocks blocks each (head_dim 128);
+// sets PA_DEVERR_PREFIX for a sequence not holding the prefix's blocks or not
+// going past them.
+cudaError_t launch_prefix_partials(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int num_blocks, float scale,
+                                   int split_blocks, int splits, float* ws_o, float* ws_m,
+                                   float* ws_l, int max_partitions, unsigned* err,
+                                   cudaStream_t stream);
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, cudaStream_t stream);
 cudaError_t launch_reshape_and_cache_int8(const CacheWriteParams& p, cudaStream_t stream);
 cudaError_t launch_copy_blocks(const CopyBlocksParams& p, int num_pairs, int num_layers,

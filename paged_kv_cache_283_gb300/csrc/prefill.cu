@@ -100,6 +100,17 @@ struct PrefillParams {
   int num_blocks;
   int total_q;
   float scale_log2;
+  // Shared-prefix mode (split_blocks > 0): one virtual sequence whose
+  // "tokens" are a decode batch's queries (q [total_q = B, Hq, D]), each row
+  // (query b, head) attending, without a causal mask, to the keys of blocks
+  // [s * split_blocks, (s + 1) * split_blocks) of block-table row 0 (s =
+  // blockIdx.z), and its partial result going to a split-K workspace [B, Hq,
+  // max_partitions] at partition s: o / l, m (natural-log units) and l.
+  int split_blocks;
+  float* ws_o;
+  float* ws_m;
+  float* ws_l;
+  int max_partitions;
 };
 
 // ---- tcgen05 / TMA wrappers -------------------------------------------------
@@ -266,20 +277,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   constexpr int kMmaWarp = kSoftmaxThreads / 32, kCopyWarp = kMmaWarp + 1;
   griddep_wait();
   griddep_launch_dependents();
-  const int tile = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const bool shared_prefix = p.split_blocks > 0;  // CTA-uniform
+  const int tile = blockIdx.x, kvh = blockIdx.y, b = shared_prefix ? 0 : blockIdx.z;
+  const int split = shared_prefix ? blockIdx.z : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // Lengths live in device memory: check them (CTA-uniform).
-  const int q0 = __ldg(p.query_start + b), q1 = __ldg(p.query_start + b + 1);
-  const int ctx = __ldg(p.context_lens + b);
+  // Lengths live in device memory: check them (CTA-uniform).  A shared
+  // prefix split: every query sees the split's keys (sizes checked on the host).
+  const int q0 = shared_prefix ? 0 : __ldg(p.query_start + b);
+  const int q1 = shared_prefix ? p.total_q : __ldg(p.query_start + b + 1);
+  const int ctx = shared_prefix ? p.split_blocks * kBS : __ldg(p.context_lens + b);
   const int n = q1 - q0;
-  if (q0 < 0 || q1 > p.total_q || n < 0 || n > ctx || ctx > p.max_blocks_per_seq * kBS) {
+  if (!shared_prefix &&
+      (q0 < 0 || q1 > p.total_q || n < 0 || n > ctx || ctx > p.max_blocks_per_seq * kBS)) {
     if (tid == 0 && tile == 0 && kvh == 0) raise_error(p.err, PA_DEVERR_CONTEXT_LEN);
     return;
   }
   const int i0 = tile * TQ;
   if (i0 >= n) return;
-  const int nk = ctx - n + min(n, i0 + TQ);  // keys the tile's last query sees
+  // keys the tile's last query sees
+  const int nk = shared_prefix ? ctx : ctx - n + min(n, i0 + TQ);
   const int nchunks = (nk + kKeys - 1) / kKeys;
   const int nblk_all = (nk + kBS - 1) / kBS;
 
@@ -329,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // a 32 KiB chunk is 16 tensor-map boxes whose issue takes ~1.6k cycles,
     // so one warp issuing both rings paced the whole pipeline.
     const bool vwarp = warp == kCopyWarp + 1;
-    const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    const int32_t* tbl = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq +
+                         static_cast<size_t>(split) * p.split_blocks;
     int last_k = -1, last_v = -1;  // last chunk copied into each ring (for the drain)
     bool ok = true;                // lane 0: every wait so far succeeded
     auto uniform = [&](bool v) { return __shfl_sync(kFullMask, v ? 1 : 0, 0) != 0; };
@@ -398,6 +416,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
       for (int i = 0; i + 1 < kIdAhead; ++i) idq[i] = idq[i + 1];
       idq[kIdAhead - 1] = fetch_id(next + kIdAhead);
+    }
+    // A shared prefix: the V warp of each KV head 0 CTA checks that its
+    // tile's sequences hold this split's blocks (the same table entries as
+    // sequence 0) and, in the first split, that their contexts go past the
+    // prefix.
+    if (shared_prefix && vwarp && kvh == 0) {
+      const int32_t* row0 = p.block_tables + static_cast<size_t>(split) * p.split_blocks;
+      const int prefix_tokens = p.split_blocks * kBS * static_cast<int>(gridDim.z);
+      const int seqs = min(TQ, n - i0);
+      const int pairs = seqs * p.split_blocks;  // (sequence, block) pairs, spread over the lanes
+      bool bad = false;
+#pragma unroll 4
+      for (int e = lane; e < pairs; e += 32) {
+        const int t = e / p.split_blocks, j = e - t * p.split_blocks;
+        bad |= __ldg(row0 + static_cast<size_t>(i0 + t) * p.max_blocks_per_seq + j) !=
+               __ldg(row0 + j);
+      }
+      if (split == 0)
+        for (int t = lane; t < seqs; t += 32) bad |= __ldg(p.context_lens + i0 + t) <= prefix_tokens;
+      if (__any_sync(kFullMask, bad) && lane == 0) raise_error(p.err, PA_DEVERR_PREFIX);
     }
     // Copies this warp issued land before the CTA's shared memory is given up
     // (earlier uses of a stage completed before its last copy was issued).
@@ -482,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int r = tid & (kRows - 1);  // row: token r / G of the tile, head r % G
     const int qi = i0 + r / G;
     const bool row_ok = qi < n;
-    const int pos = ctx - n + qi;
+    const int pos = shared_prefix ? nk - 1 : ctx - n + qi;  // sees keys 0 .. pos
     const float sl2 = p.scale_log2;
     float m_used = -INFINITY;  // reference maximum of the exponentials (base 2)
     float l_sum = 0.f;
@@ -628,7 +666,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     lok = __all_sync(kFullMask, lok);
     red[hcol * kRows + r] = l_sum;
     asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
-    if (lok) {
+    if (lok && shared_prefix) {
+      // the row's partial: o / l, and (m, l) with m in natural-log units
+      tc_fence_after();
+      const float lt = red[r] + red[kRows + r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const size_t wrow =
+          (static_cast<size_t>(row_ok ? qi : 0) * p.num_q_heads + kvh * G + r % G) *
+              p.max_partitions + split;
+      float* orow = p.ws_o + wrow * kD + 64 * hcol;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t o[16];
+        tmem_ld16(tO + 16 * q4, o);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float4*>(orow + 16 * q4 + 4 * k) = make_float4(
+                __uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
+                __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+        }
+      }
+      if (row_ok && hcol == 0) {
+        p.ws_m[wrow] = m_used * 0.6931471805599453f;
+        p.ws_l[wrow] = lt;
+      }
+    } else if (lok) {
       tc_fence_after();
       const float lt = red[r] + red[kRows + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
@@ -740,6 +804,45 @@ cudaError_t launch_prefill_g(const CUtensorMap& tq, const CUtensorMap& tk, const
 bool aligned16(const void* ptr) { return ptr && (reinterpret_cast<uintptr_t>(ptr) & 15) == 0; }
 
 }  // namespace
+
+// The shared-prefix partials of a decode batch (see PrefillParams): grid
+// (query tiles, KV heads, splits).  Arguments checked by the caller.
+cudaError_t launch_prefix_partials(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int max_blocks_per_seq,
+                                   const int32_t* context_lens, int num_seqs, int num_q_heads,
+                                   int num_kv_heads, int num_blocks, float scale,
+                                   int split_blocks, int splits, float* ws_o, float* ws_m,
+                                   float* ws_l, int max_partitions, unsigned* err,
+                                   cudaStream_t stream) {
+  const int group = num_q_heads / num_kv_heads;
+  const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * kBS;
+  CUtensorMap tq, tk, tv;
+  if (!encode_q_map(&tq, q, num_seqs, num_q_heads, group) ||
+      !encode_pool_map(&tk, k_cache, rows) || !encode_pool_map(&tv, v_cache, rows))
+    return cudaErrorInvalidValue;
+  PrefillParams p{};
+  p.block_tables = block_tables;
+  p.err = err;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.num_blocks = num_blocks;
+  p.total_q = num_seqs;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.split_blocks = split_blocks;
+  p.ws_o = ws_o;
+  p.ws_m = ws_m;
+  p.ws_l = ws_l;
+  p.max_partitions = max_partitions;
+  p.context_lens = context_lens;
+  switch (group) {
+    case 1: return launch_prefill_g<1>(tq, tk, tv, p, num_seqs, splits, stream);
+    case 2: return launch_prefill_g<2>(tq, tk, tv, p, num_seqs, splits, stream);
+    case 4: return launch_prefill_g<4>(tq, tk, tv, p, num_seqs, splits, stream);
+    default: return launch_prefill_g<8>(tq, tk, tv, p, num_seqs, splits, stream);
+  }
+}
+
 }  // namespace pa
 
 extern "C" int pa_prefill_supported(int head_dim, int group, int block_size) {

@@ -26,6 +26,7 @@ PA_DEVERR_CONTEXT_LEN = 0x2
 PA_DEVERR_SLOT = 0x4
 PA_DEVERR_WAIT_TIMEOUT = 0x8
 PA_DEVERR_ORDER = 0x10
+PA_DEVERR_PREFIX = 0x20
 PA_STEP_EARLY_READ = 0x1
 
 # Every function include/pa.h declares: name -> (restype, argtypes).
@@ -59,6 +60,9 @@ SIGNATURES = {
     "pa_splitk_reduce": (_i, [_vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _vp]),
     "pa_splitk_partition_size": (_i, [_vp, _i, _i, _i, _i, _i, _i, _i]),
     "pa_splitk_order": (_i, [_vp, _i, _i, _i, _vp]),
+    "pa_decode_step_shared_prefix": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
+                                          _i, _i, _i, _i, _i, _f, _i, _i, _i, _vp, _vp, _vp,
+                                          _vp, _i, _vp, _vp]),
     "pa_decode_step": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i, _i, _i, _i, _i,
                             _i, _f, _i, _vp, _vp, _vp, _vp, _i, _vp, _i, _vp]),
     "pa_decode_step_int8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp, _i,
@@ -529,6 +533,109 @@ def pa_decode_step(out, q, k_cache, v_cache, block_tables, context_lens, scale, 
                           value, slot_mapping, partition_size, workspace, counters, k_scales,
                           v_scales, order, early_read)
     _check(fn(*args, _stream(stream)), "pa_decode_step")
+
+
+def shared_prefix_partitions(max_context_len, prefix_len, prefix_split, partition_size):
+    """Workspace partitions a pa_decode_step_shared_prefix call needs for
+    contexts of up to max_context_len tokens: the prefix's, then the rest's."""
+    rest = max(1, int(max_context_len) - int(prefix_len))
+    return int(prefix_len) // int(prefix_split) + -(-rest // int(partition_size))
+
+
+def shared_prefix_workspace(num_seqs, num_q_heads, head_dim, max_context_len, prefix_len,
+                            prefix_split, partition_size, device=None):
+    """(ws_out, ws_m, ws_l) for pa_decode_step_shared_prefix."""
+    torch = _torch()
+    device = device or torch.device("cuda")
+    p = shared_prefix_partitions(max_context_len, prefix_len, prefix_split, partition_size)
+    return (torch.empty(num_seqs, num_q_heads, p, head_dim, dtype=torch.float32, device=device),
+            torch.empty(num_seqs, num_q_heads, p, dtype=torch.float32, device=device),
+            torch.empty(num_seqs, num_q_heads, p, dtype=torch.float32, device=device))
+
+
+def _shared_prefix_args(out, q, k_cache, v_cache, block_tables, context_lens, scale, prefix_len,
+                        prefix_split, partition_size, workspace, counters, key, value,
+                        slot_mapping, order):
+    """Checked and marshalled arguments of pa_decode_step_shared_prefix
+    (without the stream)."""
+    torch = _torch()
+    (pq, pk, pv, pt, pc), (B, hq, hkv, d, bs, nb, mb) = _decode_common(
+        q, k_cache, v_cache, block_tables, context_lens)
+    if out.shape != q.shape:
+        raise ValueError("pa_decode_step_shared_prefix: out must match q")
+    none = ctypes.c_void_p(None)
+    if key is None and value is None and slot_mapping is None:
+        kvs = (none, none, none)
+    elif key is None or value is None or slot_mapping is None:
+        raise ValueError("pa_decode_step_shared_prefix: key, value and slot_mapping go together")
+    else:
+        if key.shape != (B, hkv, d) or value.shape != key.shape or slot_mapping.shape != (B,):
+            raise ValueError("pa_decode_step_shared_prefix: key / value [B, Hkv, D], "
+                             "slot_mapping [B]")
+        kvs = (_dev(key, torch.bfloat16, "key", 3), _dev(value, torch.bfloat16, "value", 3),
+               _dev(slot_mapping, torch.int64, "slot_mapping", 1))
+    ws_o, ws_m, ws_l = workspace
+    maxp = ws_m.shape[2]
+    if ws_o.shape != (B, hq, maxp, d) or ws_l.shape != ws_m.shape or ws_m.shape[:2] != (B, hq) \
+            or counters.shape != (B * hkv,):
+        raise ValueError("pa_decode_step_shared_prefix: workspace / counters shapes")
+    return (_dev(out, torch.bfloat16, "out", 3), pq) + kvs + (
+        pk, pv, pt, mb, pc, B, hq, hkv, d, bs, nb, float(scale), int(prefix_len),
+        int(prefix_split), int(partition_size), _dev(ws_o, torch.float32, "ws_out", 4),
+        _dev(ws_m, torch.float32, "ws_m", 3), _dev(ws_l, torch.float32, "ws_l", 3),
+        _dev(counters, torch.int32, "counters", 1), maxp,
+        none if order is None else _dev(order, torch.int32, "order", 1))
+
+
+def pa_decode_step_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                 prefix_len, prefix_split, partition_size, workspace, counters,
+                                 key=None, value=None, slot_mapping=None, stream=None,
+                                 order=None):
+    """pa_decode_step for a batch whose sequences all hold the same first
+    prefix_len tokens (the same blocks as sequence 0) and go past them: the
+    prefix in partitions of prefix_split tokens, each one tensor-core launch
+    pass over the whole batch, and the rest by the split-K decode with the
+    cache write (partitions of partition_size tokens from the prefix's end),
+    merged in its last CTAs.  bf16 cache; workspace =
+    shared_prefix_workspace(...); counters = step_counters(...); order
+    (optional): shared_prefix_order(...) on the device."""
+    args = _shared_prefix_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                               prefix_len, prefix_split, partition_size, workspace, counters, key,
+                               value, slot_mapping, order)
+    _check(lib().pa_decode_step_shared_prefix(*args, _stream(stream)),
+           "pa_decode_step_shared_prefix")
+
+
+class SharedPrefixStep:
+    """One shared-prefix decode step of one layer on fixed device buffers
+    (pa_decode_step_shared_prefix), its arguments checked and marshalled
+    once; each call is one bare C call.  The buffers' contents may change
+    between calls, their shapes and addresses may not."""
+
+    def __init__(self, out, q, k_cache, v_cache, block_tables, context_lens, scale, prefix_len,
+                 prefix_split, partition_size, workspace, counters, key=None, value=None,
+                 slot_mapping=None, order=None, stream=None):
+        self._args = _shared_prefix_args(out, q, k_cache, v_cache, block_tables, context_lens,
+                                         scale, prefix_len, prefix_split, partition_size,
+                                         workspace, counters, key, value, slot_mapping, order)
+        self._stream = None if stream is None else ctypes.c_void_p(stream.cuda_stream)
+        self._keep = [out, q, k_cache, v_cache, block_tables, context_lens, workspace, counters,
+                      key, value, slot_mapping, order]
+
+    def __call__(self):
+        _check(lib().pa_decode_step_shared_prefix(*self._args, self._stream),
+               "pa_decode_step_shared_prefix")
+
+
+def shared_prefix_order(context_lens, prefix_len, partition_size, max_partitions,
+                        prefix_split):
+    """Longest-first work order (host numpy int32) of a shared-prefix step's
+    second launch: pa_splitk_order of the lengths past the prefix over the
+    partitions past the prefix's."""
+    import numpy as np
+    rest = np.maximum(np.asarray(context_lens, dtype=np.int64) - int(prefix_len), 0)
+    return splitk_order(rest.astype(np.int32), partition_size,
+                        int(max_partitions) - int(prefix_len) // int(prefix_split))
 
 
 def pa_reshape_and_cache_fp8(key, value, k_cache, v_cache, k_scales, v_scales, slot_mapping,

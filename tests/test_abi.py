@@ -129,3 +129,26 @@ def test_decode_step_host_checks(lib):
     assert call(order=f, partition=0) == pa.PA_ERR_INVALID_ARG  # an order needs split-K
     assert call(order=f, num_seqs=300, maxp=300) == pa.PA_ERR_UNSUPPORTED_SHAPE
     assert call(num_seqs=0, out=None) == pa.PA_OK               # nothing to do
+
+
+def test_shared_prefix_step_host_checks(lib):
+    # pa_decode_step_shared_prefix's own checks; each call fails one of them
+    # before any CUDA call (fake addresses never reach a kernel)
+    f = ctypes.c_void_p(0x10000)
+
+    def call(prefix=512, split=256, part=256, maxp=4, d=128, hkv=8, seqs=2, out=f, counters=f):
+        return lib.pa_decode_step_shared_prefix(out, f, None, None, None, f, f, f, 64, f, seqs, 32,
+                                                hkv, d, 16, 100, 0.1, prefix, split, part, f, f,
+                                                f, counters, maxp, None, None)
+
+    assert call(prefix=0) == pa.PA_ERR_INVALID_ARG
+    assert call(prefix=300) == pa.PA_ERR_INVALID_ARG        # not a multiple of the split
+    assert call(split=100) == pa.PA_ERR_INVALID_ARG         # not a multiple of the block
+    assert call(part=100) == pa.PA_ERR_INVALID_ARG
+    assert call(maxp=2) == pa.PA_ERR_INVALID_ARG            # no partition left past the prefix
+    assert call(counters=None) == pa.PA_ERR_INVALID_ARG     # the merge needs counters
+    assert call(prefix=2048) == pa.PA_ERR_INVALID_ARG       # longer than the tables
+    assert call(d=64) == pa.PA_ERR_UNSUPPORTED_SHAPE        # the prefill kernel's shapes only
+    assert call(hkv=2) == pa.PA_ERR_UNSUPPORTED_SHAPE       # group of 16
+    assert call(out=None) == pa.PA_ERR_INVALID_ARG
+    assert call(seqs=0) == pa.PA_OK
