@@ -756,7 +756,9 @@ def run_gpu(args):
                 "peak": hbm_peak if hbm_peak else 6800.0, "unit": "GB/s",
                 "frac": round(achieved / (hbm_peak if hbm_peak else 6800.0), 4),
                 "traffic": args.traffic if args.traffic is not None else recorded_traffic(
-                    kkey, w.name, args.partition),
+                    kkey, w.name, args.partition,
+                    ("decode.cu", "decode_tile.cuh", "prefill.cu") if lp["shared_prefix"]
+                    else ("decode.cu", "decode_tile.cuh")),
                 "kernel": kname,
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_peak
                 else "fallback 6.8 TB/s",
@@ -1197,6 +1199,7 @@ def run_prefill(args):
 
 
 def main(argv=None):
+    global SHARED_PREFIX_SPLIT
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
@@ -1219,6 +1222,9 @@ def main(argv=None):
     ap.add_argument("--order", default="longest", choices=["longest", "grid"],
                     help="fused split-K: CTAs handed out longest first (pa_splitk_order) "
                          "or in grid order")
+    ap.add_argument("--prefix-split", type=int, default=None,
+                    help="--step shared-prefix: tokens per tensor-core prefix partition "
+                         "(default %d)" % SHARED_PREFIX_SPLIT)
     ap.add_argument("--step", default="fused", choices=["fused", "separate", "shared-prefix"],
                     help="fused: one pa_decode_step launch per layer (cache write + attention "
                          "+ split-K merge); separate: the cache write, partition pass and "
@@ -1244,6 +1250,8 @@ def main(argv=None):
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.prefix_split:
+        SHARED_PREFIX_SPLIT = args.prefix_split
     if args.impl == "reference":
         return run_reference(args)
     if args.op == "copy_blocks":
