@@ -626,6 +626,12 @@ class SharedPrefixStep:
         _check(lib().pa_decode_step_shared_prefix(*self._args, self._stream),
                "pa_decode_step_shared_prefix")
 
+    def recover(self):
+        """After a launch that raised PA_DEVERR_ORDER or PA_DEVERR_WAIT_TIMEOUT:
+        re-zeroes this step's arrival counters and clears the error word
+        (recover_step_counters).  Returns the error bits found."""
+        return recover_step_counters(self._keep[7])
+
 
 def shared_prefix_order(context_lens, prefix_len, partition_size, max_partitions,
                         prefix_split):
