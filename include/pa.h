@@ -496,8 +496,8 @@ pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* 
 
 /*
  * Split-K partition size for a decode batch (host): the size, from {256, 384,
- * 512, 640, 768, 1024, 1536, 2048, 4096} tokens, that minimises a model of the
- * split-K launch's time -- its CTAs handed in grid order to the first free
+ * 512, 640, 768, 1024, 1280, 1536, 1792, 2048, 4096} tokens, that minimises a
+ * model of the split-K launch's time -- its CTAs handed in grid order to the first free
  * CTA slot (num_sms x the kernel's CTAs per SM), each costing a time per
  * token, a fixed start-up and, for sequences of several partitions, a merge
  * share -- with ties going to the larger size; in grid order a 1-byte cache

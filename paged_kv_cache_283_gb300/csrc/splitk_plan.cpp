@@ -16,7 +16,10 @@
 // launch (kApartUs).  The constants were fitted to pa_decode_step timings of
 // the Llama-3.1-8B-shaped batch-64 and 32-layer batch-256 steps on a GB300
 // (bf16 cache), once for each dispatch order: grid order at partition 384 ..
-// 1536, longest first (pa_splitk_order) at 768 .. 2048.  The 1-byte kernels are issue-bound:
+// 1536, longest first (pa_splitk_order) at 768 .. 2048 (refitted to 7 µs a
+// CTA once 1280 and 1792 were candidates: batch 64 measured 47.3-47.6 µs at
+// 1280, 47.9-48.3 at 1536, 51.0 at 1792, 53.2-53.4 at 1024 and 2048, and the
+// model now picks 1280 there).  The 1-byte kernels are issue-bound:
 // a CTA that runs with fewer neighbours on its SM does not get much faster,
 // which the grid-order model (fixed CTA durations) gets right only once the
 // batch has a CTA for every slot without splitting; with fewer (sequence, KV
@@ -43,10 +46,10 @@ struct Costs {
   double merge;
 };
 constexpr Costs kGridCosts = {0.025, 0.019, 4.0, 2.0};
-constexpr Costs kOrderedCosts = {0.022, 0.0167, 8.0, 3.0};
+constexpr Costs kOrderedCosts = {0.022, 0.0167, 7.0, 3.0};
 constexpr double kApartUs = 3.0;
 constexpr int kMergeInKernelParts = 16;  // as pa_decode_step
-constexpr int kCandidates[] = {256, 384, 512, 640, 768, 1024, 1536, 2048, 4096};
+constexpr int kCandidates[] = {256, 384, 512, 640, 768, 1024, 1280, 1536, 1792, 2048, 4096};
 
 // CTAs per SM of the split-K kernels (their __launch_bounds__ minimum).
 int ctas_per_sm(int group, int kv_kind) {

@@ -12,9 +12,9 @@ import pytest
 
 from paged_kv_cache_283_gb300 import pa
 
-CANDIDATES = (256, 384, 512, 640, 768, 1024, 1536, 2048, 4096)
+CANDIDATES = (256, 384, 512, 640, 768, 1024, 1280, 1536, 1792, 2048, 4096)
 # (token µs for bf16, for 1-byte caches, per-CTA µs, merge µs) per dispatch order
-COSTS = {False: (0.025, 0.019, 4.0, 2.0), True: (0.022, 0.0167, 8.0, 3.0)}
+COSTS = {False: (0.025, 0.019, 4.0, 2.0), True: (0.022, 0.0167, 7.0, 3.0)}
 APART_US, IN_KERNEL_PARTS = 3.0, 16
 
 
