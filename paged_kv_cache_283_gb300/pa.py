@@ -593,10 +593,10 @@ def pa_decode_step_shared_prefix(out, q, k_cache, v_cache, block_tables, context
                                  order=None):
     """pa_decode_step for a batch whose sequences all hold the same first
     prefix_len tokens (the same blocks as sequence 0) and go past them: the
-    prefix in partitions of prefix_split tokens, each one tensor-core launch
-    pass over the whole batch, and the rest by the split-K decode with the
-    cache write (partitions of partition_size tokens from the prefix's end),
-    merged in its last CTAs.  bf16 cache; workspace =
+    prefix in partitions of prefix_split tokens, the whole batch's queries
+    against each on the tensor cores (one launch for all of them), and the
+    rest by the split-K decode with the cache write (partitions of
+    partition_size tokens from the prefix's end), merged in its last CTAs.  bf16 cache; workspace =
     shared_prefix_workspace(...); counters = step_counters(...); order
     (optional): shared_prefix_order(...) on the device."""
     args = _shared_prefix_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
