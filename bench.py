@@ -273,8 +273,9 @@ def run_reference(args):
         env.pop("RANK", None)
         env.pop("WORLD_SIZE", None)
         r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                            "--steps", str(args.steps), "--warmup", str(args.warmup),
-                            "--workload", str(args.workload)], env=env, cwd=ROOT)
+                            "--gpus", str(args.gpus), "--steps", str(args.steps),
+                            "--warmup", str(args.warmup), "--workload", str(args.workload)],
+                           env=env, cwd=ROOT)
         return r.returncode
     # one oracle sample per step, sized so that warmup + steps stay within ~2 minutes
     probe = oracle_step_sample(args.workload, 0.0, out_json=False)
@@ -323,11 +324,22 @@ def _reference_timed(args, nseq):
                                                                         w.head_dim)
     value = nbytes * args.steps / dt / 1e9
     threads = os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
-    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
-            "steps": args.steps, "warmup": args.warmup,
+    # the GPU arm's workload keys; the oracle runs one layer of it on the host
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample_seqs": nseq, "batch": w.num_seqs},
+            "config": {"workload": w.name, "batch": w.num_seqs, "layers": 1,
+                       "q_heads": w.num_q_heads, "kv_heads": w.num_kv_heads,
+                       "head_dim": w.head_dim, "block_size": w.block_size,
+                       "num_blocks": w.num_blocks,
+                       "mean_context": float(np.mean(w.context_lens)),
+                       "new_tokens_per_step": w.num_seqs, "kv_cache": "bf16",
+                       "attention": "float64 oracle on one host thread: "
+                                    "oracle.cache.reshape_and_cache + "
+                                    "oracle.attention.decode_sequence per sequence",
+                       "sample_seqs": nseq,
+                       "parallelism": "rank 0 only, host cores (no GPU)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                              "cores": int(threads) if threads.isdigit() else threads,
                              "sample": f"first {nseq} of {w.num_seqs} sequences per step"},

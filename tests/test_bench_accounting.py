@@ -68,3 +68,20 @@ def test_unique_decode_bytes_shared_prefix():
     # every other workload has nothing shared
     w2 = I.llama8b_batch64(with_data=False)
     assert bench.unique_decode_bytes(w2) == bench.decode_bytes(w2.context_lens, 64, 32, 8, 128, 16)
+
+
+def test_reference_arm_line_matches_the_gpu_arm_keys():
+    # the reference arm (the float64 oracle on the host) prints the GPU arm's
+    # metric, unit, direction and workload keys; timed here on the tiny workload
+    import argparse
+    args = argparse.Namespace(workload=1, steps=1, warmup=0, gpus=1)
+    line = bench._reference_timed(args, 2)
+    assert line["impl"] == "reference"
+    assert (line["metric"], line["unit"], line["higher_is_better"]) == \
+        (bench.METRIC, bench.UNIT, True)
+    assert line["n_gpus"] == 1 and line["value"] > 0
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["value"] == line["value"]
+    for key in ("workload", "batch", "layers", "q_heads", "kv_heads", "head_dim", "block_size",
+                "num_blocks", "mean_context", "new_tokens_per_step", "kv_cache"):
+        assert key in line["config"], key
+    assert line["config"]["batch"] == 2 and line["config"]["sample_seqs"] == 2
