@@ -447,7 +447,8 @@ pa_status pa_decode_step_fp8(void* out, const void* q, const void* key, const vo
  *     partitions past the prefix (pa_splitk_order of the lengths past the
  *     prefix gives the longest first); as pa_decode_step's order otherwise.
  *   bf16 cache, head_dim and group supported by both pa_decode_supported
- *     and pa_prefill_supported (else PA_ERR_UNSUPPORTED_SHAPE); other
+ *     and pa_prefill_supported (else PA_ERR_UNSUPPORTED_SHAPE); scale > 0,
+ *     as pa_prefill's (else PA_ERR_INVALID_ARG); other
  *     arguments as pa_decode_step (key / value / slot_mapping all NULL:
  *     attention only).
  * Asynchronous on `stream`.
@@ -484,7 +485,9 @@ pa_status pa_decode_step_shared_prefix(void* out, const void* q, const void* key
  * {1, 2, 4, 8} (else PA_ERR_UNSUPPORTED_SHAPE); num_seqs <= 65535.  Device-side
  * checks: 0 <= n_b <= ctx_b <= max_blocks_per_seq * 16 and rows within T (else
  * PA_DEVERR_CONTEXT_LEN and the sequence is skipped); bad block ids as
- * pa_decode.  Pointers 16-byte aligned.  Async on `stream`.
+ * pa_decode.  Pointers 16-byte aligned.  scale > 0 (the kernel takes row
+ * maxima of the unscaled scores; else PA_ERR_INVALID_ARG).  Async on
+ * `stream`.
  */
 int pa_prefill_supported(int head_dim, int group, int block_size);
 pa_status pa_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,

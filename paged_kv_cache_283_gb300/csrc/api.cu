@@ -583,7 +583,10 @@ pa_status pa_decode_step_shared_prefix(void* out, const void* q, const void* key
                                   context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
                                   block_size, num_blocks, scale);
   if (s != PA_OK) return s;
-  if (prefix_split <= 0 || prefix_split % block_size != 0 || prefix_len <= 0 ||
+  // the prefix launch (the prefill kernel) takes row maxima of unscaled
+  // scores: a positive scale only, as pa_prefill
+  if (!(scale > 0.f) || prefix_split <= 0 ||
+      prefix_split % block_size != 0 || prefix_len <= 0 ||
       prefix_len % prefix_split != 0 || prefix_len / block_size > max_blocks_per_seq ||
       partition_size <= 0 || partition_size % block_size != 0 ||
       max_partitions <= prefix_len / prefix_split || max_partitions > 65535)

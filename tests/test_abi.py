@@ -94,6 +94,14 @@ def test_host_checks_reject_before_any_launch(lib):
     assert st == pa.PA_ERR_INVALID_ARG               # partition not a multiple of 16
     st = lib.pa_splitk_reduce(fake, fake, fake, fake, 4, fake, 2, 32, 96, 512, None)
     assert st == pa.PA_ERR_UNSUPPORTED_SHAPE
+    # pa_prefill: the kernel takes row maxima of unscaled scores, so scale > 0
+    for scale in (0.0, -0.1, float("nan")):
+        st = lib.pa_prefill(fake, fake, fake, fake, fake, 4, fake, fake, 8, 2, 16, 32, 8, 128,
+                            16, 10, scale, None)
+        assert st == pa.PA_ERR_INVALID_ARG
+    st = lib.pa_prefill(fake, fake, fake, fake, fake, 4, fake, fake, 8, 2, 16, 32, 8, 64, 16,
+                        10, 0.1, None)
+    assert st == pa.PA_ERR_UNSUPPORTED_SHAPE         # head_dim 128 only
 
 
 def test_workspace_bytes(lib):
@@ -136,12 +144,15 @@ def test_shared_prefix_step_host_checks(lib):
     # before any CUDA call (fake addresses never reach a kernel)
     f = ctypes.c_void_p(0x10000)
 
-    def call(prefix=512, split=256, part=256, maxp=4, d=128, hkv=8, seqs=2, out=f, counters=f):
+    def call(prefix=512, split=256, part=256, maxp=4, d=128, hkv=8, seqs=2, out=f, counters=f,
+             scale=0.1):
         return lib.pa_decode_step_shared_prefix(out, f, None, None, None, f, f, f, 64, f, seqs, 32,
-                                                hkv, d, 16, 100, 0.1, prefix, split, part, f, f,
+                                                hkv, d, 16, 100, scale, prefix, split, part, f, f,
                                                 f, counters, maxp, None, None)
 
     assert call(prefix=0) == pa.PA_ERR_INVALID_ARG
+    assert call(scale=0.0) == pa.PA_ERR_INVALID_ARG         # the prefill kernel: scale > 0
+    assert call(scale=-0.1) == pa.PA_ERR_INVALID_ARG
     assert call(prefix=300) == pa.PA_ERR_INVALID_ARG        # not a multiple of the split
     assert call(split=100) == pa.PA_ERR_INVALID_ARG         # not a multiple of the block
     assert call(part=100) == pa.PA_ERR_INVALID_ARG
