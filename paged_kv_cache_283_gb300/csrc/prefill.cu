@@ -82,8 +82,10 @@ constexpr int kStages = kKeys == 128 ? 3 : 2;  // K and V ring depth (chunks)
 constexpr int kK = kQ + 2 * kHalf;      // K: kStages stages x 2 halves
 constexpr int kV = kK + 2 * kStages * kKVHalf;  // V: kStages stages x 2 halves
 constexpr int kBar = kV + 2 * kStages * kKVHalf;  // mbarriers and the TMEM address slot
-constexpr int kRed = kBar + 256;        // row maxima / sums of the two column halves
-constexpr int kSmemBytes = kRed + 2 * kRows * 4 + 1024;  // + alignment slack
+// row maxima of the two column halves, double-buffered by chunk parity, then
+// the halves' final sums
+constexpr int kRed = kBar + 256;
+constexpr int kSmemBytes = kRed + 3 * 2 * kRows * 4 + 1024;  // + alignment slack
 constexpr int kSoftmaxThreads = 256;    // two threads per row, kKeys / 2 columns each
 constexpr int kThreads = kSoftmaxThreads + 96;  // + an MMA warp and two copy warps
 static_assert(kCtasPerSm * kSmemBytes <= 232448, "shared memory per SM");
@@ -250,9 +252,11 @@ __device__ __forceinline__ void pair_sync(int warp) {
 // latencies.
 //
 // Tensor memory: kSBuf S buffers of kKeys columns, then O (128 columns).  P of
-// chunk c replaces S of chunk c in place (hi part in the buffer's first
-// kKeys / 2 columns, lo part in the next, bf16 pairs packed per column); buffer
-// c % kSBuf.  K and V run in kStages-chunk rings.  Every ring slot has
+// chunk c replaces S of chunk c in place, buffer c % kSBuf: each softmax
+// thread writes its kKeys / 2 keys' weights over the kKeys / 2 columns of S it
+// read, the hi parts in the first half of them and the lo parts in the
+// second (bf16 pairs packed per column), so no thread writes a column the
+// other thread of its row still has to read.  K and V run in kStages-chunk rings.  Every ring slot has
 // its own barriers ("full": copies landed; "free": committed after the MMA
 // that read it; "pv_done": PV read the P it holds), so that each wait names
 // one use of one slot and no parity wait can match an older phase.
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // earlier chunk.
   uint64_t* p_ready = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
-  float* red = reinterpret_cast<float*>(sm + kRed);            // [2][128]
+  float* red = reinterpret_cast<float*>(sm + kRed);            // [3][2][128]
 
   if (tid == 0) {
     for (int i = 0; i < 19; ++i) mbar_init(k_full + i, 1);
@@ -493,12 +497,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (!ok) break;
         tc_fence_after();
         const uint64_t vdesc = sw128_desc(sV + 2 * st * kKVHalf, kKVHalf, 1024);
+        // keys 16 kk .. 16 kk + 15: softmax thread kk / (HK / 16) of each row
+        // wrote their hi pairs 8 (kk % (HK / 16)) columns into its HK columns
+        // of S, the lo pairs HK / 2 columns further
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
-          umma_bf16_ts(tmem + kTO, tmem + sb * kKeys + 8 * kk, vdesc + kk * (2048 >> 4),
-                       kIdescPV, (c > 0 || kk > 0) ? 1u : 0u);
-          umma_bf16_ts(tmem + kTO, tmem + sb * kKeys + kKeys / 2 + 8 * kk,
-                       vdesc + kk * (2048 >> 4), kIdescPV, 1u);
+          const uint32_t hi = sb * kKeys + HK * (kk / (HK / 16)) + 8 * (kk % (HK / 16));
+          umma_bf16_ts(tmem + kTO, tmem + hi, vdesc + kk * (2048 >> 4), kIdescPV,
+                       (c > 0 || kk > 0) ? 1u : 0u);
+          umma_bf16_ts(tmem + kTO, tmem + hi + HK / 2, vdesc + kk * (2048 >> 4), kIdescPV, 1u);
         }
         umma_commit(&pv_done[sb]);
         umma_commit(&v_free[st]);
@@ -560,13 +567,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
         mx = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
       }
-      // the row's maximum over both halves (warps w and w + 4); the second
-      // barrier also orders both halves' reads of S before the writes of P
+      // the row's maximum over both halves (warps w and w + 4), through a
+      // buffer of this chunk's parity: the partner's read of the same buffer
+      // two chunks ago came before its arrival on the last barrier, which this
+      // thread has passed
+      float* redc = red + (c & 1) * 2 * kRows;
       tc_fence_before();
-      red[hcol * kRows + r] = mx;
+      redc[hcol * kRows + r] = mx;
       pair_sync(warp);
-      mx = fmaxf(red[r], red[kRows + r]) * sl2;
-      pair_sync(warp);
+      mx = fmaxf(redc[r], redc[kRows + r]) * sl2;
       tc_fence_after();
       float alpha = 1.f;
       if (lok) {
@@ -578,6 +587,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             m_used = mx;
           }
         }
+        // no reference yet: every score of the row so far is masked (-inf),
+        // and with the offset 0 its weights come out exp2(-inf) = 0
         const bool live = m_used != -INFINITY;
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 neg2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
@@ -587,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int j = 0; j < HK; j += 2) {
           const float2 x = __ffma2_rn(
               make_float2(__uint_as_float(sv[j]), __uint_as_float(sv[j + 1])), sl2x2, neg2);
-          const float2 e = live ? make_float2(ex2(x.x), ex2(x.y)) : make_float2(0.f, 0.f);
+          const float2 e = make_float2(ex2(x.x), ex2(x.y));
           ps4[(j >> 1) & 3] = __fadd2_rn(ps4[(j >> 1) & 3], e);
           sv[j] = __float_as_uint(e.x);
           sv[j + 1] = __float_as_uint(e.y);
@@ -631,9 +642,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const __nv_bfloat162 lo = __floats2bfloat162_rn(r2.x, r2.y);
             wl[k] = *reinterpret_cast<const uint32_t*>(&lo);
           }
-          // hi pairs in the buffer's first kKeys / 2 columns, lo pairs in the next
-          tmem_st16(tmem + lane_base + sb * kKeys + (HK / 2) * hcol + 16 * q2, wh);
-          tmem_st16(tmem + lane_base + sb * kKeys + kKeys / 2 + (HK / 2) * hcol + 16 * q2, wl);
+          // over this thread's own S columns: hi pairs in the first half, lo
+          // pairs in the second
+          tmem_st16(tmem + lane_base + sb * kKeys + HK * hcol + 16 * q2, wh);
+          tmem_st16(tmem + lane_base + sb * kKeys + HK * hcol + HK / 2 + 16 * q2, wl);
         }
         tmem_wait_st();
       }
@@ -664,12 +676,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool lok = ok && mbar_wait_bounded(&pv_done[(nchunks - 1) % kSBuf],
                                        ((nchunks - 1) / kSBuf) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
-    red[hcol * kRows + r] = l_sum;
+    float* reds = red + 4 * kRows;  // not a buffer the loop's last reads may still use
+    reds[hcol * kRows + r] = l_sum;
     asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
     if (lok && shared_prefix) {
       // the row's partial: o / l, and (m, l) with m in natural-log units
       tc_fence_after();
-      const float lt = red[r] + red[kRows + r];
+      const float lt = reds[r] + reds[kRows + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const size_t wrow =
           (static_cast<size_t>(row_ok ? qi : 0) * p.num_q_heads + kvh * G + r % G) *
@@ -694,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     } else if (lok) {
       tc_fence_after();
-      const float lt = red[r] + red[kRows + r];
+      const float lt = reds[r] + reds[kRows + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       __nv_bfloat16* orow = p.out +
                             (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads +
