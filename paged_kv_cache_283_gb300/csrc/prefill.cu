@@ -27,10 +27,13 @@
 //    softmax; at 128 keys: 3 stages of 32 KiB, 3 S buffers, all 512 columns,
 //    one CTA per SM.
 //  * The online softmax reads its row of S from tensor memory (two threads per
-//    row = TMEM lane, kKeys / 2 columns each, maxima and sums combined through shared
-//    memory), masks causally, keeps a running maximum that is only raised
-//    when it grows by more than 2^8 (then O's row is rescaled in tensor
-//    memory), and writes P back into tensor memory, over its own S, as two
+//    row = TMEM lane, kKeys / 2 columns each, flags, maxima and sums combined
+//    through shared memory), masks causally, keeps a reference maximum that
+//    is only raised when the row grows past it by more than 2^8 (then O's row
+//    is rescaled in tensor memory) -- so a chunk's weights are taken against
+//    the reference first, and only a chunk whose weights could exceed 2^8
+//    (a half-row sum above 2^7) takes its maxima and redoes them -- and
+//    writes P back into tensor memory, over its own S, as two
 //    bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), each multiplied with V
 //    by its own MMA reading A from tensor memory: the weights keep ~17 bits
 //    instead of bf16's 8 (a single bf16 P puts elementwise errors of several
@@ -82,10 +85,11 @@ constexpr int kStages = kKeys == 128 ? 3 : 2;  // K and V ring depth (chunks)
 constexpr int kK = kQ + 2 * kHalf;      // K: kStages stages x 2 halves
 constexpr int kV = kK + 2 * kStages * kKVHalf;  // V: kStages stages x 2 halves
 constexpr int kBar = kV + 2 * kStages * kKVHalf;  // mbarriers and the TMEM address slot
-// row maxima of the two column halves, double-buffered by chunk parity, then
-// the halves' final sums
+// per row and column half: the flags "this chunk may move the reference",
+// double-buffered by chunk parity; the final sums; the maxima of a chunk that
+// may move it
 constexpr int kRed = kBar + 256;
-constexpr int kSmemBytes = kRed + 3 * 2 * kRows * 4 + 1024;  // + alignment slack
+constexpr int kSmemBytes = kRed + 4 * 2 * kRows * 4 + 1024;  // + alignment slack
 constexpr int kSoftmaxThreads = 256;    // two threads per row, kKeys / 2 columns each
 constexpr int kThreads = kSoftmaxThreads + 96;  // + an MMA warp and two copy warps
 static_assert(kCtasPerSm * kSmemBytes <= 232448, "shared memory per SM");
@@ -266,9 +270,11 @@ __device__ __forceinline__ void pair_sync(int warp) {
 //   V(c) and P(c): O += P V(c).
 // Copy warps, per chunk c: wait K slot of c free: copy K(c+kStages) (K warp);
 //   wait V slot of c-1 free: copy V(c+kStages-1) (V warp).
-// Softmax warps, per chunk c: wait S(c); read it; row maxima (pair of warps);
-//   exponentials; rescale O only if the reference maximum moved (after
-//   PV(c-1)); P into S[c%3]; arrive on p_ready[c%3].
+// Softmax warps, per chunk c: wait S(c); read it; exponentials against the
+//   reference; flags "may move the reference" (pair of warps); only if a row
+//   of the warp is flagged: read S again, row maxima (pair of warps), move
+//   the reference, exponentials again; rescale O only if the reference moved
+//   (after PV(c-1)); P into S[c%kSBuf]; arrive on p_ready[c%kSBuf].
 // No softmax thread leaves the loop early (the pair barriers must stay
 // matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // earlier chunk.
   uint64_t* p_ready = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
-  float* red = reinterpret_cast<float*>(sm + kRed);            // [3][2][128]
+  float* red = reinterpret_cast<float*>(sm + kRed);            // [4][2][128]
 
   if (tid == 0) {
     for (int i = 0; i < 19; ++i) mbar_init(k_full + i, 1);
@@ -548,49 +554,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         tmem_wait_ld();
       }
-      // causal mask and this half's maximum
-      float mx = -INFINITY;
-      if (lok) {
-        const int lim = row_ok ? pos - c * kKeys - HK * hcol : -1;  // visible: j <= lim
-        if (!__all_sync(kFullMask, lim >= HK - 1)) {
+      // causal mask
+      const int lim = row_ok ? pos - c * kKeys - HK * hcol : -1;  // visible: j <= lim
+      const bool masked = !__all_sync(kFullMask, lim >= HK - 1);
+      if (lok && masked) {
 #pragma unroll
-          for (int j = 0; j < HK; ++j)
-            if (j > lim) sv[j] = __float_as_uint(-INFINITY);
-        }
-        // eight independent partial maxima (max is exact in any order)
-        float m8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sv[k]);
-#pragma unroll
-        for (int j = 8; j < HK; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
-        mx = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
+        for (int j = 0; j < HK; ++j)
+          if (j > lim) sv[j] = __float_as_uint(-INFINITY);
       }
-      // the row's maximum over both halves (warps w and w + 4), through a
-      // buffer of this chunk's parity: the partner's read of the same buffer
-      // two chunks ago came before its arrival on the last barrier, which this
-      // thread has passed
-      float* redc = red + (c & 1) * 2 * kRows;
-      tc_fence_before();
-      redc[hcol * kRows + r] = mx;
-      pair_sync(warp);
-      mx = fmaxf(redc[r], redc[kRows + r]) * sl2;
-      tc_fence_after();
-      float alpha = 1.f;
-      if (lok) {
-        if (mx != -INFINITY) {
-          if (m_used == -INFINITY) {
-            m_used = mx;
-          } else if (mx > m_used + 8.f) {
-            alpha = ex2(m_used - mx);
-            m_used = mx;
-          }
-        }
-        // no reference yet: every score of the row so far is masked (-inf),
-        // and with the offset 0 its weights come out exp2(-inf) = 0
+      // The weights against the current reference (none yet: offset 0, and a
+      // row without a reference has only masked scores so far, which give
+      // exp2(-inf) = 0).  The reference moves only when the chunk's maximum
+      // exceeds it by more than 2^8, which makes a weight above 2^8 and so
+      // this half's sum above 2^7: only then (or with no reference yet) are
+      // the chunk's maxima taken, the scores read again and the weights redone.
+      const float2 sl2x2 = make_float2(sl2, sl2);
+      float psum = 0.f;
+      auto weights = [&]() {
         const bool live = m_used != -INFINITY;
-        const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 neg2 = make_float2(live ? -m_used : 0.f, live ? -m_used : 0.f);
         float2 ps4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                          make_float2(0.f, 0.f)};  // independent partial sums
@@ -604,7 +585,71 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           sv[j + 1] = __float_as_uint(e.y);
         }
         const float2 pa = __fadd2_rn(__fadd2_rn(ps4[0], ps4[2]), __fadd2_rn(ps4[1], ps4[3]));
-        l_sum = l_sum * alpha + (pa.x + pa.y);
+        psum = pa.x + pa.y;
+      };
+      // (a row of the tile without a reference yet takes the maxima anyway:
+      // its weights wait for them; a row past the chunk's queries has only
+      // masked scores, weights 0)
+      if (lok && (m_used != -INFINITY || !row_ok)) weights();
+      const bool want = lok && row_ok && (m_used == -INFINITY || !(psum <= 128.f));
+      // both halves' flags (warps w and w + 4), through a buffer of this
+      // chunk's parity: the partner's read of the same buffer two chunks ago
+      // came before its arrival on the last barrier, which this thread has
+      // passed
+      float* redc = red + (c & 1) * 2 * kRows;
+      tc_fence_before();
+      redc[hcol * kRows + r] = want ? 1.f : 0.f;
+      pair_sync(warp);
+      const bool row_want = redc[r] != 0.f || redc[kRows + r] != 0.f;
+      tc_fence_after();
+      float alpha = 1.f;
+      // the same decision in both warps of the pair (the same 32 rows)
+      if (__any_sync(kFullMask, row_want)) {
+        float mx = -INFINITY;
+        if (lok) {
+#pragma unroll
+          for (int q4 = 0; q4 < HK / 32; ++q4) {
+            uint32_t(&chunk)[32] = *reinterpret_cast<uint32_t(*)[32]>(sv + 32 * q4);
+            tmem_ld32(tmem + lane_base + sb * kKeys + HK * hcol + 32 * q4, chunk);
+          }
+          tmem_wait_ld();
+          if (masked) {
+#pragma unroll
+            for (int j = 0; j < HK; ++j)
+              if (j > lim) sv[j] = __float_as_uint(-INFINITY);
+          }
+          // eight independent partial maxima (max is exact in any order)
+          float m8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m8[k] = __uint_as_float(sv[k]);
+#pragma unroll
+          for (int j = 8; j < HK; ++j) m8[j & 7] = fmaxf(m8[j & 7], __uint_as_float(sv[j]));
+#pragma unroll
+          for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+          mx = fmaxf(fmaxf(m8[0], m8[2]), fmaxf(m8[1], m8[3]));
+        }
+        // the row's maximum over both halves; this buffer's previous reads
+        // came before both threads' arrivals on this chunk's first barrier
+        float* redm = red + 6 * kRows;
+        tc_fence_before();
+        redm[hcol * kRows + r] = mx;
+        pair_sync(warp);
+        mx = fmaxf(redm[r], redm[kRows + r]) * sl2;
+        tc_fence_after();
+        if (lok) {
+          if (mx != -INFINITY) {
+            if (m_used == -INFINITY) {
+              m_used = mx;
+            } else if (mx > m_used + 8.f) {
+              alpha = ex2(m_used - mx);
+              m_used = mx;
+            }
+          }
+          weights();  // the scores were read again: weights against the reference
+        }
+      }
+      if (lok) {
+        l_sum = l_sum * alpha + psum;
         // rescale this half of O's row when the reference maximum moved; PV(c-1)
         // (and so every earlier PV) must be done with O first (c == 0: the
         // first PV overwrites O)
