@@ -26,14 +26,15 @@
 //    columns, so two CTAs share an SM and one's MMAs overlap the other's
 //    softmax; at 128 keys: 3 stages of 32 KiB, 3 S buffers, all 512 columns,
 //    one CTA per SM.
-//  * The online softmax reads its row of S from tensor memory (two threads per
-//    row = TMEM lane, kKeys / 2 columns each, flags, maxima and sums combined
-//    through shared memory), masks causally, keeps a reference maximum that
-//    is only raised when the row grows past it by more than 2^8 (then O's row
-//    is rescaled in tensor memory) -- so a chunk's weights are taken against
-//    the reference first, and only a chunk whose weights could exceed 2^8
-//    (a half-row sum above 2^7) takes its maxima and redoes them -- and
-//    writes P back into tensor memory, over its own S, as two
+//  * The online softmax reads its row of S from tensor memory (one thread
+//    per row = TMEM lane, four softmax warps, by default; or two threads per
+//    row with flags, maxima and sums combined through shared memory), masks
+//    causally, keeps a reference maximum that is only raised when the row
+//    grows past it by more than 2^8 (then O's row is rescaled in tensor
+//    memory) -- so a chunk's weights are taken against the reference first,
+//    and only a chunk whose weights could exceed 2^8 (a sum of the thread's
+//    weights above 2^7) takes its maxima and redoes them -- and writes P
+//    back into tensor memory, over its own S, as two
 //    bf16 parts, hi = p truncated to bf16 and lo = bf16(p - hi), each multiplied with V
 //    by its own MMA reading A from tensor memory: the weights keep ~17 bits
 //    instead of bf16's 8 (a single bf16 P puts elementwise errors of several
@@ -85,12 +86,22 @@ constexpr int kStages = kKeys == 128 ? 3 : 2;  // K and V ring depth (chunks)
 constexpr int kK = kQ + 2 * kHalf;      // K: kStages stages x 2 halves
 constexpr int kV = kK + 2 * kStages * kKVHalf;  // V: kStages stages x 2 halves
 constexpr int kBar = kV + 2 * kStages * kKVHalf;  // mbarriers and the TMEM address slot
-// per row and column half: the flags "this chunk may move the reference",
-// double-buffered by chunk parity; the final sums; the maxima of a chunk that
-// may move it
+// Softmax threads per row of S (TMEM lane): 1 (all kKeys columns), or 2
+// (kKeys / 2 columns each, the two warps of a lane quarter exchanging through
+// shared memory; measured slower: 806 against 842 TFLOP/s on the 16 x 512
+// step at 64 keys).
+#ifndef PA_PREFILL_ROW_THREADS
+#define PA_PREFILL_ROW_THREADS 1
+#endif
+constexpr int kRowThreads = PA_PREFILL_ROW_THREADS;
+static_assert(kRowThreads == 1 || kRowThreads == 2, "softmax threads per row");
+constexpr int kSoftmaxThreads = 128 * kRowThreads;
+constexpr int kOCols = kD / kRowThreads;  // columns of O per softmax thread
+// Two threads per row exchange, per row and column half: the flags "this
+// chunk may move the reference", double-buffered by chunk parity; the final
+// sums; the maxima of a chunk that may move it.
 constexpr int kRed = kBar + 256;
-constexpr int kSmemBytes = kRed + 4 * 2 * kRows * 4 + 1024;  // + alignment slack
-constexpr int kSoftmaxThreads = 256;    // two threads per row, kKeys / 2 columns each
+constexpr int kSmemBytes = kRed + (kRowThreads == 2 ? 4 * 2 * kRows * 4 : 0) + 1024;  // + slack
 constexpr int kThreads = kSoftmaxThreads + 96;  // + an MMA warp and two copy warps
 static_assert(kCtasPerSm * kSmemBytes <= 232448, "shared memory per SM");
 
@@ -247,13 +258,13 @@ __device__ __forceinline__ void pair_sync(int warp) {
   asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
 }
 
-// grid (query tiles, KV heads, sequences), 352 threads.  Warps 0-7 run the
-// softmax: thread t < 256 handles row t % 128 (TMEM lane; warps w and w + 4
-// share a lane quarter), columns [h kKeys / 2, (h + 1) kKeys / 2) of S and
-// [64 h, 64 h + 64) of O, h = t / 128.
-// Warp 8 issues the MMAs (lane 0), warp 9 the Q and K copies and warp 10 the
-// V copies (one block per lane), so that no chain waits on another's
-// latencies.
+// grid (query tiles, KV heads, sequences), kThreads threads.  The first
+// kSoftmaxThreads run the softmax: thread t handles row t % 128 (TMEM lane;
+// with two threads per row, warps w and w + 4 share a lane quarter), columns
+// [h HK, (h + 1) HK) of S and [h kOCols, (h + 1) kOCols) of O, h = t / 128.
+// The next warp issues the MMAs (lane 0), the one after it the Q and K
+// copies and the last the V copies (one block per lane), so that no chain
+// waits on another's latencies.
 //
 // Tensor memory: kSBuf S buffers of kKeys columns, then O (128 columns).  P of
 // chunk c replaces S of chunk c in place, buffer c % kSBuf: each softmax
@@ -283,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                          const __grid_constant__ CUtensorMap tk,
                          const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
   constexpr int TQ = kRows / G;  // query tokens per CTA
-  constexpr int HK = kKeys / 2;  // columns per softmax thread
+  constexpr int HK = kKeys / kRowThreads;  // columns of S per softmax thread
   constexpr int kMmaWarp = kSoftmaxThreads / 32, kCopyWarp = kMmaWarp + 1;
   griddep_wait();
   griddep_launch_dependents();
@@ -529,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ------------------------------------------------------------ softmax
     const int hcol = tid >> 7;  // column half
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tO = tmem + lane_base + kTO + 64 * hcol;
+    const uint32_t tO = tmem + lane_base + kTO + kOCols * hcol;
     const int r = tid & (kRows - 1);  // row: token r / G of the tile, head r % G
     const int qi = i0 + r / G;
     const bool row_ok = qi < n;
@@ -566,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // row without a reference has only masked scores so far, which give
       // exp2(-inf) = 0).  The reference moves only when the chunk's maximum
       // exceeds it by more than 2^8, which makes a weight above 2^8 and so
-      // this half's sum above 2^7: only then (or with no reference yet) are
+      // this thread's sum above 2^7: only then (or with no reference yet) are
       // the chunk's maxima taken, the scores read again and the weights redone.
       const float2 sl2x2 = make_float2(sl2, sl2);
       float psum = 0.f;
@@ -592,18 +603,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // masked scores, weights 0)
       if (lok && (m_used != -INFINITY || !row_ok)) weights();
       const bool want = lok && row_ok && (m_used == -INFINITY || !(psum <= 128.f));
-      // both halves' flags (warps w and w + 4), through a buffer of this
-      // chunk's parity: the partner's read of the same buffer two chunks ago
-      // came before its arrival on the last barrier, which this thread has
-      // passed
-      float* redc = red + (c & 1) * 2 * kRows;
-      tc_fence_before();
-      redc[hcol * kRows + r] = want ? 1.f : 0.f;
-      pair_sync(warp);
-      const bool row_want = redc[r] != 0.f || redc[kRows + r] != 0.f;
-      tc_fence_after();
+      // with two threads per row, both halves' flags (warps w and w + 4),
+      // through a buffer of this chunk's parity: the partner's read of the
+      // same buffer two chunks ago came before its arrival on the last
+      // barrier, which this thread has passed
+      bool row_want = want;
+      if constexpr (kRowThreads == 2) {
+        float* redc = red + (c & 1) * 2 * kRows;
+        tc_fence_before();
+        redc[hcol * kRows + r] = want ? 1.f : 0.f;
+        pair_sync(warp);
+        row_want = redc[r] != 0.f || redc[kRows + r] != 0.f;
+        tc_fence_after();
+      }
       float alpha = 1.f;
-      // the same decision in both warps of the pair (the same 32 rows)
+      // warp-uniform (the tensor-memory loads are warp-wide; with two threads
+      // per row the same decision in both warps of the pair: the same rows)
       if (__any_sync(kFullMask, row_want)) {
         float mx = -INFINITY;
         if (lok) {
@@ -630,12 +645,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         // the row's maximum over both halves; this buffer's previous reads
         // came before both threads' arrivals on this chunk's first barrier
-        float* redm = red + 6 * kRows;
-        tc_fence_before();
-        redm[hcol * kRows + r] = mx;
-        pair_sync(warp);
-        mx = fmaxf(redm[r], redm[kRows + r]) * sl2;
-        tc_fence_after();
+        if constexpr (kRowThreads == 2) {
+          float* redm = red + 6 * kRows;
+          tc_fence_before();
+          redm[hcol * kRows + r] = mx;
+          pair_sync(warp);
+          mx = fmaxf(redm[r], redm[kRows + r]);
+          tc_fence_after();
+        }
+        mx *= sl2;
         if (lok) {
           if (mx != -INFINITY) {
             if (m_used == -INFINITY) {
@@ -659,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (lok) {
             tc_fence_after();
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
+            for (int q4 = 0; q4 < kOCols / 16; ++q4) {
               uint32_t o[16];
               tmem_ld16(tO + 16 * q4, o);
               tmem_wait_ld();
@@ -703,9 +721,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         lok = mbar_wait_bounded(&v_full[st], (c / kStages) & 1, p.err);
         if (lok && r >= vk && r < kKeys) {
           const uint4 z = make_uint4(0, 0, 0, 0);
-          uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hcol) * kKVHalf + prow);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) row[k] = z;
+          for (int hh = hcol; hh < 2; hh += kRowThreads) {  // the 64-column halves
+            uint4* row = reinterpret_cast<uint4*>(sm + kV + (2 * st + hh) * kKVHalf + prow);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) row[k] = z;
+          }
         }
       }
       ok = lok;
@@ -721,20 +742,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     bool lok = ok && mbar_wait_bounded(&pv_done[(nchunks - 1) % kSBuf],
                                        ((nchunks - 1) / kSBuf) & 1, p.err);
     lok = __all_sync(kFullMask, lok);
-    float* reds = red + 4 * kRows;  // not a buffer the loop's last reads may still use
-    reds[hcol * kRows + r] = l_sum;
-    asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
+    float lt = l_sum;
+    if constexpr (kRowThreads == 2) {
+      float* reds = red + 4 * kRows;  // not a buffer the loop's last reads may still use
+      reds[hcol * kRows + r] = l_sum;
+      asm volatile("bar.sync 5, %0;" ::"n"(kSoftmaxThreads) : "memory");
+      lt = reds[r] + reds[kRows + r];
+    }
     if (lok && shared_prefix) {
       // the row's partial: o / l, and (m, l) with m in natural-log units
       tc_fence_after();
-      const float lt = reds[r] + reds[kRows + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       const size_t wrow =
           (static_cast<size_t>(row_ok ? qi : 0) * p.num_q_heads + kvh * G + r % G) *
               p.max_partitions + split;
-      float* orow = p.ws_o + wrow * kD + 64 * hcol;
+      float* orow = p.ws_o + wrow * kD + kOCols * hcol;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kOCols / 16; ++q4) {
         uint32_t o[16];
         tmem_ld16(tO + 16 * q4, o);
         tmem_wait_ld();
@@ -752,13 +776,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
     } else if (lok) {
       tc_fence_after();
-      const float lt = reds[r] + reds[kRows + r];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
       __nv_bfloat16* orow = p.out +
                             (static_cast<size_t>(q0 + (row_ok ? qi : 0)) * p.num_q_heads +
-                             kvh * G + r % G) * kD + 64 * hcol;
+                             kvh * G + r % G) * kD + kOCols * hcol;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
+      for (int q4 = 0; q4 < kOCols / 16; ++q4) {
         uint32_t o[16];
         tmem_ld16(tO + 16 * q4, o);
         tmem_wait_ld();
