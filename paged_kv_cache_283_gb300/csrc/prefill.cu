@@ -268,13 +268,14 @@ __device__ __forceinline__ void pair_sync(int warp) {
 //
 // Tensor memory: kSBuf S buffers of kKeys columns, then O (128 columns).  P of
 // chunk c replaces S of chunk c in place, buffer c % kSBuf: each softmax
-// thread writes its kKeys / 2 keys' weights over the kKeys / 2 columns of S it
-// read, the hi parts in the first half of them and the lo parts in the
-// second (bf16 pairs packed per column), so no thread writes a column the
-// other thread of its row still has to read.  K and V run in kStages-chunk rings.  Every ring slot has
-// its own barriers ("full": copies landed; "free": committed after the MMA
-// that read it; "pv_done": PV read the P it holds), so that each wait names
-// one use of one slot and no parity wait can match an older phase.
+// thread writes its HK keys' weights over the HK columns of S it read, the hi
+// parts in the first half of them and the lo parts in the second (bf16 pairs
+// packed per column), so with two threads per row neither writes a column
+// the other still has to read.  K and V run in kStages-chunk rings.  Every
+// ring slot has its own barriers ("full": copies landed; "free": committed
+// after the MMA that read it; "pv_done": PV read the P it holds), so that
+// each wait names one use of one slot and no parity wait can match an older
+// phase.
 //
 // MMA warp, per chunk c (A = kAhead = kSBuf - 1): wait PV(c-1) (its buffer
 //   S[(c+A)%kSBuf] held P(c-1)) and K(c+A): S[(c+A)%kSBuf] = Q K(c+A)^T; wait
@@ -282,10 +283,11 @@ __device__ __forceinline__ void pair_sync(int warp) {
 // Copy warps, per chunk c: wait K slot of c free: copy K(c+kStages) (K warp);
 //   wait V slot of c-1 free: copy V(c+kStages-1) (V warp).
 // Softmax warps, per chunk c: wait S(c); read it; exponentials against the
-//   reference; flags "may move the reference" (pair of warps); only if a row
-//   of the warp is flagged: read S again, row maxima (pair of warps), move
-//   the reference, exponentials again; rescale O only if the reference moved
-//   (after PV(c-1)); P into S[c%kSBuf]; arrive on p_ready[c%kSBuf].
+//   reference; flags "may move the reference" (with two threads per row,
+//   combined by the pair of warps); only if a row of the warp is flagged:
+//   read S again, row maxima, move the reference, exponentials again;
+//   rescale O only if the reference moved (after PV(c-1)); P into
+//   S[c%kSBuf]; arrive on p_ready[c%kSBuf].
 // No softmax thread leaves the loop early (the pair barriers must stay
 // matched): one whose wait timed out keeps iterating without waiting or working.
 template <int G>
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // earlier chunk.
   uint64_t* p_ready = k_full + 19;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kBar + 240);
-  float* red = reinterpret_cast<float*>(sm + kRed);            // [4][2][128]
+  float* red = reinterpret_cast<float*>(sm + kRed);  // [4][2][128], two threads per row
 
   if (tid == 0) {
     for (int i = 0; i < 19; ++i) mbar_init(k_full + i, 1);
@@ -599,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         psum = pa.x + pa.y;
       };
       // (a row of the tile without a reference yet takes the maxima anyway:
-      // its weights wait for them; a row past the chunk's queries has only
+      // its weights wait for them; a row past the tile's queries has only
       // masked scores, weights 0)
       if (lok && (m_used != -INFINITY || !row_ok)) weights();
       const bool want = lok && row_ok && (m_used == -INFINITY || !(psum <= 128.f));
