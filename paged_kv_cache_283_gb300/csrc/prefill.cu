@@ -9,7 +9,7 @@
 // keys 0 .. p through the block table ("PagedAttention: Virtual Memory for
 // the KV Cache").  n = 1 is a decode step.
 //
-// Design (one CTA per 128 query rows: 8 softmax warps, an MMA warp, two copy
+// Design (one CTA per 128 query rows: 4 softmax warps, an MMA warp, two copy
 // warps; two CTAs per SM):
 //  * Rows are (token, head) pairs of one GQA group: 128 / G tokens x G heads,
 //    so each K/V tile loaded serves the whole group.  Q arrives by one 3-D TMA
